@@ -1,0 +1,290 @@
+"""CPU oracle of the fused MoE router: plain, slow, float64.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import or call
+this module; only the test suite, the smoke check and the CPU-baseline leg of
+the benchmark use it.  It shares no code with the CUDA library: it takes
+float64 copies of the same inputs and recomputes every result from the
+definitions, one token row at a time, with a full sort per row.
+
+Sources (titles of the pages the method is read from):
+
+* [TE]  NVIDIA TransformerEngine PR #3012, "[Common] Optimize fused router
+  forward/backward kernels": Summary (the two fused ops), Changes/Hardening
+  (argument rules), Performance (which tensors the forward reads and writes:
+  logits, probs, routing_map and the fp32 intermediate output), the two full
+  benchmark tables (softmax and sigmoid score functions), and the review
+  summary (the backward's gradient across score function x pre-softmax).
+* [ORT] microsoft/onnxruntime PR #33366, "[CUDA] Add fused decode routing,
+  single-pass finalize, and PDL overlap for NVFP4 QMoE": Description item 1
+  (softmax + top-k per row, one row per warp) and the review's parity request
+  (tied logits).
+
+Readings where the pages are silent (each one is also listed in the design
+notes):
+
+* softmax is taken over all E experts before the top-K choice (the
+  pre-softmax order) and the selected probabilities are not renormalised;
+* sigmoid probabilities are renormalised over the K selected experts with the
+  unbiased scores: p_i = c * s_i / sum_sel s_j, with no epsilon;
+* the selection key is s_i + b_i (b = optional per-expert bias, selection
+  only); ties go to the lower expert index, and -0.0 equals +0.0;
+* group-limited selection: E splits into num_groups contiguous groups; a
+  group's score is the sum of its K/group_topk largest keys; the group_topk
+  best groups survive (ties to the lower group index); the top-K is then taken
+  over the surviving experts.  num_groups = 0 means no grouping; the oracle
+  runs the general grouped algorithm for every num_groups >= 1;
+* the aux-loss score is q = softmax(x) for softmax and q = sigmoid(x) /
+  sum_E sigmoid(x) for sigmoid; its routing map is the top-K of q with the same
+  tie rule, without bias, groups or scaling; the sigmoid variant also saves
+  sigmoid(x) for its backward.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SOFTMAX = "softmax"
+SIGMOID = "sigmoid"
+
+# A row is a near tie when the keys on either side of its top-K boundary are
+# distinct but within this relative distance of each other.
+NEAR_TIE_REL = 1e-6
+
+
+# --------------------------------------------------------------------------
+# score function  [TE] Summary; the two benchmark tables (softmax, sigmoid)
+# --------------------------------------------------------------------------
+def score_row(x: np.ndarray, score_func: str) -> np.ndarray:
+    """Per-expert score of one token row, in float64.
+
+    softmax: s_i = exp(x_i - max x) / sum_j exp(x_j - max x) over all E.
+    sigmoid: s_i = 1 / (1 + exp(-x_i)).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if score_func == SOFTMAX:
+        e = np.exp(x - x.max())
+        return e / e.sum()
+    if score_func == SIGMOID:
+        return 1.0 / (1.0 + np.exp(-x))
+    raise ValueError(score_func)
+
+
+# --------------------------------------------------------------------------
+# ordering with the lower-index tie rule  [ORT] review: tied logits
+# --------------------------------------------------------------------------
+def order_desc(keys: np.ndarray) -> np.ndarray:
+    """Indices of ``keys`` sorted by (key descending, index ascending).
+
+    A stable sort of the negated keys keeps equal keys in ascending index
+    order; the comparison is numeric, so -0.0 and +0.0 are equal.
+    """
+    return np.argsort(-np.asarray(keys, dtype=np.float64), kind="stable")
+
+
+def group_scores(keys: np.ndarray, num_groups: int, per_group: int) -> np.ndarray:
+    """Score of each contiguous expert group: the sum of its ``per_group``
+    largest keys (a full sort of each group)."""
+    E = keys.size
+    eg = E // num_groups
+    out = np.empty(num_groups, dtype=np.float64)
+    for g in range(num_groups):
+        kg = keys[g * eg:(g + 1) * eg]
+        out[g] = kg[order_desc(kg)[:per_group]].sum()
+    return out
+
+
+def selectable_experts(keys: np.ndarray, K: int, num_groups: int,
+                       group_topk: int) -> tuple[np.ndarray, np.ndarray | None]:
+    """Experts the top-K may choose from, after group-limited pre-selection.
+
+    Returns (boolean mask over E, group scores or None).  [TE] Hardening:
+    K must be a multiple of group_topk.
+    """
+    E = keys.size
+    if num_groups <= 0:
+        return np.ones(E, dtype=bool), None
+    per_group = K // group_topk
+    gs = group_scores(keys, num_groups, per_group)
+    kept = order_desc(gs)[:group_topk]
+    eg = E // num_groups
+    mask = np.zeros(E, dtype=bool)
+    for g in kept:
+        mask[g * eg:(g + 1) * eg] = True
+    return mask, gs
+
+
+def _near(a: float, b: float) -> bool:
+    d = abs(a - b)
+    return 0.0 < d <= NEAR_TIE_REL * max(abs(a), abs(b))
+
+
+# --------------------------------------------------------------------------
+# router top-K forward  [TE] Summary, Performance
+# --------------------------------------------------------------------------
+def topk_fwd_row(x, K, score_func, num_groups=0, group_topk=0,
+                 scaling_factor=1.0, expert_bias=None):
+    """One token row of the top-K router forward.
+
+    Returns (probs, routing_map, scores, near_tie) with probs and scores in
+    float64 (not yet rounded to the output dtype).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    E = x.size
+    s = score_row(x, score_func)                                   # step 1
+    b = (np.zeros(E) if expert_bias is None
+         else np.asarray(expert_bias, dtype=np.float64))
+    key = s + b                                                    # step 2
+    allowed, gs = selectable_experts(key, K, num_groups, group_topk)  # step 3
+    cand = np.nonzero(allowed)[0]
+    order = cand[order_desc(key[cand])]                            # step 4
+    sel = order[:K]
+    m = np.zeros(E, dtype=bool)
+    m[sel] = True
+
+    if score_func == SOFTMAX:                                      # step 5
+        probs = np.where(m, scaling_factor * s, 0.0)
+    else:
+        probs = np.where(m, scaling_factor * s / s[sel].sum(), 0.0)
+
+    near = False
+    if K < order.size:
+        near = _near(key[order[K - 1]], key[order[K]])
+    if gs is not None and group_topk < num_groups:
+        go = order_desc(gs)
+        near = near or _near(gs[go[group_topk - 1]], gs[go[group_topk]])
+    return probs, m, s, near
+
+
+def topk_fwd(logits, K, score_func=SOFTMAX, num_groups=0, group_topk=0,
+             scaling_factor=1.0, expert_bias=None):
+    """Router top-K forward over all rows of ``logits`` [T, E].
+
+    Returns a dict: probs [T,E] f64, routing_map [T,E] bool, scores [T,E] f64,
+    near_tie [T] bool.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    T, E = logits.shape
+    probs = np.zeros((T, E))
+    rmap = np.zeros((T, E), dtype=bool)
+    scores = np.zeros((T, E))
+    near = np.zeros(T, dtype=bool)
+    for t in range(T):
+        probs[t], rmap[t], scores[t], near[t] = topk_fwd_row(
+            logits[t], K, score_func, num_groups, group_topk, scaling_factor,
+            expert_bias)
+    return dict(probs=probs, routing_map=rmap, scores=scores, near_tie=near)
+
+
+# --------------------------------------------------------------------------
+# router top-K backward  [TE] Backward kernels (two passes: row sums, then
+# per-element gradients); review summary (gradient per score function)
+# --------------------------------------------------------------------------
+def topk_bwd_row(g, m, s, score_func, scaling_factor=1.0):
+    """grad_logits of one row, from grad_probs g, the routing map m and the
+    saved scores s.  The selection and the bias carry no gradient.
+
+    softmax (p = c m s):       D = c sum_j m_j g_j s_j,  gx_j = s_j (c m_j g_j - D)
+    sigmoid (p = c m s / S):   S = sum_j m_j s_j,  D = sum_j m_j g_j s_j,
+                               gx_j = m_j (c / S) (g_j - D / S) s_j (1 - s_j)
+    """
+    g = np.asarray(g, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    m = np.asarray(m, dtype=bool).astype(np.float64)
+    c = float(scaling_factor)
+    if score_func == SOFTMAX:
+        D = c * np.sum(m * g * s)              # pass 1
+        return s * (c * m * g - D)             # pass 2
+    if score_func == SIGMOID:
+        S = np.sum(m * s)                      # pass 1
+        D = np.sum(m * g * s)
+        return m * (c / S) * (g - D / S) * s * (1.0 - s)   # pass 2
+    raise ValueError(score_func)
+
+
+def topk_bwd(grad_probs, routing_map, scores, score_func=SOFTMAX, scaling_factor=1.0):
+    grad_probs = np.asarray(grad_probs, dtype=np.float64)
+    out = np.zeros_like(grad_probs)
+    for t in range(grad_probs.shape[0]):
+        out[t] = topk_bwd_row(grad_probs[t], routing_map[t], scores[t], score_func,
+                              scaling_factor)
+    return out
+
+
+# --------------------------------------------------------------------------
+# aux-loss scores  [TE] Summary (fused_score_for_moe_aux_loss); the aux_loss
+# rows of both benchmark tables
+# --------------------------------------------------------------------------
+def aux_scores_fwd_row(x, K, score_func):
+    """Returns (q, routing_map, saved): q the aux-loss score row, the top-K
+    map of q, and what the backward needs (sigmoid(x) for sigmoid, q itself
+    for softmax)."""
+    x = np.asarray(x, dtype=np.float64)
+    if score_func == SOFTMAX:
+        q = score_row(x, SOFTMAX)
+        saved = q
+    elif score_func == SIGMOID:
+        sig = score_row(x, SIGMOID)
+        q = sig / sig.sum()
+        saved = sig
+    else:
+        raise ValueError(score_func)
+    m = np.zeros(x.size, dtype=bool)
+    m[order_desc(q)[:K]] = True
+    return q, m, saved
+
+
+def aux_scores_fwd(logits, K, score_func=SOFTMAX):
+    logits = np.asarray(logits, dtype=np.float64)
+    T, E = logits.shape
+    q = np.zeros((T, E))
+    m = np.zeros((T, E), dtype=bool)
+    saved = np.zeros((T, E))
+    near = np.zeros(T, dtype=bool)
+    for t in range(T):
+        q[t], m[t], saved[t] = aux_scores_fwd_row(logits[t], K, score_func)
+        if K < E:
+            o = order_desc(q[t])
+            near[t] = _near(q[t][o[K - 1]], q[t][o[K]])
+    return dict(scores=q, routing_map=m, saved=saved, near_tie=near)
+
+
+def aux_scores_bwd_row(g, saved, score_func):
+    """grad_logits of one row from grad_scores g.
+
+    softmax (saved = q):        gx_j = q_j (g_j - sum_i g_i q_i)
+    sigmoid (saved = sigma):    Z = sum_i sigma_i, Dq = sum_i g_i sigma_i / Z,
+                                gx_j = (g_j - Dq) / Z * sigma_j (1 - sigma_j)
+    """
+    g = np.asarray(g, dtype=np.float64)
+    v = np.asarray(saved, dtype=np.float64)
+    if score_func == SOFTMAX:
+        return v * (g - np.sum(g * v))
+    if score_func == SIGMOID:
+        Z = v.sum()
+        Dq = np.sum(g * v) / Z
+        return (g - Dq) / Z * v * (1.0 - v)
+    raise ValueError(score_func)
+
+
+def aux_scores_bwd(grad_scores, saved, score_func=SOFTMAX):
+    grad_scores = np.asarray(grad_scores, dtype=np.float64)
+    out = np.zeros_like(grad_scores)
+    for t in range(grad_scores.shape[0]):
+        out[t] = aux_scores_bwd_row(grad_scores[t], saved[t], score_func)
+    return out
+
+
+# --------------------------------------------------------------------------
+# output rounding
+# --------------------------------------------------------------------------
+def round_to_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 number (8 significant bits,
+    ties to even), returned as float64.  Only normal-range values occur in the
+    router's outputs; zeros stay zero."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m * 2**e, 0.5 <= |m| < 1
+    r = np.round(m * 256.0) / 256.0         # np.round: halves go to even
+    return np.ldexp(r, e)
+
+
+def round_to_f32(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)

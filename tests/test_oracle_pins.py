@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each ``check_*`` helper raises AssertionError when the oracle breaks one fact:
+a closed form, an invariant, a special case that reduces to a textbook
+definition, brute force over every K-subset of a tiny row, or central finite
+differences.  The same helpers run against deliberately broken copies of the
+oracle (``test_pins_catch_planted_mistakes``) to show that each plausible
+mistake fails at least one pin.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle.router_oracle as O
+
+
+# --------------------------------------------------------------------------
+# score functions: closed forms
+# --------------------------------------------------------------------------
+def check_softmax_closed_form():
+    # logits ln(1..4): softmax is exactly (1, 2, 3, 4) / 10
+    x = np.log(np.array([1.0, 2.0, 3.0, 4.0]))
+    s = O.score_row(x, "softmax")
+    assert np.allclose(s, [0.1, 0.2, 0.3, 0.4], rtol=0, atol=1e-15), s
+    # invariant under a shift of the whole row
+    s2 = O.score_row(x + 37.25, "softmax")
+    assert np.allclose(s, s2, rtol=0, atol=1e-15)
+    # two experts: softmax of (a, b) equals sigmoid(a - b)
+    a, b = 0.7, -1.9
+    s3 = O.score_row(np.array([a, b]), "softmax")
+    assert abs(s3[0] - 1.0 / (1.0 + math.exp(-(a - b)))) < 1e-15
+    # random rows sum to one
+    rng = np.random.default_rng(1)
+    for E in (1, 3, 64, 2304):
+        s = O.score_row(rng.normal(0, 2, E), "softmax")
+        assert abs(s.sum() - 1.0) < 1e-12
+        assert np.all(s > 0)
+
+
+def check_sigmoid_closed_form():
+    s = O.score_row(np.array([0.0, math.log(3.0), -math.log(3.0)]), "sigmoid")
+    assert np.allclose(s, [0.5, 0.75, 0.25], rtol=0, atol=1e-15), s
+    x = np.random.default_rng(2).normal(0, 3, 1000)
+    assert np.allclose(O.score_row(x, "sigmoid") + O.score_row(-x, "sigmoid"), 1.0,
+                       rtol=0, atol=1e-15)
+    assert np.all(np.diff(O.score_row(np.sort(x), "sigmoid")) >= 0)
+
+
+def test_softmax_closed_form():
+    check_softmax_closed_form()
+
+
+def test_sigmoid_closed_form():
+    check_sigmoid_closed_form()
+
+
+# --------------------------------------------------------------------------
+# top-K selection: brute force over all subsets
+# --------------------------------------------------------------------------
+def brute_force_topk(keys, K, allowed=None):
+    """The K-subset of allowed experts whose smallest key is >= every key left
+    out, choosing among valid subsets the lexicographically smallest sorted
+    index tuple (= ties to the lower index)."""
+    E = len(keys)
+    idx = [i for i in range(E) if allowed is None or allowed[i]]
+    for sub in itertools.combinations(idx, K):  # lexicographic order
+        inside = min(keys[i] for i in sub)
+        outside = [keys[i] for i in idx if i not in sub]
+        if not outside or inside >= max(outside):
+            return set(sub)
+    raise AssertionError("no valid subset")
+
+
+def brute_force_groups(keys, K, G, gk):
+    """Group-limited pre-selection by enumeration: a group's score is the
+    largest sum over its (K/gk)-subsets; kept groups are the valid gk-subset
+    of groups with the lexicographically smallest tuple."""
+    E = len(keys)
+    eg = E // G
+    M = K // gk
+    gs = [max(sum(c) for c in itertools.combinations(keys[g * eg:(g + 1) * eg], M))
+          for g in range(G)]
+    kept = brute_force_topk(gs, gk)
+    allowed = [(i // eg) in kept for i in range(E)]
+    return allowed
+
+
+def _rows_for_brute_force(rng, E):
+    yield rng.integers(-2, 3, E).astype(float)         # heavy ties
+    yield rng.normal(0, 1, E)                          # distinct
+    yield np.zeros(E)                                  # all equal
+    yield np.where(rng.random(E) < 0.5, 0.0, -0.0)     # signed zeros only
+    yield np.round(rng.normal(0, 1, E), 1)             # some ties
+
+
+def check_topk_brute_force():
+    rng = np.random.default_rng(3)
+    for E in range(1, 9):
+        for x in _rows_for_brute_force(rng, E):
+            for sf in ("softmax", "sigmoid"):
+                for bias in (None, rng.integers(-1, 2, E) * 0.25):
+                    s = O.score_row(x, sf)
+                    key = s + (0 if bias is None else bias)
+                    for K in range(1, E + 1):
+                        _, m, _, _ = O.topk_fwd_row(x, K, sf, expert_bias=bias)
+                        want = brute_force_topk(list(key), K)
+                        got = set(np.nonzero(m)[0].tolist())
+                        assert got == want, (E, K, sf, x, bias, got, want)
+
+
+def check_grouped_brute_force():
+    rng = np.random.default_rng(4)
+    for E, G in ((4, 2), (6, 3), (8, 4), (8, 2), (9, 3)):
+        for x in _rows_for_brute_force(rng, E):
+            for bias in (None, rng.uniform(-0.1, 0.1, E)):
+                s = O.score_row(x, "sigmoid")
+                key = s + (0 if bias is None else bias)
+                for gk in range(1, G + 1):
+                    for K in range(gk, gk * (E // G) + 1, gk):
+                        _, m, _, _ = O.topk_fwd_row(x, K, "sigmoid", G, gk,
+                                                    expert_bias=bias)
+                        allowed = brute_force_groups(list(key), K, G, gk)
+                        want = brute_force_topk(list(key), K, allowed)
+                        got = set(np.nonzero(m)[0].tolist())
+                        assert got == want, (E, G, gk, K, x, got, want)
+
+
+def test_topk_brute_force():
+    check_topk_brute_force()
+
+
+def test_grouped_brute_force():
+    check_grouped_brute_force()
+
+
+# --------------------------------------------------------------------------
+# probabilities: closed forms and special cases
+# --------------------------------------------------------------------------
+def check_probs_closed_forms():
+    rng = np.random.default_rng(5)
+    for E, K in ((16, 1), (64, 4), (512, 22), (300, 36)):
+        x = rng.normal(0, 1.5, E)
+        c = 2.5
+        p, m, s, _ = O.topk_fwd_row(x, K, "sigmoid", scaling_factor=c)
+        assert abs(p.sum() - c) < 1e-12                    # renormalised to c
+        assert m.sum() == K and np.all(p[m] > 0) and np.all(p[~m] == 0)
+        p, m, s, _ = O.topk_fwd_row(x, K, "softmax", scaling_factor=c)
+        assert abs(p.sum() - c * s[m].sum()) < 1e-12
+        assert np.allclose(p[m], c * s[m], rtol=0, atol=0)
+        assert m.sum() == K and np.all(p[~m] == 0)
+        # softmax keyed on the raw logits picks the K largest logits
+        assert set(np.nonzero(m)[0]) == set(np.argsort(-x, kind="stable")[:K])
+    # K = E: softmax probs are c * softmax; sigmoid probs equal c * aux scores
+    x = rng.normal(0, 1, 40)
+    p, m, s, _ = O.topk_fwd_row(x, 40, "softmax", scaling_factor=1.5)
+    assert np.allclose(p, 1.5 * O.score_row(x, "softmax"), rtol=0, atol=1e-15)
+    p, _, _, _ = O.topk_fwd_row(x, 40, "sigmoid", scaling_factor=1.5)
+    q, _, _ = O.aux_scores_fwd_row(x, 3, "sigmoid")
+    assert np.allclose(p, 1.5 * q, rtol=1e-14, atol=0)
+    # an all-equal row selects experts 0..K-1 and softmax probs are c / E
+    p, m, _, _ = O.topk_fwd_row(np.full(24, 0.3), 5, "softmax", scaling_factor=2.0)
+    assert np.array_equal(np.nonzero(m)[0], np.arange(5))
+    assert np.allclose(p[:5], 2.0 / 24, rtol=0, atol=1e-16)
+    # K = 1 sigmoid: the single probability is c
+    p, m, _, _ = O.topk_fwd_row(x, 1, "sigmoid", scaling_factor=2.5)
+    assert p[m][0] == 2.5
+
+
+def check_grouping_identities():
+    rng = np.random.default_rng(6)
+    for _ in range(20):
+        E, G = 64, 8
+        x = rng.normal(0, 1, E)
+        b = rng.uniform(-0.1, 0.1, E)
+        for sf in ("softmax", "sigmoid"):
+            ref = O.topk_fwd_row(x, 8, sf, 0, 0, 2.0, b)
+            for ng, gk in ((1, 1), (G, G), (4, 4)):
+                got = O.topk_fwd_row(x, 8, sf, ng, gk, 2.0, b)
+                assert np.array_equal(got[1], ref[1])
+                assert np.array_equal(got[0], ref[0])
+            # a constant bias does not change the selection
+            m0 = O.topk_fwd_row(x, 8, sf, G, 4, 2.0, None)[1]
+            m1 = O.topk_fwd_row(x, 8, sf, G, 4, 2.0, np.full(E, 0.07))[1]
+            assert np.array_equal(m0, m1)
+    # a hand-built grouped row: group 0 holds the single largest key, but
+    # groups 1 and 2 have larger top-2 sums, so group 0 is dropped
+    x = np.array([5.0, -5.0, 3.0, 3.0, 2.9, 2.9, 0.0, 0.0])
+    _, m, _, _ = O.topk_fwd_row(x, 2, "sigmoid", 4, 1)
+    assert np.array_equal(np.nonzero(m)[0], [2, 3])
+    _, m, _, _ = O.topk_fwd_row(x, 4, "sigmoid", 4, 2)
+    assert np.array_equal(np.nonzero(m)[0], [2, 3, 4, 5])
+
+
+def test_probs_closed_forms():
+    check_probs_closed_forms()
+
+
+def test_grouping_identities():
+    check_grouping_identities()
+
+
+# --------------------------------------------------------------------------
+# backward: central finite differences of L = sum g * p(x)
+# --------------------------------------------------------------------------
+def _fd_grad(f, x, h):
+    gx = np.zeros_like(x)
+    for j in range(x.size):
+        e = np.zeros_like(x)
+        e[j] = h
+        gx[j] = (f(x + e) - f(x - e)) / (2 * h)
+    return gx
+
+
+def check_topk_bwd_finite_differences():
+    rng = np.random.default_rng(7)
+    h = 1e-4
+    checked = 0
+    for sf in ("softmax", "sigmoid"):
+        for E, K, c, ng, gk, use_b in ((12, 1, 1.0, 0, 0, False), (12, 3, 2.5, 0, 0, True),
+                                       (32, 5, 1.0, 0, 0, False), (32, 8, 2.5, 4, 2, True),
+                                       (40, 40, 1.0, 0, 0, False)):
+            for _ in range(3):
+                x = rng.normal(0, 1.5, E)
+                b = rng.uniform(-0.1, 0.1, E) if use_b else None
+                g = rng.normal(0, 1, E)
+                p, m, s, _ = O.topk_fwd_row(x, K, sf, ng, gk, c, b)
+
+                def loss(xx):
+                    pp, mm, _, _ = O.topk_fwd_row(xx, K, sf, ng, gk, c, b)
+                    assert np.array_equal(mm, m)
+                    return float(np.dot(g, pp))
+                try:
+                    fd = _fd_grad(loss, x, h)
+                except AssertionError:
+                    continue  # the selection moved under +-h: not a smooth point
+                an = O.topk_bwd_row(g, m, s, sf, c)
+                assert np.all(np.abs(fd - an) <= 1e-3 * np.maximum(1, np.abs(an))), \
+                    (sf, E, K, np.max(np.abs(fd - an)))
+                # tighter than the stated bound: the formula is exact
+                assert np.max(np.abs(fd - an)) < 1e-6
+                if sf == "softmax":
+                    assert abs(an.sum()) < 1e-12   # constants are in the kernel
+                if sf == "sigmoid" and K == 1:
+                    assert np.all(an == 0)
+                checked += 1
+    assert checked >= 20
+
+
+def check_aux_closed_forms_and_fd():
+    rng = np.random.default_rng(8)
+    h = 1e-4
+    for sf in ("softmax", "sigmoid"):
+        for E, K in ((7, 2), (64, 8), (300, 36)):
+            x = rng.normal(0, 1.5, E)
+            q, m, saved = O.aux_scores_fwd_row(x, K, sf)
+            assert abs(q.sum() - 1) < 1e-12
+            assert m.sum() == K
+            assert set(np.nonzero(m)[0]) == set(np.argsort(-x, kind="stable")[:K])
+            if sf == "sigmoid":
+                assert np.allclose(saved, 1 / (1 + np.exp(-x)), rtol=0, atol=1e-15)
+            if E <= 64:
+                g = rng.normal(0, 1, E)
+                fd = _fd_grad(lambda xx: float(np.dot(g, O.aux_scores_fwd_row(xx, K, sf)[0])),
+                              x, h)
+                an = O.aux_scores_bwd_row(g, saved, sf)
+                assert np.max(np.abs(fd - an)) < 1e-6, (sf, E, np.max(np.abs(fd - an)))
+    # uniform logits: q is uniform, the map is experts 0..K-1
+    for sf in ("softmax", "sigmoid"):
+        q, m, _ = O.aux_scores_fwd_row(np.full(10, -0.4), 3, sf)
+        assert np.allclose(q, 0.1, rtol=0, atol=1e-16)
+        assert np.array_equal(np.nonzero(m)[0], [0, 1, 2])
+
+
+def test_topk_bwd_finite_differences():
+    check_topk_bwd_finite_differences()
+
+
+def test_aux_closed_forms_and_fd():
+    check_aux_closed_forms_and_fd()
+
+
+# --------------------------------------------------------------------------
+# output rounding to bf16 (nearest, ties to even)
+# --------------------------------------------------------------------------
+def check_bf16_rounding():
+    u = 2.0 ** -7  # bf16 spacing in [1, 2)
+    cases = {1.0: 1.0, 1 + u / 2: 1.0, 1 + 1.5 * u: 1 + 2 * u, 1 + 0.49 * u: 1.0,
+             1 + 0.51 * u: 1 + u, -3.0: -3.0, 0.0: 0.0, 255.5: 256.0, 254.5: 254.0,
+             2 - u / 4: 2.0}
+    for v, want in cases.items():
+        assert O.round_to_bf16(np.array([v]))[0] == want, (v, want)
+    # agrees with torch's fp32 -> bf16 conversion on fp32 inputs
+    import torch
+    x = np.random.default_rng(9).normal(0, 10, 10000).astype(np.float32)
+    t = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_to_bf16(x.astype(np.float64)), t)
+
+
+def test_bf16_rounding():
+    check_bf16_rounding()
+
+
+# --------------------------------------------------------------------------
+# the pins catch plausible mistakes planted in the oracle (CPU only)
+# --------------------------------------------------------------------------
+def _wrong_order(keys):  # ties to the HIGHER index
+    keys = np.asarray(keys, dtype=np.float64)
+    return np.lexsort((-np.arange(keys.size), -keys))
+
+
+def _wrong_softmax_score(x, sf):
+    x = np.asarray(x, dtype=np.float64)
+    if sf == "softmax":
+        e = np.exp(x - x.max())
+        return e / e.max()          # normalised by the max, not the sum
+    return 1 / (1 + np.exp(-x))
+
+
+def _wrong_sigmoid_sign(x, sf):
+    x = np.asarray(x, dtype=np.float64)
+    if sf == "sigmoid":
+        return 1 / (1 + np.exp(x))
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def _wrong_group_scores(keys, G, per_group):  # strided instead of contiguous
+    return np.array([np.sort(keys[g::G])[::-1][:per_group].sum() for g in range(G)])
+
+
+def _wrong_group_scores_max(keys, G, per_group):  # max instead of top-M sum
+    eg = keys.size // G
+    return np.array([keys[g * eg:(g + 1) * eg].max() for g in range(G)])
+
+
+_orig_topk_bwd_row = O.topk_bwd_row
+
+
+def _wrong_bwd_no_d(g, m, s, sf, c=1.0):
+    g = np.asarray(g, float)
+    s = np.asarray(s, float)
+    mm = np.asarray(m, bool).astype(float)
+    if sf == "softmax":
+        return s * (c * mm * g)     # drops the -D term
+    return _orig_topk_bwd_row(g, m, s, sf, c)
+
+
+def _wrong_bwd_sigmoid_scale(g, m, s, sf, c=1.0):
+    if sf == "sigmoid":
+        return _orig_topk_bwd_row(g, m, s, sf, 1.0)   # drops c
+    return _orig_topk_bwd_row(g, m, s, sf, c)
+
+
+_orig_fwd_row = O.topk_fwd_row
+
+
+def _wrong_no_renorm(x, K, score_func, num_groups=0, group_topk=0,
+                     scaling_factor=1.0, expert_bias=None):
+    p, m, s, n = _orig_fwd_row(x, K, score_func, num_groups, group_topk,
+                               scaling_factor, expert_bias)
+    if score_func == "sigmoid":
+        p = np.where(m, scaling_factor * s, 0.0)
+    return p, m, s, n
+
+
+_orig_aux_bwd = O.aux_scores_bwd_row
+
+
+def _wrong_aux_bwd(g, saved, sf):
+    if sf == "sigmoid":
+        v = np.asarray(saved, float)
+        Z = v.sum()
+        return (np.asarray(g, float) - np.sum(g * v) / Z) / Z * v   # drops (1 - v)
+    return _orig_aux_bwd(g, saved, sf)
+
+
+def _wrong_bf16(x):
+    return np.asarray(x, np.float64).astype(np.float32).view(np.uint32) \
+        .__and__(np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)  # truncation
+
+
+PLANTED = [
+    ("order_desc", _wrong_order, [check_topk_brute_force]),
+    ("score_row", _wrong_softmax_score, [check_softmax_closed_form]),
+    ("score_row", _wrong_sigmoid_sign, [check_sigmoid_closed_form]),
+    ("group_scores", _wrong_group_scores, [check_grouped_brute_force]),
+    ("group_scores", _wrong_group_scores_max, [check_grouped_brute_force]),
+    ("topk_bwd_row", _wrong_bwd_no_d, [check_topk_bwd_finite_differences]),
+    ("topk_bwd_row", _wrong_bwd_sigmoid_scale, [check_topk_bwd_finite_differences]),
+    ("topk_fwd_row", _wrong_no_renorm, [check_probs_closed_forms]),
+    ("aux_scores_bwd_row", _wrong_aux_bwd, [check_aux_closed_forms_and_fd]),
+    ("round_to_bf16", _wrong_bf16, [check_bf16_rounding]),
+]
+
+
+@pytest.mark.parametrize("name,wrong,checks", PLANTED,
+                         ids=[f"{p[0]}-{p[1].__name__}" for p in PLANTED])
+def test_pins_catch_planted_mistakes(monkeypatch, name, wrong, checks):
+    monkeypatch.setattr(O, name, wrong)
+    for check in checks:
+        with pytest.raises(AssertionError):
+            check()
