@@ -1,0 +1,216 @@
+/*
+ * moe_router.h — fused Mixture-of-Experts router for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI over caller-owned device memory.  The operations are the two fused
+ * router ops of NVIDIA TransformerEngine PR #3012 "[Common] Optimize fused
+ * router forward/backward kernels" (Summary: fused_topk_with_score_function
+ * and fused_score_for_moe_aux_loss, each with a forward and a backward).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every [T, E] tensor is dense row-major with row stride E elements, in
+ *   device memory owned by the caller.  Nothing is allocated, freed or
+ *   synchronised here: each call validates its arguments on the host,
+ *   enqueues one kernel on `stream` and returns.
+ * - `dtype` is the type of the logits and of the tensors that follow it
+ *   (probs, grad_probs, grad_logits): MR_F32 (float) or MR_BF16
+ *   (__nv_bfloat16).  Scores, intermediates, grad_scores and the expert bias
+ *   are always float; routing maps are one byte per element, 0 or 1.
+ * - All arithmetic is fp32 (bf16 inputs are widened exactly); bf16 outputs are
+ *   rounded to nearest-even once, at the store.
+ * - Ties in the top-K choice go to the lower expert index (and, for grouped
+ *   routing, to the lower group index); -0.0 and +0.0 are equal.
+ * - Inputs must be finite; NaN or Inf logits give unspecified (but in-bounds)
+ *   results.
+ * - T == 0 is a successful no-op once the other arguments have been checked;
+ *   tensor pointers may then be NULL (empty tensors have no storage).
+ * - Pointers need no particular alignment; rows that are not 16-byte aligned
+ *   take a slower element-wise path.
+ * - Return value: MR_OK (0) or a negative mr_status.  On an argument error
+ *   nothing is written and nothing is enqueued.  MR_ERR_CUDA reports a failed
+ *   launch (cudaGetLastError); kernels already enqueued are not undone.
+ * - The buffers must live on the calling thread's current CUDA device.
+ * - Calls are thread-safe with respect to each other except
+ *   moe_router_force_path and moe_router_force_fwd_lanes, which set
+ *   process-wide state.
+ */
+#ifndef MOE_ROUTER_H
+#define MOE_ROUTER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MR_API __attribute__((visibility("default")))
+#else
+#define MR_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* mr_stream_t;
+
+typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1 } mr_score_func;
+typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
+
+typedef enum {
+  MR_OK = 0,
+  MR_ERR_INVALID = -1,      /* an argument breaks the rules stated per call */
+  MR_ERR_UNSUPPORTED = -2,  /* valid, but beyond this build's limits below   */
+  MR_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed          */
+} mr_status;
+
+/* Limits of this build (MR_ERR_UNSUPPORTED beyond them). */
+#define MR_MAX_EXPERTS 2304
+#define MR_MAX_TOPK 36
+#define MR_MAX_GROUPS 32
+
+/*
+ * router_topk_fwd — score, select and emit the top-K experts of each token.
+ *
+ * Source: TransformerEngine PR #3012, Summary and Performance (the forward
+ * reads logits [T,E] and writes probs [T,E] in the logits dtype, the routing
+ * map [T,E] as one byte per element and the fp32 intermediate scores [T,E]);
+ * the benchmark tables name the softmax and sigmoid score functions.
+ *
+ * Per token row x (length E):
+ *   score     softmax: s = exp(x - max x) / sum exp(x - max x)  (all E experts)
+ *             sigmoid: s = 1 / (1 + exp(-x))
+ *   key       k = s + expert_bias (bias optional, used for selection only)
+ *   groups    if num_groups > 1: E splits into num_groups contiguous groups;
+ *             a group scores the sum of its K/group_topk largest keys; only
+ *             the group_topk best groups stay selectable
+ *   select    the K largest keys among selectable experts (ties: lower index)
+ *   probs     softmax: c * s on selected experts, 0 elsewhere (no renormalising)
+ *             sigmoid: c * s / (sum of s over the selected), 0 elsewhere
+ *   scores    s (fp32), every expert
+ * with c = scaling_factor.
+ *
+ * logits       [T,E] dtype, input
+ * expert_bias  [E] float or NULL
+ * probs        [T,E] dtype, output
+ * routing_map  [T,E] uint8 0/1, output, exactly K ones per row
+ * scores       [T,E] float, output (saved for router_topk_bwd)
+ *
+ * MR_ERR_INVALID: T < 0, E < 1, K < 1, K > E, T*E > INT_MAX, unknown dtype or
+ *   score_func, a NULL tensor when T > 0 (logits, probs, routing_map, scores),
+ *   num_groups < 0, and for num_groups > 1: E % num_groups != 0,
+ *   group_topk outside [1, num_groups], K % group_topk != 0 or
+ *   K / group_topk > E / num_groups (PR #3012, Hardening: topk in [1, E] and
+ *   topk % group_topk == 0; num_tokens * num_experts <= INT_MAX).
+ *   num_groups 0 or 1 means no grouping (group_topk is then ignored).
+ * MR_ERR_UNSUPPORTED: E > MR_MAX_EXPERTS, K > MR_MAX_TOPK,
+ *   num_groups > MR_MAX_GROUPS.
+ */
+MR_API int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
+                    mr_score_func score_func, int num_groups, int group_topk,
+                    float scaling_factor, const float* expert_bias, void* probs,
+                    uint8_t* routing_map, float* scores, mr_stream_t stream);
+
+/*
+ * router_topk_bwd — gradient of the forward's probs with respect to logits.
+ *
+ * Source: TransformerEngine PR #3012, Backward kernels (pass 1: per-row sums
+ * by register and warp reduction; pass 2: per-element gradients) and the
+ * review summary (the gradient per score function).  The selection and the
+ * expert bias carry no gradient.  With g = grad_probs, m = routing_map,
+ * s = scores and c = scaling_factor, per row:
+ *   softmax: D = c * sum_j m_j g_j s_j;   gx_j = s_j * (c m_j g_j - D)
+ *   sigmoid: S = sum_j m_j s_j, D = sum_j m_j g_j s_j;
+ *            gx_j = m_j * (c / S) * (g_j - D / S) * s_j * (1 - s_j)
+ *
+ * grad_probs   [T,E] dtype, input
+ * routing_map  [T,E] uint8 (nonzero = selected), input from router_topk_fwd
+ * scores       [T,E] float, input from router_topk_fwd
+ * grad_logits  [T,E] dtype, output
+ * K            the forward's K (checked, 1 <= K <= E)
+ *
+ * MR_ERR_INVALID / MR_ERR_UNSUPPORTED: as router_topk_fwd for T, E, K, dtype,
+ *   score_func and NULL tensors.  A sigmoid row whose map selects nothing
+ *   produces NaN (S = 0); the forward never writes such a map.
+ */
+MR_API int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,
+                    const float* scores, mr_dtype dtype, int T, int E, int K,
+                    mr_score_func score_func, float scaling_factor,
+                    void* grad_logits, mr_stream_t stream);
+
+/*
+ * router_aux_scores_fwd — full-row scores for the load-balancing aux loss,
+ * with their top-K routing map.
+ *
+ * Source: TransformerEngine PR #3012, Summary (fused_score_for_moe_aux_loss)
+ * and the aux_loss rows of both benchmark tables.  Per row:
+ *   softmax: q = softmax(x)
+ *   sigmoid: sig = 1 / (1 + exp(-x)),  q = sig / sum_E sig
+ *   routing_map = top-K of q (ties: lower index; no bias, groups or scaling)
+ *
+ * logits        [T,E] dtype, input
+ * scores        [T,E] float, output q
+ * routing_map   [T,E] uint8 0/1, output
+ * intermediate  [T,E] float, output sig (sigmoid: required; softmax: may be
+ *               NULL, and if given receives q again)
+ *
+ * Errors: as router_topk_fwd for T, E, K, dtype, score_func; when T > 0, NULL
+ *   logits, scores or routing_map, or NULL intermediate with sigmoid:
+ *   MR_ERR_INVALID.
+ */
+MR_API int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E,
+                          int K, mr_score_func score_func, float* scores,
+                          uint8_t* routing_map, float* intermediate,
+                          mr_stream_t stream);
+
+/*
+ * router_aux_scores_bwd — gradient of the aux scores q with respect to logits.
+ *
+ * Source: TransformerEngine PR #3012, Summary and Backward kernels (same
+ * two-pass structure as the top-K backward).  With g = grad_scores, per row:
+ *   softmax (saved = q):   gx_j = q_j * (g_j - sum_i g_i q_i)
+ *   sigmoid (saved = sig): Z = sum_i sig_i, Dq = sum_i g_i sig_i / Z,
+ *                          gx_j = (g_j - Dq) / Z * sig_j * (1 - sig_j)
+ *
+ * grad_scores  [T,E] float, input
+ * saved        [T,E] float: softmax the forward's scores, sigmoid its
+ *              intermediate
+ * grad_logits  [T,E] dtype, output
+ * K            the forward's K (checked, 1 <= K <= E; not otherwise used)
+ *
+ * Errors: as router_topk_bwd.
+ */
+MR_API int router_aux_scores_bwd(const float* grad_scores, const float* saved,
+                          mr_dtype dtype, int T, int E, int K,
+                          mr_score_func score_func, void* grad_logits,
+                          mr_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+MR_API const char* moe_router_strerror(int code);
+
+/*
+ * Kernel path of the top-K and aux forwards.  MR_PATH_AUTO picks by E and K;
+ * the others force one path for every shape it supports (shapes it does not
+ * support still take the automatic choice).  Process-wide; meant for tests
+ * and benchmarks.  The environment variable MOE_ROUTER_FORCE_PATH
+ * (auto|warp|cta) sets the initial value.  Returns the previous value, or
+ * MR_ERR_INVALID for an unknown path.
+ */
+typedef enum { MR_PATH_AUTO = 0, MR_PATH_WARP = 1, MR_PATH_CTA = 2 } mr_path;
+MR_API int moe_router_force_path(int path);
+
+/*
+ * Lanes that share one token row in the segment forward: 8, 16 or 32, or 0
+ * for the automatic choice (the default).  A width that cannot hold a given
+ * row (too few lanes for its E, or 2 * lanes < K) falls back to the
+ * automatic choice for that call.  Process-wide; meant for tests and
+ * benchmarks.  Returns the previous value, or MR_ERR_INVALID.
+ */
+MR_API int moe_router_force_fwd_lanes(int lanes);
+
+/* Library ABI version: 100 * major + minor. */
+MR_API int moe_router_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTER_H */

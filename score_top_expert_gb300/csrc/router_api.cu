@@ -1,0 +1,267 @@
+// C ABI of the router library: argument checks, kernel-path choice, launch.
+// Declarations and the contract of every entry point are in moe_router.h.
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "moe_router.h"
+#include "router_launch.cuh"
+
+using namespace moe_router;
+
+namespace {
+
+constexpr int kVersion = 100;
+
+std::atomic<int> g_path{-1};       // -1: not yet read from the environment
+std::atomic<int> g_fwd_lanes{0};   // 0: automatic
+
+int current_path() {
+  int p = g_path.load(std::memory_order_relaxed);
+  if (p >= 0) return p;
+  p = MR_PATH_AUTO;
+  if (const char* env = std::getenv("MOE_ROUTER_FORCE_PATH")) {
+    if (std::strcmp(env, "warp") == 0) p = MR_PATH_WARP;
+    else if (std::strcmp(env, "cta") == 0) p = MR_PATH_CTA;
+  }
+  int expected = -1;
+  g_path.compare_exchange_strong(expected, p);
+  return g_path.load(std::memory_order_relaxed);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int dtype, int T, int E, int K, int sf) {
+  if (dtype != MR_F32 && dtype != MR_BF16) return MR_ERR_INVALID;
+  if (sf != MR_SOFTMAX && sf != MR_SIGMOID) return MR_ERR_INVALID;
+  if (T < 0 || E < 1 || K < 1 || K > E) return MR_ERR_INVALID;
+  if (static_cast<long long>(T) * static_cast<long long>(E) > INT_MAX) return MR_ERR_INVALID;
+  if (E > MR_MAX_EXPERTS || K > MR_MAX_TOPK) return MR_ERR_UNSUPPORTED;
+  return MR_OK;
+}
+
+int check_groups(int E, int K, int num_groups, int group_topk) {
+  if (num_groups < 0) return MR_ERR_INVALID;
+  if (num_groups <= 1) return MR_OK;
+  if (E % num_groups != 0) return MR_ERR_INVALID;
+  if (group_topk < 1 || group_topk > num_groups) return MR_ERR_INVALID;
+  if (K % group_topk != 0) return MR_ERR_INVALID;
+  if (K / group_topk > E / num_groups) return MR_ERR_INVALID;
+  if (num_groups > MR_MAX_GROUPS) return MR_ERR_UNSUPPORTED;
+  return MR_OK;
+}
+
+// Lanes per row and chunks per lane of the segment forward.  The lower bound
+// needs 2 * lanes >= K disjoint groups; fewer lanes per row share the per-row
+// selection work among fewer lanes and route more rows per warp.
+bool choose_fwd(int E, int K, bool vec, FwdConfig* c) {
+  const int chunks = (E + 3) / 4;
+  if (!vec) {
+    c->seg = 32;
+    c->nc = 18;
+    return chunks <= 32 * 18;
+  }
+  struct Opt { int seg, nc; };
+  static const Opt opts[] = {{8, 2}, {8, 4}, {8, 8}, {16, 4}, {16, 8},
+                             {32, 2}, {32, 4}, {32, 8}, {32, 18}};
+  const int forced = g_fwd_lanes.load(std::memory_order_relaxed);
+  for (const Opt& o : opts) {
+    if (forced != 0 && o.seg != forced) continue;
+    if (2 * o.seg < K) continue;
+    if (o.seg * o.nc >= chunks) {
+      c->seg = o.seg;
+      c->nc = o.nc;
+      return true;
+    }
+  }
+  if (forced != 0) {  // the forced width cannot hold this row: automatic choice
+    for (const Opt& o : opts) {
+      if (2 * o.seg < K) continue;
+      if (o.seg * o.nc >= chunks) { c->seg = o.seg; c->nc = o.nc; return true; }
+    }
+  }
+  return false;
+}
+
+bool choose_bwd(int E, BwdConfig* c) {
+  const int chunks = (E + 3) / 4;
+  struct Opt { int seg, w, nc; };
+  static const Opt opts[] = {{8, 1, 2}, {16, 1, 4}, {32, 1, 4}, {32, 2, 4}, {32, 3, 6}};
+  for (const Opt& o : opts) {
+    if (o.seg * o.w * o.nc >= chunks) {
+      c->seg = o.seg; c->w = o.w; c->nc = o.nc;
+      return true;
+    }
+  }
+  return false;
+}
+
+int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  cudaError_t e;
+  if (sf == MR_SOFTMAX) {
+    e = dt == MR_F32 ? launch_fwd_softmax_f32(a, c, st) : launch_fwd_softmax_bf16(a, c, st);
+  } else {
+    e = dt == MR_F32 ? launch_fwd_sigmoid_f32(a, c, st) : launch_fwd_sigmoid_bf16(a, c, st);
+  }
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
+                    mr_score_func score_func, int num_groups, int group_topk,
+                    float scaling_factor, const float* expert_bias, void* probs,
+                    uint8_t* routing_map, float* scores, mr_stream_t stream) {
+  int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  rc = check_groups(E, K, num_groups, group_topk);
+  if (rc != MR_OK) return rc;
+  if (T > 0 && (logits == nullptr || probs == nullptr || routing_map == nullptr ||
+                scores == nullptr))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+
+  const bool grouped = num_groups > 1;
+  const bool vec = (E % 4 == 0) && aligned16(logits) && aligned16(probs) &&
+                   aligned16(routing_map) && aligned16(scores) &&
+                   (expert_bias == nullptr || aligned16(expert_bias));
+  FwdConfig c{};
+  if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
+  c.vec = vec;
+  c.op = 0;
+  c.km = (expert_bias != nullptr || grouped) ? 1 : 0;
+  c.extra_smem = grouped ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float) : 0;
+
+  FwdArgs a{};
+  a.logits = logits;
+  a.bias = expert_bias;
+  a.probs = probs;
+  a.map = routing_map;
+  a.scores = scores;
+  a.intermediate = nullptr;
+  a.T = T; a.E = E; a.K = K;
+  a.scaling = scaling_factor;
+  a.num_groups = grouped ? num_groups : 0;
+  a.group_topk = grouped ? group_topk : 0;
+  if (grouped) {
+    a.group_size = E / num_groups;
+    a.per_group = K / group_topk;
+    a.inv_group_size = 1.0f / static_cast<float>(a.group_size);
+    int lpg = 1;
+    while (lpg * 2 * num_groups <= c.seg) lpg *= 2;
+    a.lanes_per_group = lpg;
+  }
+  return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,
+                    const float* scores, mr_dtype dtype, int T, int E, int K,
+                    mr_score_func score_func, float scaling_factor,
+                    void* grad_logits, mr_stream_t stream) {
+  const int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  if (T > 0 && (grad_probs == nullptr || routing_map == nullptr || scores == nullptr ||
+                grad_logits == nullptr))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  BwdConfig c{};
+  if (!choose_bwd(E, &c)) return MR_ERR_UNSUPPORTED;
+  c.vec = (E % 4 == 0) && aligned16(grad_probs) && aligned16(routing_map) &&
+          aligned16(scores) && aligned16(grad_logits);
+  c.op = 0;
+  BwdArgs a{};
+  a.grad = grad_probs;
+  a.map = routing_map;
+  a.saved = scores;
+  a.grad_logits = grad_logits;
+  a.T = T; a.E = E;
+  a.scaling = scaling_factor;
+  const cudaError_t e = launch_bwd_any(score_func, dtype, a, c,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
+
+int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
+                          mr_score_func score_func, float* scores,
+                          uint8_t* routing_map, float* intermediate,
+                          mr_stream_t stream) {
+  const int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  if (T > 0 && (logits == nullptr || scores == nullptr || routing_map == nullptr ||
+                (score_func == MR_SIGMOID && intermediate == nullptr)))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  const bool vec = (E % 4 == 0) && aligned16(logits) && aligned16(scores) &&
+                   aligned16(routing_map) &&
+                   (intermediate == nullptr || aligned16(intermediate));
+  FwdConfig c{};
+  if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
+  c.vec = vec;
+  c.op = 1;
+  c.km = 0;
+  c.extra_smem = 0;
+  FwdArgs a{};
+  a.logits = logits;
+  a.map = routing_map;
+  a.scores = scores;
+  a.intermediate = intermediate;
+  a.T = T; a.E = E; a.K = K;
+  a.scaling = 1.0f;
+  return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int router_aux_scores_bwd(const float* grad_scores, const float* saved, mr_dtype dtype,
+                          int T, int E, int K, mr_score_func score_func,
+                          void* grad_logits, mr_stream_t stream) {
+  const int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  if (T > 0 && (grad_scores == nullptr || saved == nullptr || grad_logits == nullptr))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  BwdConfig c{};
+  if (!choose_bwd(E, &c)) return MR_ERR_UNSUPPORTED;
+  c.vec = (E % 4 == 0) && aligned16(grad_scores) && aligned16(saved) &&
+          aligned16(grad_logits);
+  c.op = 1;
+  BwdArgs a{};
+  a.grad = grad_scores;
+  a.map = nullptr;
+  a.saved = saved;
+  a.grad_logits = grad_logits;
+  a.T = T; a.E = E;
+  a.scaling = 1.0f;
+  const cudaError_t e = launch_bwd_any(score_func, dtype, a, c,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
+
+const char* moe_router_strerror(int code) {
+  switch (code) {
+    case MR_OK: return "success";
+    case MR_ERR_INVALID: return "invalid argument";
+    case MR_ERR_UNSUPPORTED: return "unsupported size (beyond this build's limits)";
+    case MR_ERR_CUDA: return "CUDA launch or runtime error";
+    default: return "unknown status code";
+  }
+}
+
+int moe_router_force_path(int path) {
+  if (path != MR_PATH_AUTO && path != MR_PATH_WARP && path != MR_PATH_CTA)
+    return MR_ERR_INVALID;
+  const int prev = current_path();
+  g_path.store(path, std::memory_order_relaxed);
+  return prev;
+}
+
+int moe_router_force_fwd_lanes(int lanes) {
+  if (lanes != 0 && lanes != 8 && lanes != 16 && lanes != 32) return MR_ERR_INVALID;
+  return g_fwd_lanes.exchange(lanes, std::memory_order_relaxed);
+}
+
+int moe_router_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Host-side launch of the router kernel templates: one function per
+// (score function, dtype) that maps a runtime configuration onto the
+// compiled instantiations.  Each .cu file instantiates one pair, so the
+// instantiations compile in parallel.
+#pragma once
+
+#include "router_bwd.cuh"
+#include "router_fwd.cuh"
+
+namespace moe_router {
+
+// Forward configuration chosen by the C ABI layer.
+struct FwdConfig {
+  int seg;     // lanes per row: 8, 16, 32
+  int nc;      // chunks of 4 experts per lane
+  bool vec;    // aligned 16-byte rows
+  int km;      // key mode (0: key = logit; 1: key = s + bias, optional groups)
+  int op;      // 0 top-K router, 1 aux scores
+  size_t extra_smem;  // grouped: rows of keys staged in shared memory
+};
+
+struct BwdConfig {
+  int seg, w, nc;
+  bool vec;
+  int op;
+};
+
+// compiled (SEG, NC) pairs of the forward; scalar rows use SEG 32, NC 18
+#define MR_FWD_VEC_CONFIGS(X) \
+  X(8, 2) X(8, 4) X(8, 8) X(16, 4) X(16, 8) X(32, 2) X(32, 4) X(32, 8) X(32, 18)
+
+// compiled (SEG, W, NC) triples of the backwards (vector and scalar rows)
+#define MR_BWD_CONFIGS(X) \
+  X(8, 1, 2) X(16, 1, 4) X(32, 1, 4) X(32, 2, 4) X(32, 3, 6)
+
+template <int SF, int DT, int SEG, int NC, bool VEC, int KM, int OP>
+cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  auto kern = router_fwd_seg_kernel<SF, DT, SEG, NC, VEC, KM, OP>;
+  constexpr int kSegsPerBlock = kFwdThreads / SEG;
+  const size_t smem = fwd_smem_bytes_static<SEG>() + c.extra_smem;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned grid = static_cast<unsigned>((a.T + kSegsPerBlock - 1) / kSegsPerBlock);
+  kern<<<grid, kFwdThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int SF, int DT, int SEG, int NC, bool VEC>
+cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
+  if (c.km == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 0>(a, c, st);
+  return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 0>(a, c, st);
+}
+
+template <int SF, int DT>
+cudaError_t launch_fwd(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  if (!c.vec) {
+    if (c.seg == 32 && c.nc == 18) return launch_fwd_mode<SF, DT, 32, 18, false>(a, c, st);
+    return cudaErrorInvalidConfiguration;
+  }
+#define MR_FWD_CASE(S, N) \
+  if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true>(a, c, st);
+  MR_FWD_VEC_CONFIGS(MR_FWD_CASE)
+#undef MR_FWD_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
+template <int SF, int DT, int SEG, int W, int NC, bool VEC, int OP>
+cudaError_t launch_bwd_inst(const BwdArgs& a, cudaStream_t st) {
+  using S = BwdShape<SEG, W>;
+  const unsigned grid = static_cast<unsigned>((a.T + S::RPB - 1) / S::RPB);
+  router_bwd_kernel<SF, DT, SEG, W, NC, VEC, OP><<<grid, S::THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int SF, int DT>
+cudaError_t launch_bwd(const BwdArgs& a, const BwdConfig& c, cudaStream_t st) {
+#define MR_BWD_CASE(S, W, N)                                                     \
+  if (c.seg == S && c.w == W && c.nc == N) {                                     \
+    if (c.vec) {                                                                 \
+      return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, true, 0>(a, st)        \
+                       : launch_bwd_inst<SF, DT, S, W, N, true, 1>(a, st);       \
+    }                                                                            \
+    return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, false, 0>(a, st)         \
+                     : launch_bwd_inst<SF, DT, S, W, N, false, 1>(a, st);        \
+  }
+  MR_BWD_CONFIGS(MR_BWD_CASE)
+#undef MR_BWD_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
+// One pair per translation unit.
+cudaError_t launch_fwd_softmax_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_sigmoid_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_bwd_any(int sf, int dt, const BwdArgs&, const BwdConfig&, cudaStream_t);
+
+}  // namespace moe_router

@@ -1,0 +1,210 @@
+"""Python binding of the router's C ABI (include/moe_router.h).
+
+Argument marshalling only: every function checks tensor devices, dtypes and
+shapes, allocates missing outputs with torch, passes raw device pointers and
+the current torch stream to the library, and raises on a nonzero status.
+All router arithmetic runs in the library's CUDA kernels; there is no other
+implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MR_SOFTMAX, MR_SIGMOID = 0, 1
+MR_F32, MR_BF16 = 0, 1
+MR_PATH_AUTO, MR_PATH_WARP, MR_PATH_CTA = 0, 1, 2
+STATUS = {0: "MR_OK", -1: "MR_ERR_INVALID", -2: "MR_ERR_UNSUPPORTED", -3: "MR_ERR_CUDA"}
+
+_SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID}
+_DTYPE = {torch.float32: MR_F32, torch.bfloat16: MR_BF16}
+
+_lib = None
+
+
+class RouterError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = lib().moe_router_strerror(code).decode()
+        super().__init__(f"{fn}: {STATUS.get(code, code)} ({msg})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"router CUDA library not built ({path} missing); run "
+                "`python -m score_top_expert_gb300.build`")
+        L = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.router_topk_fwd.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, vp, vp, vp]
+        L.router_topk_bwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, vp, vp]
+        L.router_aux_scores_fwd.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
+        L.router_aux_scores_bwd.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
+        for fn in ("router_topk_fwd", "router_topk_bwd", "router_aux_scores_fwd",
+                   "router_aux_scores_bwd", "moe_router_force_path",
+                   "moe_router_force_fwd_lanes", "moe_router_version"):
+            getattr(L, fn).restype = ctypes.c_int
+        L.moe_router_force_path.argtypes = [i]
+        L.moe_router_force_fwd_lanes.argtypes = [i]
+        L.moe_router_version.argtypes = []
+        L.moe_router_strerror.argtypes = [i]
+        L.moe_router_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise RouterError(fn, code)
+
+
+def _as_input(t: torch.Tensor, name: str, dtypes) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} dtype {t.dtype} not in {dtypes}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be [T, E]")
+    return t.contiguous()
+
+
+def _score(score_func: str) -> int:
+    try:
+        return _SCORE[score_func]
+    except KeyError:
+        raise ValueError(f"score_func must be one of {list(_SCORE)}") from None
+
+
+def _out(t, shape, dtype, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() \
+            or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
+    return t
+
+
+def router_topk_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax",
+                    num_groups: int = 0, group_topk: int = 0, scaling_factor: float = 1.0,
+                    expert_bias: torch.Tensor | None = None, *, probs=None,
+                    routing_map=None, scores=None):
+    """Top-K router forward.  Returns (probs [T,E] logits dtype,
+    routing_map [T,E] bool, scores [T,E] float32)."""
+    logits = _as_input(logits, "logits", _DTYPE)
+    T, E = logits.shape
+    dev = logits.device
+    if expert_bias is not None:
+        if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
+                or expert_bias.device != dev:
+            raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
+        expert_bias = expert_bias.contiguous()
+    probs = _out(probs, (T, E), logits.dtype, dev, "probs")
+    routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
+    scores = _out(scores, (T, E), torch.float32, dev, "scores")
+    with torch.cuda.device(dev):
+        rc = lib().router_topk_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
+                                   _score(score_func), int(num_groups), int(group_topk),
+                                   float(scaling_factor), _ptr(expert_bias), _ptr(probs),
+                                   _ptr(routing_map), _ptr(scores), _stream(dev))
+    _check("router_topk_fwd", rc)
+    return probs, routing_map, scores
+
+
+def router_topk_bwd(grad_probs: torch.Tensor, routing_map: torch.Tensor,
+                    scores: torch.Tensor, K: int, score_func: str = "softmax",
+                    scaling_factor: float = 1.0, *, grad_logits=None):
+    """Top-K router backward.  Returns grad_logits [T,E] in grad_probs' dtype."""
+    grad_probs = _as_input(grad_probs, "grad_probs", _DTYPE)
+    routing_map = _as_input(routing_map, "routing_map", (torch.bool, torch.uint8))
+    scores = _as_input(scores, "scores", (torch.float32,))
+    T, E = grad_probs.shape
+    if routing_map.shape != grad_probs.shape or scores.shape != grad_probs.shape:
+        raise ValueError("grad_probs, routing_map and scores must have the same shape")
+    dev = grad_probs.device
+    grad_logits = _out(grad_logits, (T, E), grad_probs.dtype, dev, "grad_logits")
+    with torch.cuda.device(dev):
+        rc = lib().router_topk_bwd(_ptr(grad_probs), _ptr(routing_map), _ptr(scores),
+                                   _DTYPE[grad_probs.dtype], T, E, int(K),
+                                   _score(score_func), float(scaling_factor),
+                                   _ptr(grad_logits), _stream(dev))
+    _check("router_topk_bwd", rc)
+    return grad_logits
+
+
+def router_aux_scores_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax", *,
+                          scores=None, routing_map=None, intermediate=None):
+    """Aux-loss scores forward.  Returns (scores q [T,E] float32,
+    routing_map [T,E] bool, intermediate [T,E] float32: sigmoid(x) for sigmoid,
+    q for softmax)."""
+    logits = _as_input(logits, "logits", _DTYPE)
+    T, E = logits.shape
+    dev = logits.device
+    scores = _out(scores, (T, E), torch.float32, dev, "scores")
+    routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
+    if score_func == "sigmoid" or intermediate is not None:
+        intermediate = _out(intermediate, (T, E), torch.float32, dev, "intermediate")
+    with torch.cuda.device(dev):
+        rc = lib().router_aux_scores_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
+                                         _score(score_func), _ptr(scores), _ptr(routing_map),
+                                         _ptr(intermediate), _stream(dev))
+    _check("router_aux_scores_fwd", rc)
+    return scores, routing_map, (intermediate if intermediate is not None else scores)
+
+
+def router_aux_scores_bwd(grad_scores: torch.Tensor, saved: torch.Tensor, K: int,
+                          score_func: str = "softmax", dtype: torch.dtype = torch.float32,
+                          *, grad_logits=None):
+    """Aux-loss scores backward.  ``saved`` is the forward's scores (softmax)
+    or intermediate (sigmoid).  Returns grad_logits [T,E] in ``dtype``."""
+    grad_scores = _as_input(grad_scores, "grad_scores", (torch.float32,))
+    saved = _as_input(saved, "saved", (torch.float32,))
+    if saved.shape != grad_scores.shape:
+        raise ValueError("grad_scores and saved must have the same shape")
+    if dtype not in _DTYPE:
+        raise ValueError(f"dtype must be one of {list(_DTYPE)}")
+    T, E = grad_scores.shape
+    dev = grad_scores.device
+    grad_logits = _out(grad_logits, (T, E), dtype, dev, "grad_logits")
+    with torch.cuda.device(dev):
+        rc = lib().router_aux_scores_bwd(_ptr(grad_scores), _ptr(saved), _DTYPE[dtype], T, E,
+                                         int(K), _score(score_func), _ptr(grad_logits),
+                                         _stream(dev))
+    _check("router_aux_scores_bwd", rc)
+    return grad_logits
+
+
+def force_path(path: str) -> str:
+    """Force the forward kernel path: 'auto', 'warp' or 'cta'; returns the previous."""
+    names = {"auto": MR_PATH_AUTO, "warp": MR_PATH_WARP, "cta": MR_PATH_CTA}
+    prev = lib().moe_router_force_path(names[path])
+    if prev < 0:
+        raise RouterError("moe_router_force_path", prev)
+    return {v: k for k, v in names.items()}[prev]
+
+
+def force_fwd_lanes(lanes: int) -> int:
+    """Force the lanes per row of the segment forward (0 = automatic)."""
+    prev = lib().moe_router_force_fwd_lanes(int(lanes))
+    if prev < 0:
+        raise RouterError("moe_router_force_fwd_lanes", prev)
+    return prev

@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from score_top_expert_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    import score_top_expert_gb300.router as r
+    return r.lib()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"MR_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_router_calls():
+    names = declared_functions()
+    for n in ("router_topk_fwd", "router_topk_bwd", "router_aux_scores_fwd",
+              "router_aux_scores_bwd", "moe_router_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(L, n)
+
+
+def test_library_is_built_for_sm_103a_only():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
+    assert B.up_to_date()
+
+
+def test_version_and_strerror(L):
+    assert L.moe_router_version() == 100
+    for code in (0, -1, -2, -3, 12345):
+        assert isinstance(L.moe_router_strerror(code), bytes)
+    assert L.moe_router_strerror(-1) == b"invalid argument"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails its checks
+
+
+def fwd(L, **kw):
+    a = dict(logits=FAKE, dtype=0, T=4, E=16, K=2, sf=0, ng=0, gk=0, c=1.0, bias=None,
+             probs=FAKE, rmap=FAKE, scores=FAKE)
+    a.update(kw)
+    return L.router_topk_fwd(a["logits"], a["dtype"], a["T"], a["E"], a["K"], a["sf"],
+                             a["ng"], a["gk"], a["c"], a["bias"], a["probs"], a["rmap"],
+                             a["scores"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), -1), (dict(E=0), -1), (dict(K=0), -1), (dict(K=17), -1),
+    (dict(dtype=2), -1), (dict(sf=2), -1), (dict(T=1 << 20, E=4096, K=4), -1),
+    (dict(logits=None), -1), (dict(probs=None), -1), (dict(rmap=None), -1),
+    (dict(scores=None), -1), (dict(ng=-1), -1),
+    (dict(ng=3, gk=1), -1),                   # E % num_groups != 0
+    (dict(ng=4, gk=0), -1), (dict(ng=4, gk=5), -1),
+    (dict(ng=4, gk=2, K=3), -1),              # K % group_topk != 0
+    (dict(ng=4, gk=1, K=8), -1),              # K / group_topk > E / num_groups
+    (dict(E=2305, K=4), -2), (dict(E=2304, K=37), -2),
+    (dict(E=64, K=4, ng=64, gk=4), -2),       # more groups than supported
+])
+def test_topk_fwd_rejects(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def test_topk_fwd_zero_tokens_is_a_noop(L):
+    # T = 0 passes the checks and returns without launching anything
+    assert fwd(L, T=0, logits=None) == 0
+    assert fwd(L, T=0, logits=None, probs=None, rmap=None, scores=None) == 0
+    assert fwd(L, T=0, logits=None, ng=4, gk=2, K=4) == 0
+
+
+def test_other_calls_reject(L):
+    f = FAKE
+    assert L.router_topk_bwd(None, f, f, 0, 4, 16, 2, 0, 1.0, f, None) == -1
+    assert L.router_topk_bwd(f, f, f, 0, 4, 16, 2, 0, 1.0, None, None) == -1
+    assert L.router_topk_bwd(None, None, None, 0, 0, 16, 2, 0, 1.0, None, None) == 0
+    assert L.router_topk_bwd(f, f, f, 0, 4, 16, 17, 0, 1.0, f, None) == -1
+    assert L.router_topk_bwd(f, f, f, 0, 4, 4000, 2, 0, 1.0, f, None) == -2
+    assert L.router_topk_bwd(None, None, None, 0, 0, 16, 2, 0, 1.0, f, None) == 0
+    # sigmoid aux needs the intermediate; softmax does not
+    assert L.router_aux_scores_fwd(f, 0, 4, 16, 2, 1, f, f, None, None) == -1
+    assert L.router_aux_scores_fwd(f, 0, 4, 16, 2, 0, None, f, None, None) == -1
+    assert L.router_aux_scores_fwd(None, 0, 0, 16, 2, 0, f, f, None, None) == 0
+    assert L.router_aux_scores_bwd(None, f, 0, 4, 16, 2, 0, f, None) == -1
+    assert L.router_aux_scores_bwd(f, f, 1, 4, 16, 0, 0, f, None) == -1
+    assert L.router_aux_scores_bwd(None, None, 1, 0, 16, 2, 1, f, None) == 0
+
+
+def test_path_knobs(L):
+    assert L.moe_router_force_path(7) == -1
+    prev = L.moe_router_force_path(1)
+    assert prev in (0, 1, 2)
+    assert L.moe_router_force_path(prev) == 1
+    assert L.moe_router_force_fwd_lanes(12) == -1
+    p = L.moe_router_force_fwd_lanes(16)
+    assert L.moe_router_force_fwd_lanes(p) == 16
+
+
+def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    import score_top_expert_gb300.router as r
+    monkeypatch.setattr(r, "_lib", None)
+    monkeypatch.setattr(r._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        r.lib()

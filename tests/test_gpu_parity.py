@@ -1,0 +1,282 @@
+"""CUDA router vs the CPU oracle, element by element, through the C ABI.
+
+Sizes: the router benchmarks' workloads at full size (the oracle handles
+8192 x 2304 in a few seconds), the decode sweep, and edge shapes (odd E,
+ragged T, K = 1 and K = E, unaligned buffers, heavy ties, every compiled
+lanes-per-row width).
+"""
+import numpy as np
+import pytest
+
+import oracle.router_oracle as O
+from compare import assert_close, compare_map
+from score_top_expert_gb300.workloads import WORKLOADS, make_case, make_workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def R():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from score_top_expert_gb300 import build
+    build.build()
+    import score_top_expert_gb300.router as r
+    r.lib()
+    return r
+
+
+DEV = "cuda:0"
+TD = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def to_dev(a, dtype="f32"):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(DEV).to(TD[dtype])
+
+
+def np64(t):
+    return t.detach().to(torch.float64).cpu().numpy() if t.dtype != torch.bool \
+        else t.cpu().numpy()
+
+
+def run_and_check_topk(R, case, K, sf, c=1.0, ng=0, gk=0, bias=None, check_bwd=True,
+                       tensors=None):
+    """Run fwd (+bwd) on the GPU and compare with the oracle; returns the map report."""
+    dt = case.dtype
+    x = to_dev(case.logits, dt) if tensors is None else tensors["x"]
+    b = None if bias is None else to_dev(bias)
+    kw = {} if tensors is None else tensors.get("out", {})
+    probs, rmap, scores = R.router_topk_fwd(x, K, sf, ng, gk, c, b, **kw)
+    ref = O.topk_fwd(case.logits, K, sf, ng, gk, c, bias)
+    rep = compare_map(rmap.cpu().numpy(), ref["routing_map"], ref["near_tie"])
+    rep.check(f"topk map {sf} {dt}")
+    ok = rep.ok_rows
+    assert_close(np64(probs), ref["probs"], dt, ok, "probs")
+    assert_close(np64(scores), ref["scores"], "f32", None, "scores")
+    assert (rmap.cpu().numpy().sum(axis=1) == K).all()
+    if check_bwd:
+        g = to_dev(case.grad_probs, dt)
+        gx = R.router_topk_bwd(g, rmap, scores, K, sf, c)
+        gref = O.topk_bwd(case.grad_probs, ref["routing_map"], ref["scores"], sf, c)
+        assert_close(np64(gx), gref, dt, ok, "grad_logits")
+    return rep
+
+
+def run_and_check_aux(R, case, K, sf):
+    dt = case.dtype
+    x = to_dev(case.logits, dt)
+    q, rmap, inter = R.router_aux_scores_fwd(x, K, sf)
+    ref = O.aux_scores_fwd(case.logits, K, sf)
+    rep = compare_map(rmap.cpu().numpy(), ref["routing_map"], ref["near_tie"])
+    rep.check(f"aux map {sf}")
+    assert_close(np64(q), ref["scores"], "f32", None, "aux scores")
+    assert_close(np64(inter), ref["saved"], "f32", None, "aux intermediate")
+    gs = to_dev(case.grad_scores)
+    gx = R.router_aux_scores_bwd(gs, inter, K, sf, TD[dt])
+    gref = O.aux_scores_bwd(case.grad_scores, ref["saved"], sf)
+    assert_close(np64(gx), gref, dt, None, "aux grad_logits")
+    return rep
+
+
+# ---------------------------------------------------------------------------
+# the benchmark workloads, full size
+# ---------------------------------------------------------------------------
+TOPK_CASES = [
+    ("t1024_e64_k4", "softmax", "f32"),
+    ("t8192_e256_k4", "softmax", "f32"), ("t8192_e256_k4", "sigmoid", "f32"),
+    ("t8192_e256_k8", "softmax", "f32"), ("t8192_e256_k8", "sigmoid", "f32"),
+    ("t8192_e256_k4", "softmax", "bf16"), ("t8192_e256_k8", "sigmoid", "bf16"),
+    ("t8192_e512_k22", "softmax", "f32"), ("t8192_e512_k22", "sigmoid", "f32"),
+    ("t8192_e2304_k36", "softmax", "f32"), ("t8192_e2304_k36", "sigmoid", "f32"),
+    ("t16384_e256_k8_grouped", "sigmoid", "bf16"),
+]
+
+
+@pytest.mark.parametrize("name,sf,dt", TOPK_CASES, ids=[f"{n}-{s}-{d}" for n, s, d in TOPK_CASES])
+def test_topk_workload(R, name, sf, dt):
+    case, args = make_workload(name, dtype=dt)
+    bias = case.expert_bias
+    rep = run_and_check_topk(R, case, args["K"], sf, args["scaling_factor"],
+                             args["num_groups"], args["group_topk"], bias)
+    print(f"{name} {sf} {dt}: near-tie rows {rep.near_tie_rows}, "
+          f"mismatched rows {rep.mismatched_rows}")
+
+
+AUX_CASES = [("t8192_e512_k22", "softmax"), ("t8192_e512_k22", "sigmoid"),
+             ("t8192_e2304_k36", "softmax"), ("t8192_e2304_k36", "sigmoid")]
+
+
+@pytest.mark.parametrize("name,sf", AUX_CASES, ids=[f"{n}-{s}" for n, s in AUX_CASES])
+def test_aux_workload(R, name, sf):
+    case, args = make_workload(name)
+    run_and_check_aux(R, case, args["K"], sf)
+
+
+def test_duplicate_rows_select_lower_indices(R):
+    case, args = make_workload("t8192_e2304_k36")
+    assert len(case.dup_rows) >= 82
+    x = to_dev(case.logits)
+    _, rmap, _ = R.router_topk_fwd(x, 36, "softmax")
+    got = rmap.cpu().numpy()[case.dup_rows]
+    for r, row in zip(case.dup_rows, got):
+        order = np.lexsort((np.arange(2304), -case.logits[r].astype(np.float64)))
+        want = np.zeros(2304, bool)
+        want[order[:36]] = True
+        assert np.array_equal(row, want), r
+
+
+# ---------------------------------------------------------------------------
+# decode sweep: 1, 2, 4 rows, E = 512, K in 1..10
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_decode_sweep(R, T, dt):
+    for K in (1, 2, 4, 6, 8, 10):
+        case = make_case(T, 512, K, dtype=dt, seed=4242 + T)
+        run_and_check_topk(R, case, K, "softmax")
+
+
+# ---------------------------------------------------------------------------
+# edge shapes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("E", [1, 2, 3, 5, 7, 13, 64, 100, 129, 255, 513, 1000, 2303, 2304])
+def test_odd_and_ragged_shapes(R, E):
+    for sf in ("softmax", "sigmoid"):
+        for K in sorted({1, min(E, 3), min(E, 36), min(E, 17)}):
+            case = make_case(37, E, K, sigma=1.5, seed=E * 31 + K)
+            run_and_check_topk(R, case, K, sf, c=1.7)
+            run_and_check_aux(R, case, K, sf)
+
+
+@pytest.mark.parametrize("E", [4, 16, 36])
+def test_k_equals_e(R, E):
+    for sf in ("softmax", "sigmoid"):
+        case = make_case(50, E, E, seed=E)
+        run_and_check_topk(R, case, E, sf, c=2.0)
+
+
+@pytest.mark.parametrize("T", [0, 1, 7, 31, 33, 257, 1001])
+def test_ragged_token_counts(R, T):
+    for E, K in ((64, 4), (256, 8), (512, 22), (2304, 36)):
+        case = make_case(T, E, K, seed=T + E)
+        if T == 0:
+            x = torch.empty(0, E, device=DEV)
+            p, m, s = R.router_topk_fwd(x, K)
+            assert p.shape == (0, E)
+            continue
+        run_and_check_topk(R, case, K, "softmax")
+
+
+@pytest.mark.parametrize("lanes", [8, 16, 32])
+def test_every_lane_width(R, lanes):
+    prev = R.force_fwd_lanes(lanes)
+    try:
+        for E, K in ((64, 4), (128, 16), (256, 8), (512, 22), (1000, 30), (2304, 36)):
+            for dt in ("f32", "bf16"):
+                case = make_case(300, E, K, dtype=dt, seed=E + lanes)
+                for sf in ("softmax", "sigmoid"):
+                    run_and_check_topk(R, case, K, sf, c=2.5)
+                    run_and_check_topk(R, case, K, sf, c=2.5,
+                                       bias=np.linspace(-0.05, 0.05, E).astype(np.float32))
+                run_and_check_aux(R, case, K, "sigmoid")
+    finally:
+        R.force_fwd_lanes(prev)
+
+
+def test_unaligned_buffers_take_the_elementwise_path(R):
+    T, E, K = 129, 512, 22
+    case = make_case(T, E, K, seed=99)
+    buf = torch.zeros(T * E + 1, device=DEV)
+    x = buf[1:].view(T, E)
+    x.copy_(to_dev(case.logits))
+    assert x.data_ptr() % 16 != 0
+    outs = dict(probs=torch.empty(T * E + 3, device=DEV)[3:].view(T, E))
+    run_and_check_topk(R, case, K, "softmax", tensors={"x": x, "out": outs})
+    run_and_check_topk(R, case, K, "sigmoid", tensors={"x": x, "out": outs})
+
+
+# ---------------------------------------------------------------------------
+# ties
+# ---------------------------------------------------------------------------
+def tie_rows(E, rng):
+    rows = [np.zeros(E), np.full(E, -3.25), rng.integers(-2, 3, E).astype(float),
+            np.where(rng.random(E) < 0.5, 0.0, -0.0),
+            np.round(rng.normal(0, 1, E), 1), np.repeat(rng.normal(0, 1, E // 4 + 1), 4)[:E]]
+    return np.array(rows, dtype=np.float32)
+
+
+@pytest.mark.parametrize("E", [8, 64, 256, 512, 2304])
+def test_tied_logits(R, E):
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    rng = np.random.default_rng(E)
+    x = tie_rows(E, rng)
+    for K in sorted({1, min(E, 4), min(E, 22), min(E, 36)}):
+        for dt in ("f32", "bf16"):
+            case = make_case(x.shape[0], E, K, dtype=dt, seed=1)
+            case.logits = x if dt == "f32" else round_to_bf16_values(x)
+            for sf in ("softmax", "sigmoid"):
+                run_and_check_topk(R, case, K, sf)
+                if dt == "f32":
+                    run_and_check_aux(R, case, K, sf)
+
+
+# ---------------------------------------------------------------------------
+# bias and groups
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("sf", ["softmax", "sigmoid"])
+def test_bias(R, sf):
+    for E, K in ((64, 4), (256, 8), (512, 22), (2304, 36)):
+        case = make_case(513, E, K, seed=E, with_bias=True, bias_range=0.1)
+        run_and_check_topk(R, case, K, sf, c=2.5, bias=case.expert_bias)
+
+
+GROUPED = [  # (E, num_groups, group_topk, K)
+    (256, 8, 4, 8), (256, 8, 1, 8), (256, 8, 8, 8), (256, 4, 2, 12), (256, 16, 4, 8),
+    (256, 32, 8, 16), (64, 2, 1, 6), (512, 8, 2, 22 - 22 % 2), (2304, 16, 4, 36),
+    (2304, 8, 1, 36), (120, 3, 2, 10), (12, 4, 2, 2), (60, 5, 5, 15), (1000, 10, 3, 30),
+]
+
+
+@pytest.mark.parametrize("E,G,gk,K", GROUPED, ids=[f"E{e}-G{g}-gk{k}-K{K}" for e, g, k, K in GROUPED])
+def test_grouped(R, E, G, gk, K):
+    for dt in ("f32", "bf16"):
+        case = make_case(300, E, K, dtype=dt, seed=E + G, with_bias=True)
+        for sf in ("sigmoid", "softmax"):
+            run_and_check_topk(R, case, K, sf, 2.5, G, gk, case.expert_bias)
+            run_and_check_topk(R, case, K, sf, 1.0, G, gk, None)
+
+
+# ---------------------------------------------------------------------------
+# nothing is written outside the outputs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("E", [7, 256, 2304])
+def test_canaries(R, E):
+    T, K = 65, min(E, 8)
+    case = make_case(T, E, K, seed=5)
+    n = T * E
+    pad = 256
+    probs = torch.full((n + pad,), 7.5, device=DEV)
+    rmap = torch.full((n + pad,), True, device=DEV)
+    scores = torch.full((n + pad,), -9.0, device=DEV)
+    out = dict(probs=probs[:n].view(T, E), routing_map=rmap[:n].view(T, E),
+               scores=scores[:n].view(T, E))
+    run_and_check_topk(R, case, K, "sigmoid", tensors={"x": to_dev(case.logits), "out": out},
+                       check_bwd=False)
+    assert (probs[n:] == 7.5).all() and (rmap[n:]).all() and (scores[n:] == -9.0).all()
+    g = to_dev(case.grad_probs)
+    gx = torch.full((n + pad,), 3.0, device=DEV)
+    R.router_topk_bwd(g, out["routing_map"], out["scores"], K, "sigmoid",
+                      grad_logits=gx[:n].view(T, E))
+    q = torch.full((n + pad,), 1.25, device=DEV)
+    R.router_aux_scores_fwd(to_dev(case.logits), K, "softmax", scores=q[:n].view(T, E))
+    torch.cuda.synchronize()
+    assert (gx[n:] == 3.0).all() and (q[n:] == 1.25).all()
+
+
+def test_errors_raise(R):
+    x = torch.zeros(4, 16, device=DEV)
+    with pytest.raises(R.RouterError):
+        R.router_topk_fwd(x, 17)
+    with pytest.raises(R.RouterError):
+        R.router_topk_fwd(x, 4, "sigmoid", num_groups=3, group_topk=1)
