@@ -1,0 +1,570 @@
+"""Benchmark of the GB300 MoE router: effective HBM GB/s of the top-K router
+forward/backward and the aux-score forward/backward at 8192 tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step is one pass of the router's hot path over one batch of synthetic
+tokens: top-K forward, aux-score forward, top-K backward, aux-score backward
+(softmax, fp32 logits, 8192 tokens x 2304 experts, K = 36).  L2 is flushed
+(a write larger than L2) before every kernel, outside that kernel's CUDA
+events.  value = algorithmic bytes of the step / the step's kernel time.
+
+Algorithmic bytes per token row of E experts (d = bytes per logit):
+  top-K fwd  E (d + d + 1 + 4)   logits in; probs, map, scores out (+ bias 4E once)
+  top-K bwd  E (d + 1 + 4 + d)   grad_probs, map, scores in; grad_logits out
+  aux fwd    softmax E (d + 4 + 1); sigmoid E (d + 4 + 1 + 4)
+  aux bwd    E (4 + 4 + d)       grad_scores, saved scores in; grad_logits out
+
+Under torchrun (N > 1) every rank routes its own 8192-token batch (token rows
+are independent: no collective on the data path), the timed region is
+bracketed by barriers, the kernel time is the max over ranks and value is the
+bytes of all ranks over that time ("weak" scaling).
+
+--impl reference times the CPU oracle (float64 numpy, one row at a time, the
+test suite's reference) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "t8192_e2304_k36"
+METRIC = "effective HBM GB/s of router top-k fwd/bwd vs GB300 peak, 8192 tokens"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# byte accounting
+# ---------------------------------------------------------------------------
+def bytes_per_launch(op: str, T: int, E: int, d: int, sf: str = "softmax",
+                     bias: bool = False) -> int:
+    if op == "topk_fwd":
+        return T * E * (2 * d + 5) + (4 * E if bias else 0)
+    if op == "topk_bwd":
+        return T * E * (2 * d + 5)
+    if op == "aux_fwd":
+        return T * E * (d + 5 + (4 if sf == "sigmoid" else 0))
+    if op == "aux_bwd":
+        return T * E * (8 + d)
+    raise ValueError(op)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "score_top_expert_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernels changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    e = t.get("kernels", {}).get(f"{kernel}@{workload}")
+    return None if e is None else int(e["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(f[0]), max=float(f[1]), power=float(f[2]),
+                                 hw=f[4], hwt=f[5], swt=f[6], swp=f[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        load = [r for r in rows if r["power"] > 0.25 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in load:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(load), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Step:
+    """Inputs and outputs of one router step on the device."""
+
+    def __init__(self, R, torch, case, args, dev, sf="softmax"):
+        self.R, self.torch = R, torch
+        T, E = case.logits.shape
+        dt = torch.float32 if case.dtype == "f32" else torch.bfloat16
+        self.dt = dt
+        self.K, self.sf = args["K"], sf
+        self.c, self.ng, self.gk = args["scaling_factor"], args["num_groups"], args["group_topk"]
+        self.x = torch.from_numpy(case.logits).to(dev).to(dt)
+        self.g = torch.from_numpy(case.grad_probs).to(dev).to(dt)
+        self.gs = torch.from_numpy(case.grad_scores).to(dev)
+        self.bias = None if case.expert_bias is None else torch.from_numpy(case.expert_bias).to(dev)
+        self.probs = torch.empty(T, E, dtype=dt, device=dev)
+        self.rmap = torch.empty(T, E, dtype=torch.bool, device=dev)
+        self.scores = torch.empty(T, E, dtype=torch.float32, device=dev)
+        self.gx = torch.empty(T, E, dtype=dt, device=dev)
+        self.q = torch.empty(T, E, dtype=torch.float32, device=dev)
+        self.amap = torch.empty(T, E, dtype=torch.bool, device=dev)
+        self.inter = torch.empty(T, E, dtype=torch.float32, device=dev) if sf == "sigmoid" else None
+        self.agx = torch.empty(T, E, dtype=dt, device=dev)
+        self.T, self.E, self.d = T, E, (4 if dt == torch.float32 else 2)
+
+    def ops(self):
+        R = self
+        return [
+            ("topk_fwd", lambda: R.R.router_topk_fwd(
+                R.x, R.K, R.sf, R.ng, R.gk, R.c, R.bias, probs=R.probs, routing_map=R.rmap,
+                scores=R.scores)),
+            ("aux_fwd", lambda: R.R.router_aux_scores_fwd(
+                R.x, R.K, R.sf, scores=R.q, routing_map=R.amap, intermediate=R.inter)),
+            ("topk_bwd", lambda: R.R.router_topk_bwd(
+                R.g, R.rmap, R.scores, R.K, R.sf, R.c, grad_logits=R.gx)),
+            ("aux_bwd", lambda: R.R.router_aux_scores_bwd(
+                R.gs, R.inter if R.inter is not None else R.q, R.K, R.sf, R.dt,
+                grad_logits=R.agx)),
+        ]
+
+    def bytes(self, op):
+        return bytes_per_launch(op, self.T, self.E, self.d, self.sf, self.bias is not None)
+
+
+def time_ops(torch, stream, flush, ops, reps, warmup):
+    """Per-op device times (ms) over ``reps`` passes, L2 flushed before each op."""
+    for _ in range(warmup):
+        for _, fn in ops:
+            flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in ops] for _ in range(reps)]
+    torch.cuda._sleep(2_000_000)  # let the host run ahead of the GPU
+    for r in range(reps):
+        for i, (_, fn) in enumerate(ops):
+            flush.zero_()
+            ev[r][i][0].record(stream)
+            fn()
+            ev[r][i][1].record(stream)
+    torch.cuda.synchronize()
+    return [[ev[r][i][0].elapsed_time(ev[r][i][1]) for r in range(reps)]
+            for i in range(len(ops))]
+
+
+def gpu_arm(a, world, rank, local):
+    import torch
+
+    import score_top_expert_gb300.router as R
+    from score_top_expert_gb300 import build
+    from score_top_expert_gb300.workloads import make_workload
+
+    build.build()
+    R.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    peak, peak_kind = hbm_peak()
+
+    case, args = make_workload(WORKLOAD)
+    step = Step(R, torch, case, args, dev, "softmax")
+    ops = step.ops()
+
+    # ---- the timed region: K steps ------------------------------------------
+    for _ in range(a.warmup):
+        for _, fn in ops:
+            flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in ops] for _ in range(a.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        wall0 = time.perf_counter()
+        torch.cuda._sleep(2_000_000)
+        t_all0.record(stream)
+        for r in range(a.steps):
+            for i, (_, fn) in enumerate(ops):
+                flush.zero_()
+                ev[r][i][0].record(stream)
+                fn()
+                ev[r][i][1].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall1 = time.perf_counter()
+    per_op = [[ev[r][i][0].elapsed_time(ev[r][i][1]) for r in range(a.steps)]
+              for i in range(len(ops))]
+    step_ms = [sum(per_op[i][r] for i in range(len(ops))) for r in range(a.steps)]
+    kernel_ms = max_over_ranks(sum(step_ms), world, dev)
+    region_ms = max_over_ranks(t_all0.elapsed_time(t_all1), world, dev)
+    step_bytes = sum(step.bytes(n) for n, _ in ops)
+    value = world * step_bytes * a.steps / (kernel_ms * 1e-3) / 1e9
+
+    kern = {}
+    for i, (n, _) in enumerate(ops):
+        avg = sum(per_op[i]) / len(per_op[i])
+        kern[n] = dict(avg_us=round(avg * 1e3, 2), gbs=round(step.bytes(n) / (avg * 1e-3) / 1e9, 1),
+                       frac=round(step.bytes(n) / (avg * 1e-3) / 1e9 / peak, 4),
+                       bytes=step.bytes(n))
+    dom = max(kern, key=lambda n: kern[n]["avg_us"])
+
+    # ---- end to end through the public API with host buffers ----------------
+    e2e = e2e_arm(torch, R, step, stream, max(3, min(a.steps, 20)), world, dev)
+
+    if rank != 0:
+        return None
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(kernel_ms / a.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} softmax: router_topk_fwd + router_aux_scores_fwd"
+                               " + router_topk_bwd + router_aux_scores_bwd",
+                   "tokens": 8192, "experts": 2304, "topk": 36, "score_func": "softmax",
+                   "logits_dtype": "f32", "tokens_per_gpu": 8192,
+                   "parallelism": f"data-parallel x{world} (independent token batches)",
+                   "l2": "flushed before every kernel (write of "
+                         f"{flush.numel() * 4 >> 20} MiB), outside the kernel events",
+                   "peak_hbm_gbs": peak, "peak_kind": peak_kind},
+        "gpu_launches": len(ops) * a.steps,
+        "region_ms_per_step": round(region_ms / a.steps, 4),
+        "wall_s": round(wall1 - wall0, 3),
+        "kernels": kern,
+        "roofline": {"bound": "hbm", "kernel": dom,
+                     "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": kern[dom]["frac"], "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": kern[dom]["bytes"],
+                     "traffic": traffic_for(dom, WORKLOAD)},
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if not a.no_extra:
+        out["breakdown"] = breakdown(torch, R, stream, flush, dev, peak)
+        out["decode_us"] = decode_latency(torch, R, stream, dev)
+    out["cpu_baseline"] = cpu_baseline(a.cpu_seconds)
+    return out
+
+
+def e2e_arm(torch, R, step, stream, reps, world, dev):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in, the four router calls, every output copied back, per step."""
+    hx = step.x.cpu().pin_memory()
+    hg = step.g.cpu().pin_memory()
+    hgs = step.gs.cpu().pin_memory()
+    outs = [step.probs, step.rmap, step.scores, step.gx, step.q, step.amap, step.agx]
+    if step.inter is not None:
+        outs.append(step.inter)
+    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hg, hgs))
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def one():
+        step.x.copy_(hx, non_blocking=True)
+        step.g.copy_(hg, non_blocking=True)
+        step.gs.copy_(hgs, non_blocking=True)
+        for _, fn in step.ops():
+            fn()
+        for d, h in zip(outs, hout):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    step_bytes = sum(step.bytes(n) for n, _ in step.ops())
+    return {"value": round(world * step_bytes * reps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / reps, 4)}
+
+
+def breakdown(torch, R, stream, flush, dev, peak):
+    """Per-kernel effective GB/s on the other benchmark workloads."""
+    from score_top_expert_gb300.workloads import make_workload
+    res = {}
+    for name, sfs, dts in (("t8192_e512_k22", ("softmax", "sigmoid"), ("f32",)),
+                           ("t8192_e2304_k36", ("softmax", "sigmoid"), ("f32",)),
+                           ("t8192_e256_k8", ("softmax", "sigmoid"), ("f32", "bf16")),
+                           ("t16384_e256_k8_grouped", ("sigmoid",), ("bf16",))):
+        for dt in dts:
+            case, args = make_workload(name, dtype=dt)
+            for sf in sfs:
+                st = Step(R, torch, case, args, dev, sf)
+                ops = st.ops()
+                t = time_ops(torch, stream, flush, ops, 20, 3)
+                row = {}
+                for i, (n, _) in enumerate(ops):
+                    med = statistics.median(t[i])
+                    gbs = st.bytes(n) / (med * 1e-3) / 1e9
+                    row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
+                              "frac": round(gbs / peak, 3)}
+                res[f"{name}/{sf}/{dt}"] = row
+                del st
+    return res
+
+
+def decode_latency(torch, R, stream, dev):
+    """Decode sweep: 1, 2, 4 rows x 512 experts, softmax, K in 1..10: device
+    time per launch from a CUDA graph of 100 launches (L2-warm)."""
+    from score_top_expert_gb300.workloads import make_case
+    res = {}
+    for T in (1, 2, 4):
+        case = make_case(T, 512, 10, seed=77 + T)
+        x = torch.from_numpy(case.logits).to(dev)
+        p = torch.empty(T, 512, device=dev)
+        m = torch.empty(T, 512, dtype=torch.bool, device=dev)
+        s = torch.empty(T, 512, device=dev)
+        for K in (1, 2, 4, 6, 8, 10):
+            def launch():
+                R.router_topk_fwd(x, K, "softmax", probs=p, routing_map=m, scores=s)
+            launch()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(100):
+                    launch()
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[f"T{T}_K{K}"] = round(e0.elapsed_time(e1) * 1e3 / 500, 2)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle
+# ---------------------------------------------------------------------------
+def oracle_step(O, case, K, rows):
+    """The oracle over ``rows`` token rows of the workload: the same four ops."""
+    x = case.logits[rows]
+    f = O.topk_fwd(x, K, "softmax")
+    a = O.aux_scores_fwd(x, K, "softmax")
+    O.topk_bwd(case.grad_probs[rows], f["routing_map"], f["scores"], "softmax")
+    O.aux_scores_bwd(case.grad_scores[rows], a["saved"], "softmax")
+
+
+def cpu_baseline(seconds: float):
+    import oracle.router_oracle as O
+    from score_top_expert_gb300.workloads import make_workload
+    case, args = make_workload(WORKLOAD)
+    E, K = case.logits.shape[1], args["K"]
+    row_bytes = sum(bytes_per_launch(op, 1, E, 4) for op in
+                    ("topk_fwd", "aux_fwd", "topk_bwd", "aux_bwd"))
+    done, t0 = 0, time.perf_counter()
+    chunk = 128
+    while time.perf_counter() - t0 < seconds and done + chunk <= case.logits.shape[0]:
+        oracle_step(O, case, K, slice(done, done + chunk))
+        done += chunk
+    dt = time.perf_counter() - t0
+    return {"value": round(row_bytes * done / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"first {done} of 8192 token rows of {WORKLOAD} (softmax, fp32): "
+                      f"the four ops, float64 numpy, one thread, {dt:.1f} s"}
+
+
+def reference_arm(a, world, rank):
+    """The oracle as the reference arm: each step runs the four ops over a
+    bounded sample of the workload's rows on the host cores."""
+    if rank != 0:
+        return None
+    import oracle.router_oracle as O
+    from score_top_expert_gb300.workloads import make_workload
+    case, args = make_workload(WORKLOAD)
+    E, K = case.logits.shape[1], args["K"]
+    rows_per_step = 64
+    row_bytes = sum(bytes_per_launch(op, 1, E, 4) for op in
+                    ("topk_fwd", "aux_fwd", "topk_bwd", "aux_bwd"))
+    for w in range(a.warmup):
+        oracle_step(O, case, K, slice(w * rows_per_step, (w + 1) * rows_per_step))
+    times = []
+    for s in range(a.steps):
+        lo = (s * rows_per_step) % (8192 - rows_per_step)
+        t0 = time.perf_counter()
+        oracle_step(O, case, K, slice(lo, lo + rows_per_step))
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = row_bytes * rows_per_step * a.steps / total / 1e9
+    sample = (f"{rows_per_step} token rows per step of {WORKLOAD} (softmax, fp32): the four "
+              "ops, float64 numpy, one thread")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": round(total / a.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} softmax: the four router ops (bounded sample)",
+                       "tokens": 8192, "experts": 2304, "topk": 36},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def profile_run(a):
+    """Untimed steps for an ncu capture: every op once per step, no flush."""
+    import torch
+
+    import score_top_expert_gb300.router as R
+    from score_top_expert_gb300 import build
+    from score_top_expert_gb300.workloads import make_workload
+    build.build()
+    dev = torch.device("cuda", 0)
+    case, args = make_workload(a.profile)
+    st = Step(R, torch, case, args, dev, a.profile_score)
+    for _ in range(a.warmup + a.steps):
+        for _, fn in st.ops():
+            fn()
+    torch.cuda.synchronize()
+    print(f"profile run done: {a.profile} {a.profile_score}, {a.warmup + a.steps} steps")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="length of the CPU-oracle baseline sample")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload breakdown and the decode sweep")
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="run W + K untimed steps of the four ops on a named workload "
+                         "(softmax; for ncu captures) and print nothing else")
+    ap.add_argument("--profile-score", default="softmax", choices=("softmax", "sigmoid"))
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if a.profile:
+        profile_run(a)
+        return
+    if a.impl == "reference":
+        out = reference_arm(a, world, rank)
+    else:
+        out = gpu_arm(a, world, rank, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and a.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

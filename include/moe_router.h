@@ -187,14 +187,19 @@ MR_API int router_aux_scores_bwd(const float* grad_scores, const float* saved,
 MR_API const char* moe_router_strerror(int code);
 
 /*
- * Kernel path of the top-K and aux forwards.  MR_PATH_AUTO picks by E and K;
- * the others force one path for every shape it supports (shapes it does not
- * support still take the automatic choice).  Process-wide; meant for tests
- * and benchmarks.  The environment variable MOE_ROUTER_FORCE_PATH
- * (auto|warp|cta) sets the initial value.  Returns the previous value, or
- * MR_ERR_INVALID for an unknown path.
+ * Kernel path of the top-K and aux forwards.
+ *   MR_PATH_SEGMENT: the row of logits lives in the registers of 8, 16 or 32
+ *     lanes of a warp (every shape, bias and groups included);
+ *   MR_PATH_STAGED: each warp streams rows through shared memory with bulk
+ *     copies (no bias, no groups; E % 4 == 0 for fp32, E % 8 == 0 for bf16;
+ *     16-byte aligned tensors).
+ * MR_PATH_AUTO takes the staged path from E = 512 up where it applies.  A
+ * forced path that does not apply to a call falls back to the automatic
+ * choice.  Process-wide; meant for tests and benchmarks.  The environment
+ * variable MOE_ROUTER_FORCE_PATH (auto|segment|staged) sets the initial
+ * value.  Returns the previous value, or MR_ERR_INVALID for an unknown path.
  */
-typedef enum { MR_PATH_AUTO = 0, MR_PATH_WARP = 1, MR_PATH_CTA = 2 } mr_path;
+typedef enum { MR_PATH_AUTO = 0, MR_PATH_SEGMENT = 1, MR_PATH_STAGED = 2 } mr_path;
 MR_API int moe_router_force_path(int path);
 
 /*
@@ -205,6 +210,14 @@ MR_API int moe_router_force_path(int path);
  * benchmarks.  Returns the previous value, or MR_ERR_INVALID.
  */
 MR_API int moe_router_force_fwd_lanes(int lanes);
+
+/*
+ * Device status of the current device: 0, or 1 when a kernel gave up a
+ * bounded wait for a bulk copy (about one second) and returned early, leaving
+ * its outputs incomplete.  Reading clears the word.  Synchronous: it waits
+ * for the device's outstanding work (a blocking cudaMemcpy).
+ */
+MR_API int moe_router_device_status(int* status);
 
 /* Library ABI version: 100 * major + minor. */
 MR_API int moe_router_version(void);

@@ -5,11 +5,15 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "moe_router.h"
 #include "router_launch.cuh"
 
 using namespace moe_router;
+
+// Status word the kernels write when a bounded wait gives up (one per device).
+__device__ int g_mr_device_status;
 
 namespace {
 
@@ -23,8 +27,8 @@ int current_path() {
   if (p >= 0) return p;
   p = MR_PATH_AUTO;
   if (const char* env = std::getenv("MOE_ROUTER_FORCE_PATH")) {
-    if (std::strcmp(env, "warp") == 0) p = MR_PATH_WARP;
-    else if (std::strcmp(env, "cta") == 0) p = MR_PATH_CTA;
+    if (std::strcmp(env, "segment") == 0) p = MR_PATH_SEGMENT;
+    else if (std::strcmp(env, "staged") == 0) p = MR_PATH_STAGED;
   }
   int expected = -1;
   g_path.compare_exchange_strong(expected, p);
@@ -32,6 +36,150 @@ int current_path() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- per-device facts, read once -------------------------------------------
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready;
+  int sms;
+  int smem_per_sm;
+  int smem_per_block;
+  int* status;  // device address of g_mr_device_status
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               dev) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_mr_device_status) !=
+            cudaSuccess)
+      return false;
+    d.ready = true;
+  }
+  *out = d;
+  return true;
+}
+
+// ---- staged forward plans, computed once per (device, shape) ----------------
+struct PlanKey {
+  int dev, sf, dt, op, E;
+};
+struct PlanEntry {
+  PlanKey key;
+  StagedPlan plan;
+  bool valid;
+};
+constexpr int kPlanCache = 256;
+PlanEntry g_plans[kPlanCache];
+int g_nplans = 0;
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+StagedLayout staged_layout(int E, int dt) {
+  StagedLayout L{};
+  const int d = dt == MR_F32 ? 4 : 2;
+  L.stage_bytes = round_up(E * d, 128);
+  int off = 2 * L.stage_bytes;
+  L.work_off = off;
+  if (dt == MR_BF16) off += round_up(E * 4, 128);
+  L.cand_off = off;
+  off += kCandPerLane * 32 * 8;
+  L.cand_s_off = off;
+  off += kCandPerLane * 32 * 4;
+  L.mask_off = off;
+  off += round_up(((E + 31) / 32) * 4, 16);
+  L.bar_off = off;
+  off += 16;
+  L.warp_bytes = round_up(off, 128);
+  return L;
+}
+
+int occupancy_any(int sf, int dt, const StagedPlan& p) {
+  if (sf == MR_SOFTMAX)
+    return dt == MR_F32 ? occupancy_staged_softmax_f32(p) : occupancy_staged_softmax_bf16(p);
+  return dt == MR_F32 ? occupancy_staged_sigmoid_f32(p) : occupancy_staged_sigmoid_bf16(p);
+}
+
+// Warps per block that keep the most warps resident per SM (shared memory is
+// the limit: one slice per warp).
+bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, StagedPlan* out) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < g_nplans; ++i) {
+      const PlanKey& k = g_plans[i].key;
+      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E) {
+        *out = g_plans[i].plan;
+        return g_plans[i].valid;
+      }
+    }
+  }
+  StagedPlan p{};
+  p.layout = staged_layout(E, dt);
+  p.op = op;
+  p.nc = E <= 512 ? 4 : (E <= 1024 ? 8 : 18);
+  int best_warps = 0;
+  for (int w = 1; w <= kStagedMaxWarps; ++w) {
+    const int smem = w * p.layout.warp_bytes;
+    if (smem > di.smem_per_block) break;
+    int blocks = di.smem_per_sm / (smem + 1024);
+    blocks = blocks < 2048 / (32 * w) ? blocks : 2048 / (32 * w);
+    blocks = blocks < 32 ? blocks : 32;
+    if (blocks * w > best_warps) {
+      best_warps = blocks * w;
+      p.warps_per_block = w;
+    }
+  }
+  bool valid = best_warps > 0;
+  if (valid) {
+    const int per_sm = occupancy_any(sf, dt, p);
+    valid = per_sm > 0;
+    p.max_blocks = per_sm * di.sms;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_nplans < kPlanCache) g_plans[g_nplans++] = PlanEntry{{dev, sf, dt, op, E}, p, valid};
+  *out = p;
+  return valid;
+}
+
+bool staged_shape_ok(int E, int dt) {
+  return E % 4 == 0 && (dt == MR_F32 || E % 8 == 0) && E <= 2304;
+}
+
+// The staged path serves rows from 512 experts up unless a path is forced.
+bool use_staged(int E, int dt, bool key_on_logit, bool aligned) {
+  if (!key_on_logit || !aligned || !staged_shape_ok(E, dt)) return false;
+  const int path = current_path();
+  if (path == MR_PATH_SEGMENT) return false;
+  if (path == MR_PATH_STAGED) return true;
+  return E >= 512;
+}
+
+int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st) {
+  DeviceInfo di{};
+  if (!device_info(&di)) return MR_ERR_CUDA;
+  StagedPlan p{};
+  if (!staged_plan(di, sf, dt, op, a.E, &p)) return MR_ERR_CUDA;
+  cudaError_t e;
+  if (sf == MR_SOFTMAX) {
+    e = dt == MR_F32 ? launch_staged_softmax_f32(a, p, di.status, st)
+                     : launch_staged_softmax_bf16(a, p, di.status, st);
+  } else {
+    e = dt == MR_F32 ? launch_staged_sigmoid_f32(a, p, di.status, st)
+                     : launch_staged_sigmoid_bf16(a, p, di.status, st);
+  }
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
 
 int check_shape(int dtype, int T, int E, int K, int sf) {
   if (dtype != MR_F32 && dtype != MR_BF16) return MR_ERR_INVALID;
@@ -129,11 +277,22 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
   const bool vec = (E % 4 == 0) && aligned16(logits) && aligned16(probs) &&
                    aligned16(routing_map) && aligned16(scores) &&
                    (expert_bias == nullptr || aligned16(expert_bias));
+  const int km = (expert_bias != nullptr || grouped) ? 1 : 0;
+  if (use_staged(E, dtype, km == 0, vec)) {
+    FwdArgs a{};
+    a.logits = logits;
+    a.probs = probs;
+    a.map = routing_map;
+    a.scores = scores;
+    a.T = T; a.E = E; a.K = K;
+    a.scaling = scaling_factor;
+    return launch_staged_any(score_func, dtype, a, 0, reinterpret_cast<cudaStream_t>(stream));
+  }
   FwdConfig c{};
   if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;
   c.op = 0;
-  c.km = (expert_bias != nullptr || grouped) ? 1 : 0;
+  c.km = km;
   c.extra_smem = grouped ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float) : 0;
 
   FwdArgs a{};
@@ -198,12 +357,6 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   const bool vec = (E % 4 == 0) && aligned16(logits) && aligned16(scores) &&
                    aligned16(routing_map) &&
                    (intermediate == nullptr || aligned16(intermediate));
-  FwdConfig c{};
-  if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
-  c.vec = vec;
-  c.op = 1;
-  c.km = 0;
-  c.extra_smem = 0;
   FwdArgs a{};
   a.logits = logits;
   a.map = routing_map;
@@ -211,6 +364,14 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.intermediate = intermediate;
   a.T = T; a.E = E; a.K = K;
   a.scaling = 1.0f;
+  if (use_staged(E, dtype, true, vec))
+    return launch_staged_any(score_func, dtype, a, 1, reinterpret_cast<cudaStream_t>(stream));
+  FwdConfig c{};
+  if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
+  c.vec = vec;
+  c.op = 1;
+  c.km = 0;
+  c.extra_smem = 0;
   return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -250,7 +411,7 @@ const char* moe_router_strerror(int code) {
 }
 
 int moe_router_force_path(int path) {
-  if (path != MR_PATH_AUTO && path != MR_PATH_WARP && path != MR_PATH_CTA)
+  if (path != MR_PATH_AUTO && path != MR_PATH_SEGMENT && path != MR_PATH_STAGED)
     return MR_ERR_INVALID;
   const int prev = current_path();
   g_path.store(path, std::memory_order_relaxed);
@@ -260,6 +421,22 @@ int moe_router_force_path(int path) {
 int moe_router_force_fwd_lanes(int lanes) {
   if (lanes != 0 && lanes != 8 && lanes != 16 && lanes != 32) return MR_ERR_INVALID;
   return g_fwd_lanes.exchange(lanes, std::memory_order_relaxed);
+}
+
+int moe_router_device_status(int* status) {
+  if (status == nullptr) return MR_ERR_INVALID;
+  DeviceInfo di{};
+  if (!device_info(&di)) return MR_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MR_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MR_ERR_CUDA;
+  }
+  *status = v;
+  return MR_OK;
 }
 
 int moe_router_version(void) { return kVersion; }

@@ -19,8 +19,10 @@
 //      compacted into shared memory (at most 4 per lane).
 //   3. exact rank.  Each candidate counts the candidates above it; the one
 //      with rank K-1 is W.
-// Rows with more candidates than the buffer holds (many equal keys) take an
-// exact bit-by-bit search of W over the whole row instead.
+// Rows with more candidates than the buffer holds (many equal keys) walk the
+// distinct keys down from the largest (one pass each) to the K-th largest
+// key, falling back to a bitwise search after eight distinct values; the
+// index part of W then comes from an ordered prefix count of the equal keys.
 //
 // KM (key mode) 0: no bias, no groups.  The key is the raw logit: softmax and
 //   sigmoid are strictly increasing, so the order is the order of the scores,
@@ -363,34 +365,73 @@ router_fwd_seg_kernel(const FwdArgs a) {
     thr = sm.thr;
     __syncwarp(smask);
   } else {
-    // exact search over the whole row: the K-th largest key value ...
-    uint32_t tk = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t c = tk | (1u << bit);
-      int n = 0;
+    // more candidates than the buffer holds: many equal keys.  Walk the
+    // distinct keys down from the largest until K are covered (one pass per
+    // distinct value), else search the K-th largest key bit by bit.
+    uint32_t tk = max(gmax[0], gmax[1]);
+#pragma unroll
+    for (int o = SEG / 2; o > 0; o >>= 1) tk = max(tk, __shfl_xor_sync(smask, tk, o));
+    int above = 0;
+    bool found = false;
+#pragma unroll 1
+    for (int round = 0; round < 8 && !found; ++round) {
+      int eq = 0;
+      uint32_t below = 0;
 #pragma unroll
       for (int j = 0; j < NC; ++j)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) n += key_at(j, u) >= c;
-      if (seg_sum_int<SEG>(n) >= K) tk = c;
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t k = key_at(j, u);
+          eq += k == tk;
+          if (k < tk) below = max(below, k);
+        }
+      eq = seg_sum_int<SEG>(eq);
+#pragma unroll
+      for (int o = SEG / 2; o > 0; o >>= 1) below = max(below, __shfl_xor_sync(smask, below, o));
+      if (above + eq >= K) found = true;
+      else { above += eq; tk = below; }
     }
-    // ... then, among the keys equal to it, the need-th lowest index
-    int gt = 0;
+    if (!found) {
+      tk = 0;
+#pragma unroll 1
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = tk | (1u << bit);
+        int n = 0;
 #pragma unroll
-    for (int j = 0; j < NC; ++j)
+        for (int j = 0; j < NC; ++j)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) gt += key_at(j, u) > tk;
-    const int need = K - seg_sum_int<SEG>(gt);
-    int ti = 0;
-    for (int bit = 12; bit >= 0; --bit) {
-      const int c = ti | (1 << bit);
-      int n = 0;
+          for (int u = 0; u < 4; ++u) n += key_at(j, u) >= c;
+        if (seg_sum_int<SEG>(n) >= K) tk = c;
+      }
+      int gt = 0;
 #pragma unroll
       for (int j = 0; j < NC; ++j)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) gt += key_at(j, u) > tk;
+      above = seg_sum_int<SEG>(gt);
+    }
+    // the need-th lowest index among the keys equal to tk: chunks in index
+    // order, prefix counts across the segment's lanes
+    const int need = K - above;
+    int ti = -1, run = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (ti >= 0) break;
+      int e = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) e += key_at(j, u) == tk;
+      const int excl = seg_exclusive_scan<SEG>(e);
+      const int tot = __shfl_sync(smask, excl + e, SEG - 1, SEG);
+      int mine = -1;
+      if (run + excl < need && run + excl + e >= need) {
+        int left = need - run - excl;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          n += (key_at(j, u) == tk) && (4 * (li + SEG * j) + u < c);
-      if (seg_sum_int<SEG>(n) < need) ti = c;
+          if (key_at(j, u) == tk && --left == 0 && mine < 0) mine = 4 * (li + SEG * j) + u;
+      }
+      const unsigned who = __ballot_sync(smask, mine >= 0) & smask;
+      if (who) ti = __shfl_sync(smask, mine, __ffs(who) - 1);
+      run += tot;
     }
     thr = pack_key(tk, ti);
     if constexpr (kNeedSelSum) {
@@ -399,7 +440,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
       for (int j = 0; j < NC; ++j)
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (pack_key(key_at(j, u), 4 * (li + SEG * j) + u) >= thr && key_at(j, u) != 0u)
+          if (key_at(j, u) != 0u && pack_key(key_at(j, u), 4 * (li + SEG * j) + u) >= thr)
             part += score_at(j, u);
       sel_sum = seg_sum<SEG>(part);
     }

@@ -6,6 +6,7 @@
 
 #include "router_bwd.cuh"
 #include "router_fwd.cuh"
+#include "router_fwd_staged.cuh"
 
 namespace moe_router {
 
@@ -92,7 +93,83 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdConfig& c, cudaStream_t st) {
   return cudaErrorInvalidConfiguration;
 }
 
-// One pair per translation unit.
+// Staged forward: warps per block, the per-warp slice and the grid cap.
+struct StagedPlan {
+  StagedLayout layout;
+  int warps_per_block;
+  int max_blocks;  // resident blocks per SM x SMs
+  int nc;          // chunks of 4 experts per lane: 4, 8 or 18
+  int op;
+};
+
+#define MR_STAGED_NCS(X) X(4) X(8) X(18)
+
+template <int SF, int DT, int NC, int OP>
+cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* status,
+                               cudaStream_t st) {
+  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP>;
+  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const long long need = (static_cast<long long>(a.T) + p.warps_per_block - 1) / p.warps_per_block;
+  const unsigned grid = static_cast<unsigned>(need < p.max_blocks ? need : p.max_blocks);
+  kern<<<grid, p.warps_per_block * 32, smem, st>>>(a, p.layout, status);
+  return cudaGetLastError();
+}
+
+// Resident blocks per SM of one staged instantiation (occupancy query).
+template <int SF, int DT, int NC, int OP>
+int staged_blocks_per_sm(int warps_per_block, size_t smem) {
+  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, warps_per_block * 32, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int SF, int DT>
+cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
+#define MR_STAGED_CASE(N)                                                          \
+  if (p.nc == N) {                                                                 \
+    return p.op == 0 ? launch_staged_inst<SF, DT, N, 0>(a, p, status, st)          \
+                     : launch_staged_inst<SF, DT, N, 1>(a, p, status, st);         \
+  }
+  MR_STAGED_NCS(MR_STAGED_CASE)
+#undef MR_STAGED_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
+template <int SF, int DT>
+int staged_occupancy(const StagedPlan& p) {
+  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
+#define MR_STAGED_OCC(N)                                                           \
+  if (p.nc == N) {                                                                 \
+    return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0>(p.warps_per_block, smem) \
+                     : staged_blocks_per_sm<SF, DT, N, 1>(p.warps_per_block, smem); \
+  }
+  MR_STAGED_NCS(MR_STAGED_OCC)
+#undef MR_STAGED_OCC
+  return 0;
+}
+
+// One (score function, dtype) pair per translation unit.
+cudaError_t launch_staged_softmax_f32(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+cudaError_t launch_staged_softmax_bf16(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+cudaError_t launch_staged_sigmoid_f32(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+cudaError_t launch_staged_sigmoid_bf16(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+int occupancy_staged_softmax_f32(const StagedPlan&);
+int occupancy_staged_softmax_bf16(const StagedPlan&);
+int occupancy_staged_sigmoid_f32(const StagedPlan&);
+int occupancy_staged_sigmoid_bf16(const StagedPlan&);
+
 cudaError_t launch_fwd_softmax_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_fwd_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_fwd_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);

@@ -17,7 +17,7 @@ from . import build as _build
 
 MR_SOFTMAX, MR_SIGMOID = 0, 1
 MR_F32, MR_BF16 = 0, 1
-MR_PATH_AUTO, MR_PATH_WARP, MR_PATH_CTA = 0, 1, 2
+MR_PATH_AUTO, MR_PATH_SEGMENT, MR_PATH_STAGED = 0, 1, 2
 STATUS = {0: "MR_OK", -1: "MR_ERR_INVALID", -2: "MR_ERR_UNSUPPORTED", -3: "MR_ERR_CUDA"}
 
 _SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID}
@@ -54,11 +54,13 @@ def lib() -> ctypes.CDLL:
         L.router_aux_scores_bwd.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
         for fn in ("router_topk_fwd", "router_topk_bwd", "router_aux_scores_fwd",
                    "router_aux_scores_bwd", "moe_router_force_path",
-                   "moe_router_force_fwd_lanes", "moe_router_version"):
+                   "moe_router_force_fwd_lanes", "moe_router_version",
+                   "moe_router_device_status"):
             getattr(L, fn).restype = ctypes.c_int
         L.moe_router_force_path.argtypes = [i]
         L.moe_router_force_fwd_lanes.argtypes = [i]
         L.moe_router_version.argtypes = []
+        L.moe_router_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         L.moe_router_strerror.argtypes = [i]
         L.moe_router_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -194,8 +196,9 @@ def router_aux_scores_bwd(grad_scores: torch.Tensor, saved: torch.Tensor, K: int
 
 
 def force_path(path: str) -> str:
-    """Force the forward kernel path: 'auto', 'warp' or 'cta'; returns the previous."""
-    names = {"auto": MR_PATH_AUTO, "warp": MR_PATH_WARP, "cta": MR_PATH_CTA}
+    """Force the forward kernel path: 'auto', 'segment' or 'staged'; returns the
+    previous one."""
+    names = {"auto": MR_PATH_AUTO, "segment": MR_PATH_SEGMENT, "staged": MR_PATH_STAGED}
     prev = lib().moe_router_force_path(names[path])
     if prev < 0:
         raise RouterError("moe_router_force_path", prev)
@@ -208,3 +211,11 @@ def force_fwd_lanes(lanes: int) -> int:
     if prev < 0:
         raise RouterError("moe_router_force_fwd_lanes", prev)
     return prev
+
+
+def device_status() -> int:
+    """Read and clear the current device's status word (0 = no kernel gave
+    up a bounded wait).  Synchronous."""
+    v = ctypes.c_int(0)
+    _check("moe_router_device_status", lib().moe_router_device_status(ctypes.byref(v)))
+    return v.value

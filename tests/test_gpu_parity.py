@@ -28,6 +28,15 @@ def R():
 
 
 DEV = "cuda:0"
+PATHS = ["auto", "segment", "staged"]
+
+
+@pytest.fixture(params=PATHS)
+def path(R, request):
+    prev = R.force_path(request.param)
+    yield request.param
+    R.force_path(prev)
+    assert R.device_status() == 0
 TD = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -40,15 +49,29 @@ def np64(t):
         else t.cpu().numpy()
 
 
+_REF_CACHE = {}
+
+
+def oracle_topk(case, K, sf, ng, gk, c, bias, key=None):
+    if key is not None and key in _REF_CACHE:
+        return _REF_CACHE[key]
+    ref = O.topk_fwd(case.logits, K, sf, ng, gk, c, bias)
+    ref["grad"] = O.topk_bwd(case.grad_probs, ref["routing_map"], ref["scores"], sf, c)
+    if key is not None:
+        _REF_CACHE.clear()
+        _REF_CACHE[key] = ref
+    return ref
+
+
 def run_and_check_topk(R, case, K, sf, c=1.0, ng=0, gk=0, bias=None, check_bwd=True,
-                       tensors=None):
+                       tensors=None, ref_key=None):
     """Run fwd (+bwd) on the GPU and compare with the oracle; returns the map report."""
     dt = case.dtype
     x = to_dev(case.logits, dt) if tensors is None else tensors["x"]
     b = None if bias is None else to_dev(bias)
     kw = {} if tensors is None else tensors.get("out", {})
     probs, rmap, scores = R.router_topk_fwd(x, K, sf, ng, gk, c, b, **kw)
-    ref = O.topk_fwd(case.logits, K, sf, ng, gk, c, bias)
+    ref = oracle_topk(case, K, sf, ng, gk, c, bias, ref_key)
     rep = compare_map(rmap.cpu().numpy(), ref["routing_map"], ref["near_tie"])
     rep.check(f"topk map {sf} {dt}")
     ok = rep.ok_rows
@@ -58,16 +81,21 @@ def run_and_check_topk(R, case, K, sf, c=1.0, ng=0, gk=0, bias=None, check_bwd=T
     if check_bwd:
         g = to_dev(case.grad_probs, dt)
         gx = R.router_topk_bwd(g, rmap, scores, K, sf, c)
-        gref = O.topk_bwd(case.grad_probs, ref["routing_map"], ref["scores"], sf, c)
-        assert_close(np64(gx), gref, dt, ok, "grad_logits")
+        assert_close(np64(gx), ref["grad"], dt, ok, "grad_logits")
     return rep
 
 
-def run_and_check_aux(R, case, K, sf):
+def run_and_check_aux(R, case, K, sf, ref_key=None):
     dt = case.dtype
     x = to_dev(case.logits, dt)
     q, rmap, inter = R.router_aux_scores_fwd(x, K, sf)
-    ref = O.aux_scores_fwd(case.logits, K, sf)
+    if ref_key is not None and ref_key in _REF_CACHE:
+        ref = _REF_CACHE[ref_key]
+    else:
+        ref = O.aux_scores_fwd(case.logits, K, sf)
+        if ref_key is not None:
+            _REF_CACHE.clear()
+            _REF_CACHE[ref_key] = ref
     rep = compare_map(rmap.cpu().numpy(), ref["routing_map"], ref["near_tie"])
     rep.check(f"aux map {sf}")
     assert_close(np64(q), ref["scores"], "f32", None, "aux scores")
@@ -94,12 +122,13 @@ TOPK_CASES = [
 
 
 @pytest.mark.parametrize("name,sf,dt", TOPK_CASES, ids=[f"{n}-{s}-{d}" for n, s, d in TOPK_CASES])
-def test_topk_workload(R, name, sf, dt):
+def test_topk_workload(R, path, name, sf, dt):
     case, args = make_workload(name, dtype=dt)
     bias = case.expert_bias
     rep = run_and_check_topk(R, case, args["K"], sf, args["scaling_factor"],
-                             args["num_groups"], args["group_topk"], bias)
-    print(f"{name} {sf} {dt}: near-tie rows {rep.near_tie_rows}, "
+                             args["num_groups"], args["group_topk"], bias,
+                             ref_key=("topk", name, sf, dt))
+    print(f"{name} {sf} {dt} {path}: near-tie rows {rep.near_tie_rows}, "
           f"mismatched rows {rep.mismatched_rows}")
 
 
@@ -108,12 +137,28 @@ AUX_CASES = [("t8192_e512_k22", "softmax"), ("t8192_e512_k22", "sigmoid"),
 
 
 @pytest.mark.parametrize("name,sf", AUX_CASES, ids=[f"{n}-{s}" for n, s in AUX_CASES])
-def test_aux_workload(R, name, sf):
+def test_aux_workload(R, path, name, sf):
     case, args = make_workload(name)
-    run_and_check_aux(R, case, args["K"], sf)
+    run_and_check_aux(R, case, args["K"], sf, ref_key=("aux", name, sf))
 
 
-def test_duplicate_rows_select_lower_indices(R):
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E", [8, 64, 256, 512, 520, 1000, 1024, 2048, 2304])
+def test_staged_shapes(R, E, dt):
+    prev = R.force_path("staged")
+    try:
+        for K in sorted({1, min(E, 4), min(E, 22), min(E, 36)}):
+            case = make_case(129, E, K, dtype=dt, sigma=1.5, seed=E + K)
+            for sf in ("softmax", "sigmoid"):
+                run_and_check_topk(R, case, K, sf, c=2.5)
+                if dt == "f32":
+                    run_and_check_aux(R, case, K, sf)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
+
+
+def test_duplicate_rows_select_lower_indices(R, path):
     case, args = make_workload("t8192_e2304_k36")
     assert len(case.dup_rows) >= 82
     x = to_dev(case.logits)
@@ -207,7 +252,7 @@ def tie_rows(E, rng):
 
 
 @pytest.mark.parametrize("E", [8, 64, 256, 512, 2304])
-def test_tied_logits(R, E):
+def test_tied_logits(R, path, E):
     from score_top_expert_gb300.workloads import round_to_bf16_values
     rng = np.random.default_rng(E)
     x = tie_rows(E, rng)
