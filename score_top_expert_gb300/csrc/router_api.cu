@@ -84,21 +84,19 @@ int g_nplans = 0;
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-StagedLayout staged_layout(int E, int dt) {
+int staged_nc(int E) { return E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18)); }
+
+StagedLayout staged_layout(int nc, int dt) {
   StagedLayout L{};
   const int d = dt == MR_F32 ? 4 : 2;
-  L.stage_bytes = round_up(E * d, 128);
+  L.stage_bytes = 128 * nc * d;  // 32 * nc chunks of four logits
   int off = 2 * L.stage_bytes;
-  L.work_off = off;
-  if (dt == MR_BF16) off += round_up(E * 4, 128);
   L.cand_off = off;
   off += kCandPerLane * 32 * 8;
-  L.cand_s_off = off;
-  off += kCandPerLane * 32 * 4;
   L.mask_off = off;
-  off += round_up(((E + 31) / 32) * 4, 16);
-  L.bar_off = off;
-  off += 16;
+  off += 16 * nc;  // one bit per padded expert
+  L.bar_off = round_up(off, 16);
+  off = L.bar_off + 32;
   L.warp_bytes = round_up(off, 128);
   return L;
 }
@@ -125,9 +123,10 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, StagedPlan
     }
   }
   StagedPlan p{};
-  p.layout = staged_layout(E, dt);
+  p.nc = staged_nc(E);
+  p.full = E == 128 * p.nc;
+  p.layout = staged_layout(p.nc, dt);
   p.op = op;
-  p.nc = E <= 512 ? 4 : (E <= 1024 ? 8 : 18);
   int best_warps = 0;
   for (int w = 1; w <= kStagedMaxWarps; ++w) {
     const int smem = w * p.layout.warp_bytes;
@@ -135,7 +134,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, StagedPlan
     int blocks = di.smem_per_sm / (smem + 1024);
     blocks = blocks < 2048 / (32 * w) ? blocks : 2048 / (32 * w);
     blocks = blocks < 32 ? blocks : 32;
-    if (blocks * w > best_warps) {
+    if (blocks * w >= best_warps) {
       best_warps = blocks * w;
       p.warps_per_block = w;
     }

@@ -35,9 +35,36 @@ __device__ __forceinline__ unsigned long long pack_key(uint32_t key, int idx) {
 
 // ---------------------------------------------------------------------------
 // score functions in fp32
+//
+// e^t is computed as 2^(t log2 e) with the hardware base-2 exponential
+// (ex2.approx, about 2 ulp).  For softmax the argument is one FFMA,
+// x * log2e - max * log2e: the rounding of max * log2e scales every e of the
+// row by the same factor, which cancels in the normalisation, and the
+// rounding of the FFMA itself costs at most |x - max| * 2^-24 relative, which
+// is negligible where e is not.  The sigmoid takes the hardware reciprocal
+// (rcp.approx, about 1 ulp) of 1 + e^-x; it saturates correctly to 0 and 1.
 // ---------------------------------------------------------------------------
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float t) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float t) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+// exp(x - max) given max_l2e = max * log2e
+__device__ __forceinline__ float exp_shifted(float x, float max_l2e) {
+  return ex2_approx(fmaf(x, kLog2e, -max_l2e));
+}
+
 __device__ __forceinline__ float sigmoid_f32(float x) {
-  return __frcp_rn(1.0f + expf(-x));
+  return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
 }
 
 // ---------------------------------------------------------------------------

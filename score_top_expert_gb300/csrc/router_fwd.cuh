@@ -220,14 +220,14 @@ router_fwd_seg_kernel(const FwdArgs a) {
 
   float row_max = 0.0f, inv_sum = 1.0f;
   if constexpr (SF == SF_SOFTMAX) {
-    row_max = seg_max<SEG>(fmaxf(hmax[0], hmax[1]));
+    row_max = seg_max<SEG>(fmaxf(hmax[0], hmax[1])) * kLog2e;
     float sum = 0.0f;
 #pragma unroll
     for (int j = 0; j < NC; ++j)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (elem_ok(j, u)) {
-          const float e = expf(v[j][u] - row_max);
+          const float e = exp_shifted(v[j][u], row_max);
           if constexpr (KM == 1) v[j][u] = e;
           sum += e;
         }
@@ -298,7 +298,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
   };
   auto score_at = [&](int j, int u) -> float {  // the score s of the element
     if constexpr (KM == 1) return v[j][u];
-    else if constexpr (SF == SF_SOFTMAX) return expf(v[j][u] - row_max) * inv_sum;
+    else if constexpr (SF == SF_SOFTMAX) return exp_shifted(v[j][u], row_max) * inv_sum;
     else return sigmoid_f32(v[j][u]);
   };
 

@@ -98,16 +98,17 @@ struct StagedPlan {
   StagedLayout layout;
   int warps_per_block;
   int max_blocks;  // resident blocks per SM x SMs
-  int nc;          // chunks of 4 experts per lane: 4, 8 or 18
+  int nc;          // chunks of 4 experts per lane: 2, 4, 8 or 18
   int op;
+  bool full;       // E == 128 * nc: no padding chunks
 };
 
-#define MR_STAGED_NCS(X) X(4) X(8) X(18)
+#define MR_STAGED_NCS(X) X(2) X(4) X(8) X(18)
 
-template <int SF, int DT, int NC, int OP>
+template <int SF, int DT, int NC, int OP, bool FULL>
 cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* status,
                                cudaStream_t st) {
-  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP>;
+  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP, FULL>;
   const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -121,9 +122,9 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
 }
 
 // Resident blocks per SM of one staged instantiation (occupancy query).
-template <int SF, int DT, int NC, int OP>
+template <int SF, int DT, int NC, int OP, bool FULL>
 int staged_blocks_per_sm(int warps_per_block, size_t smem) {
-  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP>;
+  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP, FULL>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -137,10 +138,13 @@ int staged_blocks_per_sm(int warps_per_block, size_t smem) {
 
 template <int SF, int DT>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
-#define MR_STAGED_CASE(N)                                                          \
-  if (p.nc == N) {                                                                 \
-    return p.op == 0 ? launch_staged_inst<SF, DT, N, 0>(a, p, status, st)          \
-                     : launch_staged_inst<SF, DT, N, 1>(a, p, status, st);         \
+#define MR_STAGED_CASE(N)                                                             \
+  if (p.nc == N) {                                                                    \
+    if (p.full)                                                                       \
+      return p.op == 0 ? launch_staged_inst<SF, DT, N, 0, true>(a, p, status, st)     \
+                       : launch_staged_inst<SF, DT, N, 1, true>(a, p, status, st);    \
+    return p.op == 0 ? launch_staged_inst<SF, DT, N, 0, false>(a, p, status, st)      \
+                     : launch_staged_inst<SF, DT, N, 1, false>(a, p, status, st);     \
   }
   MR_STAGED_NCS(MR_STAGED_CASE)
 #undef MR_STAGED_CASE
@@ -150,10 +154,14 @@ cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cu
 template <int SF, int DT>
 int staged_occupancy(const StagedPlan& p) {
   const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
-#define MR_STAGED_OCC(N)                                                           \
-  if (p.nc == N) {                                                                 \
-    return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0>(p.warps_per_block, smem) \
-                     : staged_blocks_per_sm<SF, DT, N, 1>(p.warps_per_block, smem); \
+#define MR_STAGED_OCC(N)                                                                 \
+  if (p.nc == N) {                                                                       \
+    const int w = p.warps_per_block;                                                     \
+    if (p.full)                                                                          \
+      return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0, true>(w, smem)               \
+                       : staged_blocks_per_sm<SF, DT, N, 1, true>(w, smem);              \
+    return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0, false>(w, smem)                \
+                     : staged_blocks_per_sm<SF, DT, N, 1, false>(w, smem);               \
   }
   MR_STAGED_NCS(MR_STAGED_OCC)
 #undef MR_STAGED_OCC
