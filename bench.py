@@ -6,8 +6,11 @@ forward/backward and the aux-score forward/backward at 8192 tokens.
 One step is one pass of the router's hot path over one batch of synthetic
 tokens: top-K forward, aux-score forward, top-K backward, aux-score backward
 (softmax, fp32 logits, 8192 tokens x 2304 experts, K = 36).  L2 is flushed
-(a write larger than L2) before every kernel, outside that kernel's CUDA
-events.  value = algorithmic bytes of the step / the step's kernel time.
+before every kernel, outside that kernel's CUDA events: a write of a buffer
+larger than L2, then a read of a second one, so that the written lines are
+back in HBM before the kernel starts (otherwise their write-back would land
+inside the kernel's time).  value = algorithmic bytes of the step / the
+step's kernel time.
 
 Algorithmic bytes per token row of E experts (d = bytes per logit):
   top-K fwd  E (d + d + 1 + 4)   logits in; probs, map, scores out (+ bias 4E once)
@@ -225,6 +228,25 @@ class Step:
         return bytes_per_launch(op, self.T, self.E, self.d, self.sf, self.bias is not None)
 
 
+class L2Flush:
+    """Evict L2 with clean lines: write one buffer larger than L2, then read
+    another one of the same size (the write-backs of the first happen during
+    the read, not during the next timed kernel)."""
+
+    def __init__(self, torch, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(n // 4096, 4096, dtype=torch.float32, device=dev)
+        self.acc = torch.empty(4096, dtype=torch.float32, device=dev)
+        self.torch = torch
+        self.mib = n * 4 >> 20
+
+    def zero_(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.acc)
+
+
 def time_ops(torch, stream, flush, ops, reps, warmup):
     """Per-op device times (ms) over ``reps`` passes, L2 flushed before each op."""
     for _ in range(warmup):
@@ -263,7 +285,7 @@ def gpu_arm(a, world, rank, local):
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     peak, peak_kind = hbm_peak()
 
     case, args = make_workload(WORKLOAD)
@@ -328,8 +350,8 @@ def gpu_arm(a, world, rank, local):
                    "tokens": 8192, "experts": 2304, "topk": 36, "score_func": "softmax",
                    "logits_dtype": "f32", "tokens_per_gpu": 8192,
                    "parallelism": f"data-parallel x{world} (independent token batches)",
-                   "l2": "flushed before every kernel (write of "
-                         f"{flush.numel() * 4 >> 20} MiB), outside the kernel events",
+                   "l2": f"flushed before every kernel (write of {flush.mib} MiB, then a "
+                         f"read of another {flush.mib} MiB), outside the kernel events",
                    "peak_hbm_gbs": peak, "peak_kind": peak_kind},
         "gpu_launches": len(ops) * a.steps,
         "region_ms_per_step": round(region_ms / a.steps, 4),

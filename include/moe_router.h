@@ -193,7 +193,7 @@ MR_API const char* moe_router_strerror(int code);
  *   MR_PATH_STAGED: each warp streams rows through shared memory with bulk
  *     copies (no bias, no groups; E % 4 == 0 for fp32, E % 8 == 0 for bf16;
  *     16-byte aligned tensors).
- * MR_PATH_AUTO takes the staged path from E = 512 up where it applies.  A
+ * MR_PATH_AUTO takes the staged path from E = 256 up where it applies.  A
  * forced path that does not apply to a call falls back to the automatic
  * choice.  Process-wide; meant for tests and benchmarks.  The environment
  * variable MOE_ROUTER_FORCE_PATH (auto|segment|staged) sets the initial

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -155,13 +156,13 @@ bool staged_shape_ok(int E, int dt) {
   return E % 4 == 0 && (dt == MR_F32 || E % 8 == 0) && E <= 2304;
 }
 
-// The staged path serves rows from 512 experts up unless a path is forced.
+// The staged path serves rows from 256 experts up unless a path is forced.
 bool use_staged(int E, int dt, bool key_on_logit, bool aligned) {
   if (!key_on_logit || !aligned || !staged_shape_ok(E, dt)) return false;
   const int path = current_path();
   if (path == MR_PATH_SEGMENT) return false;
   if (path == MR_PATH_STAGED) return true;
-  return E >= 512;
+  return E >= 256;
 }
 
 int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st) {
@@ -232,11 +233,30 @@ bool choose_fwd(int E, int K, bool vec, FwdConfig* c) {
   return false;
 }
 
-bool choose_bwd(int E, BwdConfig* c) {
+// Lanes x warps x chunks per row of the two-pass backwards (measured best
+// per row size: more warps per row at large E keep more loads in flight).
+bool choose_bwd(int E, int op, BwdConfig* c) {
   const int chunks = (E + 3) / 4;
   struct Opt { int seg, w, nc; };
-  static const Opt opts[] = {{8, 1, 2}, {16, 1, 4}, {32, 1, 4}, {32, 2, 4}, {32, 3, 6}};
-  for (const Opt& o : opts) {
+  static const Opt all[] = {{8, 1, 2}, {16, 1, 4}, {32, 1, 2}, {32, 1, 4}, {32, 2, 1},
+                            {32, 2, 2}, {32, 2, 4}, {32, 4, 1}, {32, 4, 2}, {32, 3, 6},
+                            {32, 6, 3}, {32, 9, 2}};
+  // tuning override: MOE_ROUTER_BWD_SHAPE="lanes,warps,chunks" (a compiled
+  // shape that holds the row), else the table below
+  if (const char* env = std::getenv("MOE_ROUTER_BWD_SHAPE")) {
+    int sg = 0, w = 0, nc = 0;
+    if (std::sscanf(env, "%d,%d,%d", &sg, &w, &nc) == 3) {
+      for (const Opt& o : all) {
+        if (o.seg == sg && o.w == w && o.nc == nc && o.seg * o.w * o.nc >= chunks) {
+          c->seg = sg; c->w = w; c->nc = nc;
+          return true;
+        }
+      }
+    }
+  }
+  static const Opt opts_topk[] = {{8, 1, 2}, {32, 1, 2}, {32, 1, 4}, {32, 2, 4}, {32, 9, 2}};
+  static const Opt opts_aux[] = {{8, 1, 2}, {32, 1, 2}, {32, 1, 4}, {32, 2, 4}, {32, 6, 3}};
+  for (const Opt& o : (op == 0 ? opts_topk : opts_aux)) {
     if (o.seg * o.w * o.nc >= chunks) {
       c->seg = o.seg; c->w = o.w; c->nc = o.nc;
       return true;
@@ -327,7 +347,7 @@ int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,
     return MR_ERR_INVALID;
   if (T == 0) return MR_OK;
   BwdConfig c{};
-  if (!choose_bwd(E, &c)) return MR_ERR_UNSUPPORTED;
+  if (!choose_bwd(E, 0, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = (E % 4 == 0) && aligned16(grad_probs) && aligned16(routing_map) &&
           aligned16(scores) && aligned16(grad_logits);
   c.op = 0;
@@ -383,7 +403,7 @@ int router_aux_scores_bwd(const float* grad_scores, const float* saved, mr_dtype
     return MR_ERR_INVALID;
   if (T == 0) return MR_OK;
   BwdConfig c{};
-  if (!choose_bwd(E, &c)) return MR_ERR_UNSUPPORTED;
+  if (!choose_bwd(E, 1, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = (E % 4 == 0) && aligned16(grad_scores) && aligned16(saved) &&
           aligned16(grad_logits);
   c.op = 1;

@@ -31,8 +31,9 @@ struct BwdConfig {
   X(8, 2) X(8, 4) X(8, 8) X(16, 4) X(16, 8) X(32, 2) X(32, 4) X(32, 8) X(32, 18)
 
 // compiled (SEG, W, NC) triples of the backwards (vector and scalar rows)
-#define MR_BWD_CONFIGS(X) \
-  X(8, 1, 2) X(16, 1, 4) X(32, 1, 4) X(32, 2, 4) X(32, 3, 6)
+#define MR_BWD_CONFIGS(X)                                                      \
+  X(8, 1, 2) X(16, 1, 4) X(32, 1, 2) X(32, 1, 4) X(32, 2, 1) X(32, 2, 2) X(32, 2, 4) \
+  X(32, 4, 1) X(32, 4, 2) X(32, 3, 6) X(32, 6, 3) X(32, 9, 2)
 
 template <int SF, int DT, int SEG, int NC, bool VEC, int KM, int OP>
 cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {

@@ -325,3 +325,24 @@ def test_errors_raise(R):
         R.router_topk_fwd(x, 17)
     with pytest.raises(R.RouterError):
         R.router_topk_fwd(x, 4, "sigmoid", num_groups=3, group_topk=1)
+
+
+BWD_SHAPES = [(8, 1, 2), (16, 1, 4), (32, 1, 2), (32, 1, 4), (32, 2, 1), (32, 2, 2), (32, 2, 4),
+              (32, 4, 1), (32, 4, 2), (32, 3, 6), (32, 6, 3), (32, 9, 2)]
+
+
+@pytest.mark.parametrize("shape", BWD_SHAPES, ids=["x".join(map(str, s)) for s in BWD_SHAPES])
+def test_every_backward_shape(R, shape, monkeypatch):
+    """Each compiled backward row shape (lanes, warps, chunks per lane),
+    forced through the tuning override, on rows that fill it and rows that
+    leave lanes idle."""
+    cap = 4 * shape[0] * shape[1] * shape[2]
+    monkeypatch.setenv("MOE_ROUTER_BWD_SHAPE", ",".join(map(str, shape)))
+    for E in sorted({cap, max(4, cap - 36), max(3, cap // 2 + 1)}):
+        K = min(E, 8)
+        for dt in ("f32", "bf16"):
+            case = make_case(77, E, K, dtype=dt, seed=E)
+            for sf in ("softmax", "sigmoid"):
+                run_and_check_topk(R, case, K, sf, c=1.5)
+                if dt == "f32":
+                    run_and_check_aux(R, case, K, sf)
