@@ -72,7 +72,7 @@ bool device_info(DeviceInfo* out) {
 
 // ---- staged forward plans, computed once per (device, shape) ----------------
 struct PlanKey {
-  int dev, sf, dt, op, E;
+  int dev, sf, dt, op, E, K;
 };
 struct PlanEntry {
   PlanKey key;
@@ -85,20 +85,27 @@ int g_nplans = 0;
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-int staged_nc(int E) { return E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18)); }
+// Lanes per row and chunks per lane of the staged forward.  (16-lane
+// segments, two rows per warp, measured slower at 256 and 512 experts: the
+// two rows of a warp take different selection paths and wait for each
+// other.)
+void staged_shape(int E, int /*K*/, int* seg, int* nc) {
+  *seg = 32;
+  *nc = E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18));
+}
 
-StagedLayout staged_layout(int nc, int dt) {
+StagedLayout staged_layout(int seg, int nc, int dt) {
   StagedLayout L{};
   const int d = dt == MR_F32 ? 4 : 2;
-  L.stage_bytes = 128 * nc * d;  // 32 * nc chunks of four logits
+  L.stage_bytes = 4 * seg * nc * d;  // seg * nc chunks of four logits
   int off = 2 * L.stage_bytes;
   L.cand_off = off;
-  off += kCandPerLane * 32 * 8;
+  off += kCandPerLane * seg * 8;
   L.mask_off = off;
-  off += 16 * nc;  // one bit per padded expert
+  off += round_up(seg * nc / 2, 16);  // one bit per padded expert
   L.bar_off = round_up(off, 16);
   off = L.bar_off + 32;
-  L.warp_bytes = round_up(off, 128);
+  L.seg_bytes = round_up(off, 128);
   return L;
 }
 
@@ -110,44 +117,53 @@ int occupancy_any(int sf, int dt, const StagedPlan& p) {
 
 // Warps per block that keep the most warps resident per SM (shared memory is
 // the limit: one slice per warp).
-bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, StagedPlan* out) {
+bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, int K, StagedPlan* out) {
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < g_nplans; ++i) {
       const PlanKey& k = g_plans[i].key;
-      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E) {
+      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E && k.K == K) {
         *out = g_plans[i].plan;
         return g_plans[i].valid;
       }
     }
   }
   StagedPlan p{};
-  p.nc = staged_nc(E);
-  p.full = E == 128 * p.nc;
-  p.layout = staged_layout(p.nc, dt);
+  staged_shape(E, K, &p.seg, &p.nc);
+  p.full = E == 4 * p.seg * p.nc;
+  p.layout = staged_layout(p.seg, p.nc, dt);
   p.op = op;
+  const int warp_bytes = (32 / p.seg) * p.layout.seg_bytes;
   int best_warps = 0;
+  // tuning override: MOE_ROUTER_STAGED_WARPS caps the resident warps per SM
+  int cap_warps = 64;
+  if (const char* env = std::getenv("MOE_ROUTER_STAGED_WARPS")) {
+    const int v = std::atoi(env);
+    if (v > 0) cap_warps = v;
+  }
   for (int w = 1; w <= kStagedMaxWarps; ++w) {
-    const int smem = w * p.layout.warp_bytes;
+    const int smem = w * warp_bytes;
     if (smem > di.smem_per_block) break;
     int blocks = di.smem_per_sm / (smem + 1024);
     blocks = blocks < 2048 / (32 * w) ? blocks : 2048 / (32 * w);
     blocks = blocks < 32 ? blocks : 32;
-    if (blocks * w >= best_warps) {
+    if (blocks * w > cap_warps) blocks = cap_warps / w;
+    if (blocks > 0 && blocks * w >= best_warps) {
       best_warps = blocks * w;
       p.warps_per_block = w;
     }
   }
   bool valid = best_warps > 0;
   if (valid) {
-    const int per_sm = occupancy_any(sf, dt, p);
+    int per_sm = occupancy_any(sf, dt, p);
+    if (per_sm * p.warps_per_block > cap_warps) per_sm = cap_warps / p.warps_per_block;
     valid = per_sm > 0;
     p.max_blocks = per_sm * di.sms;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_nplans < kPlanCache) g_plans[g_nplans++] = PlanEntry{{dev, sf, dt, op, E}, p, valid};
+  if (g_nplans < kPlanCache) g_plans[g_nplans++] = PlanEntry{{dev, sf, dt, op, E, K}, p, valid};
   *out = p;
   return valid;
 }
@@ -169,7 +185,7 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st)
   DeviceInfo di{};
   if (!device_info(&di)) return MR_ERR_CUDA;
   StagedPlan p{};
-  if (!staged_plan(di, sf, dt, op, a.E, &p)) return MR_ERR_CUDA;
+  if (!staged_plan(di, sf, dt, op, a.E, a.K, &p)) return MR_ERR_CUDA;
   cudaError_t e;
   if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_staged_softmax_f32(a, p, di.status, st)

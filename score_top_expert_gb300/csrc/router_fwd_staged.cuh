@@ -1,29 +1,33 @@
 // Router forward, shared-memory staged path (no bias, no groups).
 //
-// Each warp owns one token row at a time and walks the rows of the batch
-// persistently (row, row + all warps, ...).  Rows arrive in shared memory by
-// one bulk copy each, double-buffered: while the warp works on row r from one
-// stage, the copy of its next row fills the other, so every warp keeps a row
-// in flight without holding it in registers.
+// A segment of SEG lanes (16 or 32; a warp holds 32 / SEG segments) owns one
+// token row at a time and walks the rows of the batch persistently (row,
+// row + all segments, ...).  Rows arrive in shared memory by one bulk copy
+// each, double-buffered: while the segment works on row r from one stage, the
+// copy of its next row fills the other, so every segment keeps a row in
+// flight without holding it in registers.  Segments only synchronise among
+// their own lanes, so the segments of a warp may take different paths.
 //
-// Per row (lane l holds chunks c = l + 32 j, four consecutive experts each):
-//   1  row max and two half maxima per lane (64 group maxima); if the warp
-//      carries a threshold from its previous row, each lane also marks its
-//      logits >= that threshold in a candidate bit mask (branch-free).  The
-//      speculation is kept only if it yields at least K and at most 128
+// Per row (lane l of the segment holds chunks c = l + SEG j, four consecutive
+// experts each):
+//   1  row max and two half maxima per lane (2 SEG group maxima); if the
+//      segment carries a threshold from its previous row, each lane also
+//      marks its logits >= that threshold in a candidate bit mask (branch-free).
+//      The speculation is kept only if it yields at least K and at most 4 SEG
 //      candidates, which makes it exact: every top-K logit is a candidate.
-//   2  otherwise: a lower bound on the K-th largest logit from the 64 group
+//   2  otherwise: a lower bound on the K-th largest logit from the 2 SEG group
 //      maxima (the K-th largest of them, rounded down to 16 high bits; a
 //      16-step search) and a second pass marking logits >= the bound.
 //   3  the marked logits are compacted as (ordered key << 32 | ~index) words
 //      (ffs over each lane's mask, lanes in order by a prefix count); each
 //      word's exact rank among them selects the K best, which set their bits
 //      in a per-row bitmask.  The candidate ranked about 1.5 K gives the next
-//      row's threshold.  A row with more than 128 candidates (many equal
-//      logits) instead walks the distinct logits down from the maximum, one
-//      pass each, to the K-th largest (a bitwise search after eight values),
-//      takes the tied ones in index order by a prefix count, and marks the
-//      bitmask directly.
+//      row's threshold.  A row with more than 4 SEG logits at the bound
+//      narrows the threshold by a binary search on the key (one counting pass
+//      per step, stopping at K..4 SEG candidates); when the search closes on
+//      a single key that still holds too many, that key is tied: the tied
+//      logits are taken in index order by a prefix count and marked directly
+//      (so is a row whose maximum alone is tied K times).
 //   4  scores: softmax e = exp(x - max) and the row sum, or sigmoid s; fp32
 //      rows store them over their logits (bf16 rows recompute them in 5).
 //   5  outputs from the scores and the bitmask: probs, map, scores (top-K)
@@ -37,16 +41,16 @@
 
 namespace moe_router {
 
-// Byte offsets inside one warp's slice of shared memory (set on the host).
-// A stage holds one row padded to the full chunk grid (32 * NC chunks), so
+// Byte offsets inside one segment's slice of shared memory (set on the host).
+// A stage holds one row padded to the full chunk grid (SEG * NC chunks), so
 // every lane reads every chunk without a bound check; the padding is never
 // written by the copy and is masked out when the row is not full.
 struct StagedLayout {
-  int stage_bytes;  // 32 * NC chunks of 4 logits
-  int cand_off;     // kCandPerLane * 32 packed candidate words
+  int stage_bytes;  // SEG * NC chunks of 4 logits
+  int cand_off;     // kCandPerLane * SEG packed candidate words
   int mask_off;     // selection words, one bit per expert of the padded row
   int bar_off;      // two mbarriers and one 32-bit slot
-  int warp_bytes;   // slice size, multiple of 128
+  int seg_bytes;    // slice size, multiple of 128
 };
 
 constexpr int kStagedMaxWarps = 12;
@@ -98,6 +102,16 @@ __device__ __forceinline__ float stage_x1(const unsigned char* stage, int idx) {
   }
 }
 
+// Sum over the segment's lanes (one warp reduction when SEG == 32).
+template <int SEG>
+__device__ __forceinline__ int seg_reduce_add(int v) {
+  if constexpr (SEG == 32) {
+    return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(v)));
+  } else {
+    return seg_sum_int<SEG>(v);
+  }
+}
+
 // Candidate mask of one lane: bit 4 j + u marks element u of chunk j.
 template <int NC>
 struct CandMask {
@@ -119,16 +133,16 @@ struct CandMask {
 };
 
 // Compact the marked logits of the lane into cand[pos...] as packed words.
-template <int DT, int NC>
+template <int DT, int SEG, int NC>
 __device__ __forceinline__ void compact_marked(const unsigned char* stage, const CandMask<NC>& m,
-                                               int pos, int lane, unsigned long long* cand) {
+                                               int pos, int li, unsigned long long* cand) {
 #pragma unroll
   for (int i = 0; i < CandMask<NC>::W; ++i) {
     uint32_t bits = m.w[i];
     while (bits) {
       const int b = 32 * i + __ffs(bits) - 1;
       bits &= bits - 1;
-      const int idx = 4 * (lane + 32 * (b >> 2)) + (b & 3);
+      const int idx = 4 * (li + SEG * (b >> 2)) + (b & 3);
       cand[pos++] = pack_key(ordered_key(stage_x1<DT>(stage, idx)), idx);
     }
   }
@@ -137,26 +151,47 @@ __device__ __forceinline__ void compact_marked(const unsigned char* stage, const
 // Rank of each owned candidate among all `total` candidates (NOWN per lane):
 // the K best set their selection bits; the one ranked `target` publishes its
 // key as the next row's threshold; sigmoid rows sum their selected scores.
-template <int NOWN, bool SIG>
+// With TRY32 (fp32 rows, where equal logits are rare) the rank first counts
+// the candidates with a larger 32-bit key (one compare per pair); when keys
+// repeat, the ranks of the tied candidates coincide and no longer sum to
+// 0 + 1 + ... + (total - 1), and the rank is recounted on the full
+// (key, ~index) words, which is what bf16 rows do directly.
+template <int SEG, int NOWN, bool SIG, bool TRY32>
 __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, int total,
-                                                int lane, int K, int target, uint32_t* selmask,
+                                                int li, int K, int target, uint32_t* selmask,
                                                 uint32_t* next_key, float& part) {
+  const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(cand) + 1;  // keys
   unsigned long long own[NOWN];
   int rank[NOWN];
+  int rsum = 0;
 #pragma unroll
   for (int r = 0; r < NOWN; ++r) {
-    own[r] = (r * 32 + lane < total) ? cand[r * 32 + lane] : ~0ull;
+    own[r] = (r * SEG + li < total) ? cand[r * SEG + li] : ~0ull;
     rank[r] = 0;
   }
+  if constexpr (TRY32) {
 #pragma unroll 4
-  for (int c = 0; c < total; ++c) {
-    const unsigned long long w = cand[c];
+    for (int c = 0; c < total; ++c) {
+      const uint32_t w = hi_words[2 * c];
 #pragma unroll
-    for (int r = 0; r < NOWN; ++r) rank[r] += w > own[r];
+      for (int r = 0; r < NOWN; ++r) rank[r] += w > static_cast<uint32_t>(own[r] >> 32);
+    }
+#pragma unroll
+    for (int r = 0; r < NOWN; ++r) rsum += (r * SEG + li < total) ? rank[r] : 0;
+  }
+  if (!TRY32 || seg_reduce_add<SEG>(rsum) != total * (total - 1) / 2) {
+#pragma unroll
+    for (int r = 0; r < NOWN; ++r) rank[r] = 0;
+#pragma unroll 4
+    for (int c = 0; c < total; ++c) {
+      const unsigned long long w = cand[c];
+#pragma unroll
+      for (int r = 0; r < NOWN; ++r) rank[r] += w > own[r];
+    }
   }
 #pragma unroll
   for (int r = 0; r < NOWN; ++r) {
-    if (r * 32 + lane < total) {
+    if (r * SEG + li < total) {
       if (rank[r] < K) {
         const uint32_t idx = ~static_cast<uint32_t>(own[r]);
         atomicOr(&selmask[idx >> 5], 1u << (idx & 31));
@@ -167,19 +202,27 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
   }
 }
 
-template <int SF, int DT, int NC, int OP, bool FULL>
-__global__ void __launch_bounds__(kStagedMaxWarps * 32)
+// Registers of the 18-chunk bf16 kernels are capped so that they keep 16
+// warps per SM (their shared memory would allow 21; uncapped they need 160).
+template <int DT, int NC>
+constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18) ? 128 : 168; }
+
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
+__global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC>()))
 router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
-  constexpr int CAP = kCandPerLane * 32;
+  constexpr int CAP = kCandPerLane * SEG;
+  constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
   constexpr int D = DT == DT_F32 ? 4 : 2;
   constexpr bool kSigTopk = (OP == 0 && SF == SF_SIGMOID);
   constexpr bool kStore = (DT == DT_F32);       // scores kept over the fp32 logits
   constexpr bool kNeedSum = (SF == SF_SOFTMAX || OP == 1);
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int wpb = blockDim.x >> 5;
-  unsigned char* base = smem + warp * L.warp_bytes;
+  const int li = lane & (SEG - 1);
+  const int seg = (threadIdx.x >> 5) * RPW + lane / SEG;  // segment in the block
+  const int spb = (blockDim.x >> 5) * RPW;                // segments per block
+  const unsigned smask = seg_mask<SEG>();
+  unsigned char* base = smem + seg * L.seg_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   uint32_t* next_key = reinterpret_cast<uint32_t*>(bars + 2);
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(base + L.cand_off);
@@ -188,13 +231,13 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   const int E = a.E, K = a.K, T = a.T;
   const int nchunks = E >> 2;
   const uint32_t row_bytes = static_cast<uint32_t>(E) * D;
-  const int nwarps = gridDim.x * wpb;
+  const int nsegs = gridDim.x * spb;
   const unsigned char* src = static_cast<const unsigned char*>(a.logits);
   const int target = K - 1 + (K / 2 > 4 ? K / 2 : 4);  // rank giving the next threshold
 
   // logits of chunk j; padding chunks of a partial row read as -inf
   auto load_x = [&](const unsigned char* stage, int j, float (&x)[4]) {
-    const int c = lane + 32 * j;
+    const int c = li + SEG * j;
     stage_x<DT>(stage, c, x);
     if constexpr (!FULL) {
       const bool ok = c < nchunks;
@@ -203,43 +246,56 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
   };
 
-  if (lane == 0) {
+  if (li == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncwarp(smask);
 
-  int row = blockIdx.x * wpb + warp;
-  if (lane == 0) {
-    if (row < T) bulk_load(base, src + static_cast<size_t>(row) * row_bytes, row_bytes, &bars[0]);
-    if (row + nwarps < T)
-      bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row + nwarps) * row_bytes,
+  const int row0 = blockIdx.x * spb + seg;
+  if (li == 0) {
+    if (row0 < T)
+      bulk_load(base, src + static_cast<size_t>(row0) * row_bytes, row_bytes, &bars[0]);
+    if (row0 + nsegs < T)
+      bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nsegs) * row_bytes,
                 row_bytes, &bars[1]);
   }
 
+  // The loop is uniform over the warp: the segments of a warp process rows
+  // in step and meet at full-warp barriers after the copy wait and after the
+  // selection, so that their paths reconverge.
   bool have_spec = false;  // a threshold carried over from the previous row
   float spec_t = 0.0f;
   uint32_t phase = 0;
-  for (int it = 0; row < T; ++it, row += nwarps) {
+  for (int it = 0;; ++it) {
+    const int row = row0 + it * nsegs;
+    const bool active = row < T;
+    if (!__any_sync(0xffffffffu, active)) break;
     const int b = it & 1;
-    bool ok = mbar_wait_bounded(&bars[b], (phase >> b) & 1u);
+    bool ok = true;
+    if (active) ok = mbar_wait_bounded(&bars[b], (phase >> b) & 1u);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
       // record the failure, let the other stage's copy (if any) land, leave
-      if (lane == 0) {
+      if (active && li == 0) {
         atomicExch(status, kDeviceWaitTimeout);
-        if (row + nwarps < T) mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
+        if (row + nsegs < T) mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
       }
       __syncwarp();
       return;
+    }
+    if (!active) {  // this segment has no row left; its partner still has one
+      __syncwarp();
+      __syncwarp();
+      continue;
     }
     phase ^= 1u << b;
     unsigned char* stage = base + b * L.stage_bytes;
     const size_t off = static_cast<size_t>(row) * static_cast<size_t>(E);
 
 #pragma unroll
-    for (int w = lane; w < NC * 4; w += 32) selmask[w] = 0u;
+    for (int w = li; w < NC * SEG / 8; w += SEG) selmask[w] = 0u;
 
     // ---- 1: maxima, speculative candidate mask -------------------------------------
     float hm[2] = {-INFINITY, -INFINITY};
@@ -252,15 +308,18 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       load_x(stage, j, x);
       const float m4 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       hm[half_of<NC>(j, 0)] = fmaxf(hm[half_of<NC>(j, 0)], m4);
+      if (have_spec) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) cm.mark(4 * j + u, x[u] >= ts);
+        for (int u = 0; u < 4; ++u) cm.mark(4 * j + u, x[u] >= ts);
+      }
     }
-    const float row_max = seg_max<32>(fmaxf(hm[0], hm[1]));
+    const float row_max = seg_max<SEG>(fmaxf(hm[0], hm[1]));
     int cnt = cm.count();
-    int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
+    int total = seg_reduce_add<SEG>(cnt);
     bool cand_ok = have_spec && total >= K && total <= CAP;
 
     // ---- 2: bound from the group maxima ---------------------------------------------
+    uint32_t lo_key = 0;  // a key with more than CAP logits at or above it
     if (!cand_ok) {
       uint32_t gmax[2];
 #pragma unroll
@@ -269,12 +328,15 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
 #pragma unroll
       for (int bit = 31; bit >= 16; --bit) {
         const uint32_t cb = bound | (1u << bit);
-        const unsigned n = __reduce_add_sync(
-            0xffffffffu, static_cast<unsigned>((gmax[0] >= cb) + (gmax[1] >= cb)));
-        if (static_cast<int>(n) >= K) bound = cb;
+        int n;
+        if constexpr (SEG == 32) n = seg_reduce_add<32>((gmax[0] >= cb) + (gmax[1] >= cb));
+        else n = seg_count<SEG>(gmax[0] >= cb) + seg_count<SEG>(gmax[1] >= cb);
+        if (n >= K) bound = cb;
       }
       // lowest finite float when the bound says nothing: padding (-inf) stays out
-      const float tf = bound < 0x00800000u ? -3.402823466e38f : key_to_float(bound);
+      if (bound < 0x00800000u) bound = 0x00800000u;
+      lo_key = bound;
+      const float tf = key_to_float(bound);
       cm.clear();
 #pragma unroll
       for (int j = 0; j < NC; ++j) {
@@ -284,90 +346,104 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         for (int u = 0; u < 4; ++u) cm.mark(4 * j + u, x[u] >= tf);
       }
       cnt = cm.count();
-      total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
+      total = seg_reduce_add<SEG>(cnt);
       cand_ok = total <= CAP;
     }
 
     // ---- 3: exact selection ----------------------------------------------------------
     float part = 0.0f;  // sum of the selected scores (sigmoid top-K)
-    if (cand_ok) {
-      compact_marked<DT, NC>(stage, cm, seg_exclusive_scan<32>(cnt), lane, cand);
-      __syncwarp();
-      const int nown = (total + 31) >> 5;
-      const int tgt = target < total - 1 ? target : total - 1;
-      if (nown <= 1) rank_candidates<1, kSigTopk>(cand, total, lane, K, tgt, selmask, next_key, part);
-      else if (nown == 2) rank_candidates<2, kSigTopk>(cand, total, lane, K, tgt, selmask, next_key, part);
-      else if (nown == 3) rank_candidates<3, kSigTopk>(cand, total, lane, K, tgt, selmask, next_key, part);
-      else rank_candidates<4, kSigTopk>(cand, total, lane, K, tgt, selmask, next_key, part);
-      __syncwarp();
-      spec_t = key_to_float(*next_key);
-      have_spec = true;
-    } else {
-      // more candidates than the buffer holds: many equal logits.  Walk the
-      // distinct values down from the maximum to the K-th largest logit v.
-      float v = row_max;
-      int above = 0;      // logits > v
-      bool found = false;
+    bool tie_row = false;
+    float v = row_max;    // tied rows: the K-th largest logit
+    int above = 0;        // tied rows: logits > v
+    if (!cand_ok) {
+      // more than CAP logits reach the bound.  Either the maximum alone is
+      // tied K times, or a binary search on the key between the bound and
+      // the maximum finds a threshold with K..CAP logits above it; if the
+      // search closes on one key that still holds more, that key is tied.
+      int eq = 0;
 #pragma unroll 1
-      for (int round = 0; round < 8 && !found; ++round) {
-        int eq = 0;
-        float below = -INFINITY;
-#pragma unroll 1
-        for (int j = 0; j < NC; ++j) {
-          float x[4];
-          load_x(stage, j, x);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            eq += x[u] == v;
-            if (x[u] < v) below = fmaxf(below, x[u]);
-          }
-        }
-        eq = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(eq)));
-        below = seg_max<32>(below);
-        if (above + eq >= K) found = true;
-        else { above += eq; v = below; }
+      for (int j = 0; j < NC; ++j) {
+        float x[4];
+        load_x(stage, j, x);
+        eq += (x[0] == v) + (x[1] == v) + (x[2] == v) + (x[3] == v);
       }
-      if (!found) {
-        // general case: bitwise search for the K-th largest key (padding is
-        // -inf, below every finite logit, and K <= E keeps it out)
-        uint32_t tk = 0;
+      eq = seg_reduce_add<SEG>(eq);
+      if (eq >= K) {
+        tie_row = true;
+      } else {
+        uint32_t lo = lo_key, hi = ordered_key(row_max) + 1u;
+        int n_hi = 0;
 #pragma unroll 1
-        for (int bit = 31; bit >= 0; --bit) {
-          const uint32_t cb = tk | (1u << bit);
+        while (hi - lo > 1u) {
+          const uint32_t mid = lo + (hi - lo) / 2u;
+          const float tm = key_to_float(mid);
           int n = 0;
 #pragma unroll 1
           for (int j = 0; j < NC; ++j) {
             float x[4];
             load_x(stage, j, x);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) n += ordered_key(x[u]) >= cb;
+            n += (x[0] >= tm) + (x[1] >= tm) + (x[2] >= tm) + (x[3] >= tm);
           }
-          if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n))) >= K)
-            tk = cb;
+          n = seg_reduce_add<SEG>(n);
+          if (n > CAP) {
+            lo = mid;
+          } else if (n < K) {
+            hi = mid;
+            n_hi = n;
+          } else {
+            lo = mid;
+            cand_ok = true;
+            break;
+          }
         }
-        v = key_to_float(tk);
-        int gt = 0;
-#pragma unroll 1
-        for (int j = 0; j < NC; ++j) {
-          float x[4];
-          load_x(stage, j, x);
+        if (cand_ok) {
+          const float tm = key_to_float(lo);
+          cm.clear();
 #pragma unroll
-          for (int u = 0; u < 4; ++u) gt += x[u] > v;
+          for (int j = 0; j < NC; ++j) {
+            float x[4];
+            load_x(stage, j, x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cm.mark(4 * j + u, x[u] >= tm);
+          }
+          cnt = cm.count();
+          total = seg_reduce_add<SEG>(cnt);
+        } else {
+          tie_row = true;
+          v = key_to_float(lo);
+          above = n_hi;
         }
-        above = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(gt)));
       }
+    }
+    if (cand_ok) {
+      compact_marked<DT, SEG, NC>(stage, cm, seg_exclusive_scan<SEG>(cnt), li, cand);
+      __syncwarp(smask);
+      const int nown = (total + SEG - 1) / SEG;
+      const int tgt = target < total - 1 ? target : total - 1;
+      if (nown <= 1)
+        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+      else if (nown == 2)
+        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+      else if (nown == 3)
+        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+      else
+        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+      __syncwarp(smask);
+      spec_t = key_to_float(*next_key);
+      have_spec = true;
+    } else if (tie_row) {
       // need-th lowest index among the logits equal to v: chunks in index
       // order (chunk c covers experts 4c..4c+3), prefix counts across lanes
       const int need = K - above;
       int ti = -1, run = 0;
 #pragma unroll 1
       for (int j = 0; j < NC && ti < 0; ++j) {
-        const int c = lane + 32 * j;
+        const int c = li + SEG * j;
         float x[4];
         load_x(stage, j, x);
         const int e = (x[0] == v) + (x[1] == v) + (x[2] == v) + (x[3] == v);
-        const int excl = seg_exclusive_scan<32>(e);
-        const int tot = __shfl_sync(0xffffffffu, excl + e, 31);
+        const int excl = seg_exclusive_scan<SEG>(e);
+        const int tot = __shfl_sync(smask, excl + e, SEG - 1, SEG);
         int mine = -1;
         if (run + excl < need && run + excl + e >= need) {
           int left = need - run - excl;
@@ -375,15 +451,15 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           for (int u = 0; u < 4; ++u)
             if (x[u] == v && --left == 0 && mine < 0) mine = 4 * c + u;
         }
-        const unsigned who = __ballot_sync(0xffffffffu, mine >= 0);
-        if (who) ti = __shfl_sync(0xffffffffu, mine, __ffs(who) - 1);
+        const unsigned who = __ballot_sync(smask, mine >= 0) & smask;
+        if (who) ti = __shfl_sync(smask, mine, __ffs(who) - 1);
         run += tot;
       }
-      __syncwarp();
+      __syncwarp(smask);
       // mark the selection: logits > v, and the equal ones up to index ti
 #pragma unroll 1
       for (int j = 0; j < NC; ++j) {
-        const int c = lane + 32 * j;
+        const int c = li + SEG * j;
         float x[4];
         load_x(stage, j, x);
         uint32_t bits = 0;
@@ -398,6 +474,8 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       }
       have_spec = false;
     }
+
+    __syncwarp(0xffffffffu);  // reconverge the segments of the warp
 
     // ---- 4: scores ----------------------------------------------------------------------
     const float max_l2e = row_max * kLog2e;
@@ -418,19 +496,19 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           if (j & 1) sum1 += add; else sum0 += add;
         }
         if constexpr (kStore)
-          sts_f4(stage + 16 * (lane + 32 * j), make_float4(s[0], s[1], s[2], s[3]));
+          sts_f4(stage + 16 * (li + SEG * j), make_float4(s[0], s[1], s[2], s[3]));
       }
-      if constexpr (kNeedSum) inv = 1.0f / seg_sum<32>(sum0 + sum1);
+      if constexpr (kNeedSum) inv = 1.0f / seg_sum<SEG>(sum0 + sum1);
     }
     float pf = a.scaling;
-    if constexpr (kSigTopk) pf = a.scaling / seg_sum<32>(part);
+    if constexpr (kSigTopk) pf = a.scaling / seg_sum<SEG>(part);
     else if constexpr (SF == SF_SOFTMAX && OP == 0) pf = a.scaling * inv;
-    __syncwarp();
+    __syncwarp(smask);
 
     // ---- 5: outputs -----------------------------------------------------------------------
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-      const int c = lane + 32 * j;
+      const int c = li + SEG * j;
       if (FULL || c < nchunks) {
         float w[4];  // e (softmax) or s (sigmoid)
         if constexpr (kStore) {
@@ -470,9 +548,9 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       }
     }
     fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const int nr = row + 2 * nwarps;
+    __syncwarp(0xffffffffu);
+    if (li == 0) {
+      const int nr = row + 2 * nsegs;
       if (nr < T) bulk_load(stage, src + static_cast<size_t>(nr) * row_bytes, row_bytes, &bars[b]);
     }
   }

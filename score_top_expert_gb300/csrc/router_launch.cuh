@@ -94,38 +94,42 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdConfig& c, cudaStream_t st) {
   return cudaErrorInvalidConfiguration;
 }
 
-// Staged forward: warps per block, the per-warp slice and the grid cap.
+// Staged forward: segment shape, warps per block, the per-segment slice and
+// the grid cap.
 struct StagedPlan {
   StagedLayout layout;
   int warps_per_block;
   int max_blocks;  // resident blocks per SM x SMs
-  int nc;          // chunks of 4 experts per lane: 2, 4, 8 or 18
+  int seg;         // lanes per row (32 in this build)
+  int nc;          // chunks of 4 experts per lane
   int op;
-  bool full;       // E == 128 * nc: no padding chunks
+  bool full;       // E == 4 * seg * nc: no padding chunks
 };
 
-#define MR_STAGED_NCS(X) X(2) X(4) X(8) X(18)
+// compiled (SEG, NC) pairs of the staged forward
+#define MR_STAGED_SHAPES(X) X(32, 2) X(32, 4) X(32, 8) X(32, 18)
 
-template <int SF, int DT, int NC, int OP, bool FULL>
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
 cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* status,
                                cudaStream_t st) {
-  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP, FULL>;
-  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
+  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL>;
+  const size_t smem = static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  const long long need = (static_cast<long long>(a.T) + p.warps_per_block - 1) / p.warps_per_block;
+  const long long rows_per_block = static_cast<long long>(p.warps_per_block) * (32 / SEG);
+  const long long need = (static_cast<long long>(a.T) + rows_per_block - 1) / rows_per_block;
   const unsigned grid = static_cast<unsigned>(need < p.max_blocks ? need : p.max_blocks);
   kern<<<grid, p.warps_per_block * 32, smem, st>>>(a, p.layout, status);
   return cudaGetLastError();
 }
 
 // Resident blocks per SM of one staged instantiation (occupancy query).
-template <int SF, int DT, int NC, int OP, bool FULL>
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
 int staged_blocks_per_sm(int warps_per_block, size_t smem) {
-  auto kern = router_fwd_staged_kernel<SF, DT, NC, OP, FULL>;
+  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -139,32 +143,33 @@ int staged_blocks_per_sm(int warps_per_block, size_t smem) {
 
 template <int SF, int DT>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
-#define MR_STAGED_CASE(N)                                                             \
-  if (p.nc == N) {                                                                    \
-    if (p.full)                                                                       \
-      return p.op == 0 ? launch_staged_inst<SF, DT, N, 0, true>(a, p, status, st)     \
-                       : launch_staged_inst<SF, DT, N, 1, true>(a, p, status, st);    \
-    return p.op == 0 ? launch_staged_inst<SF, DT, N, 0, false>(a, p, status, st)      \
-                     : launch_staged_inst<SF, DT, N, 1, false>(a, p, status, st);     \
+#define MR_STAGED_CASE(S, N)                                                            \
+  if (p.seg == S && p.nc == N) {                                                        \
+    if (p.full)                                                                         \
+      return p.op == 0 ? launch_staged_inst<SF, DT, S, N, 0, true>(a, p, status, st)    \
+                       : launch_staged_inst<SF, DT, S, N, 1, true>(a, p, status, st);   \
+    return p.op == 0 ? launch_staged_inst<SF, DT, S, N, 0, false>(a, p, status, st)     \
+                     : launch_staged_inst<SF, DT, S, N, 1, false>(a, p, status, st);    \
   }
-  MR_STAGED_NCS(MR_STAGED_CASE)
+  MR_STAGED_SHAPES(MR_STAGED_CASE)
 #undef MR_STAGED_CASE
   return cudaErrorInvalidConfiguration;
 }
 
 template <int SF, int DT>
 int staged_occupancy(const StagedPlan& p) {
-  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
-#define MR_STAGED_OCC(N)                                                                 \
-  if (p.nc == N) {                                                                       \
-    const int w = p.warps_per_block;                                                     \
-    if (p.full)                                                                          \
-      return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0, true>(w, smem)               \
-                       : staged_blocks_per_sm<SF, DT, N, 1, true>(w, smem);              \
-    return p.op == 0 ? staged_blocks_per_sm<SF, DT, N, 0, false>(w, smem)                \
-                     : staged_blocks_per_sm<SF, DT, N, 1, false>(w, smem);               \
+  const size_t smem =
+      static_cast<size_t>(p.warps_per_block) * (32 / p.seg) * p.layout.seg_bytes;
+#define MR_STAGED_OCC(S, N)                                                             \
+  if (p.seg == S && p.nc == N) {                                                        \
+    const int w = p.warps_per_block;                                                    \
+    if (p.full)                                                                         \
+      return p.op == 0 ? staged_blocks_per_sm<SF, DT, S, N, 0, true>(w, smem)           \
+                       : staged_blocks_per_sm<SF, DT, S, N, 1, true>(w, smem);          \
+    return p.op == 0 ? staged_blocks_per_sm<SF, DT, S, N, 0, false>(w, smem)            \
+                     : staged_blocks_per_sm<SF, DT, S, N, 1, false>(w, smem);           \
   }
-  MR_STAGED_NCS(MR_STAGED_OCC)
+  MR_STAGED_SHAPES(MR_STAGED_OCC)
 #undef MR_STAGED_OCC
   return 0;
 }

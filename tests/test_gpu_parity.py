@@ -346,3 +346,42 @@ def test_every_backward_shape(R, shape, monkeypatch):
                 run_and_check_topk(R, case, K, sf, c=1.5)
                 if dt == "f32":
                     run_and_check_aux(R, case, K, sf)
+
+
+def adversarial_rows(E, K, rng):
+    """Rows that defeat the cheap candidate bound: sorted rows (the top values
+    sit in a few lanes), long runs of one value at the K boundary, a value
+    tied far more often than the candidate buffer holds."""
+    rows = []
+    x = np.sort(rng.normal(0, 1, E))
+    rows += [x[::-1].copy(), x.copy()]
+    y = rng.normal(0, 1, E)
+    top = np.sort(y)[::-1]
+    v = top[K - 1]
+    pos = rng.choice(E, size=min(E, 3 * K + 150), replace=False)
+    y2 = np.where(y >= v, y, y - 10.0)
+    y2[pos[: min(E, 3 * K + 150)]] = v           # many copies of the K-th value
+    rows.append(y2)
+    z = np.full(E, -4.0)
+    z[: max(K - 3, 0)] = np.linspace(3, 2, max(K - 3, 0))
+    z[rng.choice(np.arange(max(K - 3, 0), E), size=min(E - max(K - 3, 0), 200), replace=False)] = 1.5
+    rows.append(z)
+    w = rng.normal(0, 1, E)
+    w[rng.choice(E, size=min(E, 4 * K), replace=False)] = 5.0 + rng.normal(0, 1e-3, min(E, 4 * K))
+    rows.append(w)                                  # a dense cluster just above the rest
+    return np.array(rows, dtype=np.float32)
+
+
+@pytest.mark.parametrize("E,K", [(256, 8), (256, 22), (512, 22), (512, 36), (1024, 30), (2304, 36),
+                                 (2304, 4)])
+def test_adversarial_rows(R, path, E, K):
+    rng = np.random.default_rng(E * 7 + K)
+    x = adversarial_rows(E, K, rng)
+    for dt in ("f32", "bf16"):
+        from score_top_expert_gb300.workloads import round_to_bf16_values
+        case = make_case(x.shape[0], E, K, dtype=dt, seed=3)
+        case.logits = x if dt == "f32" else round_to_bf16_values(x)
+        for sf in ("softmax", "sigmoid"):
+            run_and_check_topk(R, case, K, sf, c=2.0)
+            if dt == "f32":
+                run_and_check_aux(R, case, K, sf)
