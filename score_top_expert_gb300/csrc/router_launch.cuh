@@ -119,9 +119,18 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
+  // Rows go round-robin over all resident segments.  When they take more
+  // than one round, use the fewest blocks that still need the same number of
+  // rounds, so that every segment carries the same number of rows (no
+  // half-empty last round).
   const long long rows_per_block = static_cast<long long>(p.warps_per_block) * (32 / SEG);
   const long long need = (static_cast<long long>(a.T) + rows_per_block - 1) / rows_per_block;
-  const unsigned grid = static_cast<unsigned>(need < p.max_blocks ? need : p.max_blocks);
+  long long blocks = need;
+  if (need > p.max_blocks) {
+    const long long rounds = (need + p.max_blocks - 1) / p.max_blocks;
+    blocks = (need + rounds - 1) / rounds;
+  }
+  const unsigned grid = static_cast<unsigned>(blocks);
   kern<<<grid, p.warps_per_block * 32, smem, st>>>(a, p.layout, status);
   return cudaGetLastError();
 }
