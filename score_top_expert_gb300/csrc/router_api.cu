@@ -72,7 +72,7 @@ bool device_info(DeviceInfo* out) {
 
 // ---- staged forward plans, computed once per (device, shape) ----------------
 struct PlanKey {
-  int dev, sf, dt, op, E, K;
+  int dev, sf, dt, op, km, E, K;
 };
 struct PlanEntry {
   PlanKey key;
@@ -94,11 +94,18 @@ void staged_shape(int E, int /*K*/, int* seg, int* nc) {
   *nc = E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18));
 }
 
-StagedLayout staged_layout(int seg, int nc, int dt) {
+StagedLayout staged_layout(int seg, int nc, int dt, int km) {
   StagedLayout L{};
   const int d = dt == MR_F32 ? 4 : 2;
+  L.head_bytes = km == 1 ? round_up(4 * seg * nc * 4, 128) : 0;  // the bias row
   L.stage_bytes = 4 * seg * nc * d;  // seg * nc chunks of four logits
   int off = 2 * L.stage_bytes;
+  if (km == 1) {
+    L.work_off = off;
+    off += 4 * seg * nc * 4;  // keys
+    L.grp_off = off;
+    off += 2 * kMaxGroups * 4;
+  }
   L.cand_off = off;
   off += kCandPerLane * seg * 8;
   L.mask_off = off;
@@ -117,14 +124,16 @@ int occupancy_any(int sf, int dt, const StagedPlan& p) {
 
 // Warps per block that keep the most warps resident per SM (shared memory is
 // the limit: one slice per warp).
-bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, int K, StagedPlan* out) {
+bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, int K,
+                 StagedPlan* out) {
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < g_nplans; ++i) {
       const PlanKey& k = g_plans[i].key;
-      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E && k.K == K) {
+      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.km == km && k.E == E &&
+          k.K == K) {
         *out = g_plans[i].plan;
         return g_plans[i].valid;
       }
@@ -133,8 +142,9 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, int K, Sta
   StagedPlan p{};
   staged_shape(E, K, &p.seg, &p.nc);
   p.full = E == 4 * p.seg * p.nc;
-  p.layout = staged_layout(p.seg, p.nc, dt);
+  p.layout = staged_layout(p.seg, p.nc, dt, km);
   p.op = op;
+  p.km = km;
   const int warp_bytes = (32 / p.seg) * p.layout.seg_bytes;
   int best_warps = 0;
   // tuning override: MOE_ROUTER_STAGED_WARPS caps the resident warps per SM
@@ -144,7 +154,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, int K, Sta
     if (v > 0) cap_warps = v;
   }
   for (int w = 1; w <= kStagedMaxWarps; ++w) {
-    const int smem = w * warp_bytes;
+    const int smem = p.layout.head_bytes + w * warp_bytes;
     if (smem > di.smem_per_block) break;
     int blocks = di.smem_per_sm / (smem + 1024);
     blocks = blocks < 2048 / (32 * w) ? blocks : 2048 / (32 * w);
@@ -163,7 +173,8 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int E, int K, Sta
     p.max_blocks = per_sm * di.sms;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_nplans < kPlanCache) g_plans[g_nplans++] = PlanEntry{{dev, sf, dt, op, E, K}, p, valid};
+  if (g_nplans < kPlanCache)
+    g_plans[g_nplans++] = PlanEntry{{dev, sf, dt, op, km, E, K}, p, valid};
   *out = p;
   return valid;
 }
@@ -173,19 +184,19 @@ bool staged_shape_ok(int E, int dt) {
 }
 
 // The staged path serves rows from 256 experts up unless a path is forced.
-bool use_staged(int E, int dt, bool key_on_logit, bool aligned) {
-  if (!key_on_logit || !aligned || !staged_shape_ok(E, dt)) return false;
+bool use_staged(int E, int dt, bool aligned) {
+  if (!aligned || !staged_shape_ok(E, dt)) return false;
   const int path = current_path();
   if (path == MR_PATH_SEGMENT) return false;
   if (path == MR_PATH_STAGED) return true;
   return E >= 256;
 }
 
-int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st) {
+int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStream_t st) {
   DeviceInfo di{};
   if (!device_info(&di)) return MR_ERR_CUDA;
   StagedPlan p{};
-  if (!staged_plan(di, sf, dt, op, a.E, a.K, &p)) return MR_ERR_CUDA;
+  if (!staged_plan(di, sf, dt, op, km, a.E, a.K, &p)) return MR_ERR_CUDA;
   cudaError_t e;
   if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_staged_softmax_f32(a, p, di.status, st)
@@ -313,22 +324,15 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
                    aligned16(routing_map) && aligned16(scores) &&
                    (expert_bias == nullptr || aligned16(expert_bias));
   const int km = (expert_bias != nullptr || grouped) ? 1 : 0;
-  if (use_staged(E, dtype, km == 0, vec)) {
-    FwdArgs a{};
-    a.logits = logits;
-    a.probs = probs;
-    a.map = routing_map;
-    a.scores = scores;
-    a.T = T; a.E = E; a.K = K;
-    a.scaling = scaling_factor;
-    return launch_staged_any(score_func, dtype, a, 0, reinterpret_cast<cudaStream_t>(stream));
-  }
+  const bool staged = use_staged(E, dtype, vec);
   FwdConfig c{};
-  if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
+  if (!staged && !choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;
   c.op = 0;
   c.km = km;
-  c.extra_smem = grouped ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float) : 0;
+  c.extra_smem = (grouped && !staged)
+                     ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float)
+                     : 0;
 
   FwdArgs a{};
   a.logits = logits;
@@ -345,10 +349,13 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
     a.group_size = E / num_groups;
     a.per_group = K / group_topk;
     a.inv_group_size = 1.0f / static_cast<float>(a.group_size);
+    const int lanes = staged ? 32 : c.seg;
     int lpg = 1;
-    while (lpg * 2 * num_groups <= c.seg) lpg *= 2;
+    while (lpg * 2 * num_groups <= lanes) lpg *= 2;
     a.lanes_per_group = lpg;
   }
+  if (staged)
+    return launch_staged_any(score_func, dtype, a, 0, km, reinterpret_cast<cudaStream_t>(stream));
   return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -399,8 +406,8 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.intermediate = intermediate;
   a.T = T; a.E = E; a.K = K;
   a.scaling = 1.0f;
-  if (use_staged(E, dtype, true, vec))
-    return launch_staged_any(score_func, dtype, a, 1, reinterpret_cast<cudaStream_t>(stream));
+  if (use_staged(E, dtype, vec))
+    return launch_staged_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));
   FwdConfig c{};
   if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;

@@ -83,10 +83,11 @@ __device__ __forceinline__ int half_of(int j, int u) {
 }
 
 // Sum of the M largest keys of each expert group, for the group-limited
-// pre-selection; writes the kept flags of the groups to sm.kept.
+// pre-selection; writes the groups' scores to gs[] and their kept flags to
+// kept[] (both in shared memory, num_groups entries).
 template <int SEG>
 __device__ __forceinline__ void group_select(const FwdArgs& a, const float* rowkeys,
-                                             FwdSegSmem<SEG>& sm) {
+                                             float* gs_out, int* kept_out) {
   const unsigned smask = seg_mask<SEG>();
   const int li = threadIdx.x & (SEG - 1);
   const int G = a.num_groups, Eg = a.group_size, M = a.per_group;
@@ -160,17 +161,17 @@ __device__ __forceinline__ void group_select(const FwdArgs& a, const float* rowk
       }
       gsum = above + static_cast<float>(M - n_above) * key_to_float(t);
     }
-    if (act && r == 0) sm.gs[g] = gsum;
+    if (act && r == 0) gs_out[g] = gsum;
   }
   __syncwarp(smask);
   for (int g = li; g < G; g += SEG) {
-    const float mine = sm.gs[g];
+    const float mine = gs_out[g];
     int rank = 0;
     for (int h = 0; h < G; ++h) {
-      const float o = sm.gs[h];
+      const float o = gs_out[h];
       rank += (o > mine) || (o == mine && h < g);
     }
-    sm.kept[g] = rank < a.group_topk;
+    kept_out[g] = rank < a.group_topk;
   }
   __syncwarp(smask);
 }
@@ -273,7 +274,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
         for (int u = 0; u < 4; ++u)
           if (elem_ok(j, u)) rowkeys[4 * (li + SEG * j) + u] = key_to_float(kk[j][u]);
       __syncwarp(smask);
-      group_select<SEG>(a, rowkeys, sm);
+      group_select<SEG>(a, rowkeys, sm.gs, sm.kept);
 #pragma unroll
       for (int j = 0; j < NC; ++j)
 #pragma unroll

@@ -33,6 +33,14 @@
 //   5  outputs from the scores and the bitmask: probs, map, scores (top-K)
 //      or q, map, intermediate (aux scores).
 // Keying on the logit is exact: softmax and sigmoid are strictly increasing.
+//
+// Key mode KM 1 (top-K with a bias and/or groups): before pass 1 the row's
+// keys s + bias are built in a per-warp fp32 key row (the bias sits in shared
+// memory once per block); with groups, a group scores the sum of its
+// per_group largest keys, and the keys of every group outside the
+// group_topk best are set to -inf.  Passes 1-3 then select on that key row
+// exactly as KM 0 selects on the logits; the scores are recomputed from the
+// logits in pass 5.
 #pragma once
 
 #include "router_common.cuh"
@@ -46,6 +54,9 @@ namespace moe_router {
 // every lane reads every chunk without a bound check; the padding is never
 // written by the copy and is masked out when the row is not full.
 struct StagedLayout {
+  int head_bytes;   // KM 1: the block's bias row (fp32, padded), before the slices
+  int work_off;     // KM 1: the row's keys (fp32, padded)
+  int grp_off;      // KM 1: group scores and kept flags (32 + 32 words)
   int stage_bytes;  // SEG * NC chunks of 4 logits
   int cand_off;     // kCandPerLane * SEG packed candidate words
   int mask_off;     // selection words, one bit per expert of the padded row
@@ -156,10 +167,11 @@ __device__ __forceinline__ void compact_marked(const unsigned char* stage, const
 // repeat, the ranks of the tied candidates coincide and no longer sum to
 // 0 + 1 + ... + (total - 1), and the rank is recounted on the full
 // (key, ~index) words, which is what bf16 rows do directly.
-template <int SEG, int NOWN, bool SIG, bool TRY32>
+template <int SEG, int NOWN, bool SIG, bool TRY32, class ScoreOf>
 __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, int total,
                                                 int li, int K, int target, uint32_t* selmask,
-                                                uint32_t* next_key, float& part) {
+                                                uint32_t* next_key, float& part,
+                                                const ScoreOf& score_of) {
   const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(cand) + 1;  // keys
   unsigned long long own[NOWN];
   int rank[NOWN];
@@ -195,7 +207,7 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
       if (rank[r] < K) {
         const uint32_t idx = ~static_cast<uint32_t>(own[r]);
         atomicOr(&selmask[idx >> 5], 1u << (idx & 31));
-        if constexpr (SIG) part += sigmoid_f32(key_to_float(static_cast<uint32_t>(own[r] >> 32)));
+        if constexpr (SIG) part += score_of(static_cast<int>(idx), static_cast<uint32_t>(own[r] >> 32));
       }
       if (rank[r] == target) *next_key = static_cast<uint32_t>(own[r] >> 32);
     }
@@ -207,22 +219,27 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
 template <int DT, int NC>
 constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18) ? 128 : 168; }
 
-template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
 __global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC>()))
 router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   constexpr int CAP = kCandPerLane * SEG;
   constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
   constexpr int D = DT == DT_F32 ? 4 : 2;
   constexpr bool kSigTopk = (OP == 0 && SF == SF_SIGMOID);
-  constexpr bool kStore = (DT == DT_F32);       // scores kept over the fp32 logits
-  constexpr bool kNeedSum = (SF == SF_SOFTMAX || OP == 1);
+  constexpr bool kStore = (DT == DT_F32 && KM == 0);  // scores kept over the fp32 logits
+  constexpr bool kNeedSum = (SF == SF_SOFTMAX || OP == 1) && KM == 0;
+  constexpr int KDT = KM == 0 ? DT : DT_F32;  // type of the selection keys
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int li = lane & (SEG - 1);
   const int seg = (threadIdx.x >> 5) * RPW + lane / SEG;  // segment in the block
   const int spb = (blockDim.x >> 5) * RPW;                // segments per block
   const unsigned smask = seg_mask<SEG>();
-  unsigned char* base = smem + seg * L.seg_bytes;
+  unsigned char* base = smem + L.head_bytes + seg * L.seg_bytes;
+  float* bias_s = reinterpret_cast<float*>(smem);           // KM 1
+  float* work = reinterpret_cast<float*>(base + L.work_off);  // KM 1
+  float* gs = reinterpret_cast<float*>(base + L.grp_off);     // KM 1, grouped
+  int* kept = reinterpret_cast<int*>(gs + kMaxGroups);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   uint32_t* next_key = reinterpret_cast<uint32_t*>(bars + 2);
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(base + L.cand_off);
@@ -235,8 +252,14 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   const unsigned char* src = static_cast<const unsigned char*>(a.logits);
   const int target = K - 1 + (K / 2 > 4 ? K / 2 : 4);  // rank giving the next threshold
 
-  // logits of chunk j; padding chunks of a partial row read as -inf
+  // logits (KM 0) or keys (KM 1) of chunk j; padding chunks of a partial
+  // row read as -inf
   auto load_x = [&](const unsigned char* stage, int j, float (&x)[4]) {
+    if constexpr (KM == 1) {
+      const float4 t = lds_f4(reinterpret_cast<const unsigned char*>(work) + 16 * (li + SEG * j));
+      x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+      return;
+    }
     const int c = li + SEG * j;
     stage_x<DT>(stage, c, x);
     if constexpr (!FULL) {
@@ -246,6 +269,11 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
   };
 
+  if constexpr (KM == 1) {
+    for (int i = threadIdx.x; i < 4 * SEG * NC; i += blockDim.x)
+      bias_s[i] = (a.bias != nullptr && i < E) ? a.bias[i] : 0.0f;
+    __syncthreads();
+  }
   if (li == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
@@ -296,6 +324,74 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
 
 #pragma unroll
     for (int w = li; w < NC * SEG / 8; w += SEG) selmask[w] = 0u;
+
+    // ---- 0 (KM 1): keys s + bias, group mask ------------------------------------------
+    float xmax_l2e = 0.0f;  // KM 1 softmax: row max of the logits * log2e
+    float xinv = 1.0f;      // KM 1 softmax: 1 / row sum of exp
+    if constexpr (KM == 1) {
+      auto logits_of = [&](int j, float (&x)[4]) {
+        const int c = li + SEG * j;
+        stage_x<DT>(stage, c, x);
+        if constexpr (!FULL) {
+          const bool okc = c < nchunks;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[u] = okc ? x[u] : -INFINITY;
+        }
+      };
+      if constexpr (SF == SF_SOFTMAX) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          float x[4];
+          logits_of(j, x);
+          mx = fmaxf(mx, fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+        }
+        xmax_l2e = seg_max<SEG>(mx) * kLog2e;
+        float sm0 = 0.0f, sm1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          float x[4];
+          logits_of(j, x);
+          const float add = (exp_shifted(x[0], xmax_l2e) + exp_shifted(x[1], xmax_l2e)) +
+                            (exp_shifted(x[2], xmax_l2e) + exp_shifted(x[3], xmax_l2e));
+          if (j & 1) sm1 += add; else sm0 += add;
+        }
+        xinv = 1.0f / seg_sum<SEG>(sm0 + sm1);
+      }
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        const int c = li + SEG * j;
+        float x[4], k[4];
+        logits_of(j, x);
+        const float4 bv = lds_f4(bias_s + 4 * c);
+        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float sc = (SF == SF_SOFTMAX) ? exp_shifted(x[u], xmax_l2e) * xinv : sigmoid_f32(x[u]);
+          k[u] = (FULL || c < nchunks) ? sc + bb[u] : -INFINITY;
+        }
+        sts_f4(work + 4 * c, make_float4(k[0], k[1], k[2], k[3]));
+      }
+      if (a.num_groups > 1) {
+        __syncwarp(smask);
+        group_select<SEG>(a, work, gs, kept);
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          const int c = li + SEG * j;
+          if (FULL || c < nchunks) {
+            float4 t = lds_f4(work + 4 * c);
+            float k[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int g = static_cast<int>((static_cast<float>(4 * c + u) + 0.5f) * a.inv_group_size);
+              if (!kept[g]) k[u] = -INFINITY;
+            }
+            sts_f4(work + 4 * c, make_float4(k[0], k[1], k[2], k[3]));
+          }
+        }
+      }
+      __syncwarp(smask);
+    }
 
     // ---- 1: maxima, speculative candidate mask -------------------------------------
     float hm[2] = {-INFINITY, -INFINITY};
@@ -415,19 +511,25 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         }
       }
     }
+    // the score s of a selected candidate (sigmoid top-K sums them)
+    auto score_of = [&](int idx, uint32_t key) -> float {
+      if constexpr (KM == 1) return sigmoid_f32(stage_x1<DT>(stage, idx));
+      else return sigmoid_f32(key_to_float(key));
+    };
     if (cand_ok) {
-      compact_marked<DT, SEG, NC>(stage, cm, seg_exclusive_scan<SEG>(cnt), li, cand);
+      compact_marked<KDT, SEG, NC>(KM == 1 ? reinterpret_cast<const unsigned char*>(work) : stage,
+                                   cm, seg_exclusive_scan<SEG>(cnt), li, cand);
       __syncwarp(smask);
       const int nown = (total + SEG - 1) / SEG;
       const int tgt = target < total - 1 ? target : total - 1;
       if (nown <= 1)
-        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
       else if (nown == 2)
-        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
       else if (nown == 3)
-        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
       else
-        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part);
+        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
       __syncwarp(smask);
       spec_t = key_to_float(*next_key);
       have_spec = true;
@@ -467,7 +569,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         for (int u = 0; u < 4; ++u) {
           if (x[u] > v || (x[u] == v && 4 * c + u <= ti)) {
             bits |= 1u << u;
-            if constexpr (kSigTopk) part += sigmoid_f32(x[u]);
+            if constexpr (kSigTopk) part += score_of(4 * c + u, ordered_key(x[u]));
           }
         }
         if (bits) atomicOr(&selmask[c >> 3], bits << (4 * (c & 7)));
@@ -478,8 +580,8 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     __syncwarp(0xffffffffu);  // reconverge the segments of the warp
 
     // ---- 4: scores ----------------------------------------------------------------------
-    const float max_l2e = row_max * kLog2e;
-    float inv = 1.0f;
+    const float max_l2e = KM == 1 ? xmax_l2e : row_max * kLog2e;
+    float inv = xinv;
     if constexpr (kNeedSum || kStore) {
       float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll

@@ -103,17 +103,19 @@ struct StagedPlan {
   int seg;         // lanes per row (32 in this build)
   int nc;          // chunks of 4 experts per lane
   int op;
+  int km;          // key mode: 0 logits, 1 s + bias (and groups), top-K only
   bool full;       // E == 4 * seg * nc: no padding chunks
 };
 
 // compiled (SEG, NC) pairs of the staged forward
 #define MR_STAGED_SHAPES(X) X(32, 2) X(32, 4) X(32, 8) X(32, 18)
 
-template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
 cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* status,
                                cudaStream_t st) {
-  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL>;
-  const size_t smem = static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes;
+  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL, KM>;
+  const size_t smem = p.layout.head_bytes +
+                      static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -136,9 +138,9 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
 }
 
 // Resident blocks per SM of one staged instantiation (occupancy query).
-template <int SF, int DT, int SEG, int NC, int OP, bool FULL>
+template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
 int staged_blocks_per_sm(int warps_per_block, size_t smem) {
-  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL>;
+  auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL, KM>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -152,13 +154,16 @@ int staged_blocks_per_sm(int warps_per_block, size_t smem) {
 
 template <int SF, int DT>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
-#define MR_STAGED_CASE(S, N)                                                            \
-  if (p.seg == S && p.nc == N) {                                                        \
-    if (p.full)                                                                         \
-      return p.op == 0 ? launch_staged_inst<SF, DT, S, N, 0, true>(a, p, status, st)    \
-                       : launch_staged_inst<SF, DT, S, N, 1, true>(a, p, status, st);   \
-    return p.op == 0 ? launch_staged_inst<SF, DT, S, N, 0, false>(a, p, status, st)     \
-                     : launch_staged_inst<SF, DT, S, N, 1, false>(a, p, status, st);    \
+#define MR_STAGED_CASE(S, N)                                                               \
+  if (p.seg == S && p.nc == N) {                                                           \
+    if (p.op == 1)                                                                         \
+      return p.full ? launch_staged_inst<SF, DT, S, N, 1, true, 0>(a, p, status, st)       \
+                    : launch_staged_inst<SF, DT, S, N, 1, false, 0>(a, p, status, st);     \
+    if (p.km == 1)                                                                         \
+      return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 1>(a, p, status, st)       \
+                    : launch_staged_inst<SF, DT, S, N, 0, false, 1>(a, p, status, st);     \
+    return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 0>(a, p, status, st)         \
+                  : launch_staged_inst<SF, DT, S, N, 0, false, 0>(a, p, status, st);       \
   }
   MR_STAGED_SHAPES(MR_STAGED_CASE)
 #undef MR_STAGED_CASE
@@ -167,16 +172,19 @@ cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cu
 
 template <int SF, int DT>
 int staged_occupancy(const StagedPlan& p) {
-  const size_t smem =
+  const size_t smem = p.layout.head_bytes +
       static_cast<size_t>(p.warps_per_block) * (32 / p.seg) * p.layout.seg_bytes;
-#define MR_STAGED_OCC(S, N)                                                             \
-  if (p.seg == S && p.nc == N) {                                                        \
-    const int w = p.warps_per_block;                                                    \
-    if (p.full)                                                                         \
-      return p.op == 0 ? staged_blocks_per_sm<SF, DT, S, N, 0, true>(w, smem)           \
-                       : staged_blocks_per_sm<SF, DT, S, N, 1, true>(w, smem);          \
-    return p.op == 0 ? staged_blocks_per_sm<SF, DT, S, N, 0, false>(w, smem)            \
-                     : staged_blocks_per_sm<SF, DT, S, N, 1, false>(w, smem);           \
+#define MR_STAGED_OCC(S, N)                                                                \
+  if (p.seg == S && p.nc == N) {                                                           \
+    const int w = p.warps_per_block;                                                       \
+    if (p.op == 1)                                                                         \
+      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 1, true, 0>(w, smem)              \
+                    : staged_blocks_per_sm<SF, DT, S, N, 1, false, 0>(w, smem);            \
+    if (p.km == 1)                                                                         \
+      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 1>(w, smem)              \
+                    : staged_blocks_per_sm<SF, DT, S, N, 0, false, 1>(w, smem);            \
+    return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 0>(w, smem)                \
+                  : staged_blocks_per_sm<SF, DT, S, N, 0, false, 0>(w, smem);              \
   }
   MR_STAGED_SHAPES(MR_STAGED_OCC)
 #undef MR_STAGED_OCC

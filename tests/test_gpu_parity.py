@@ -270,7 +270,7 @@ def test_tied_logits(R, path, E):
 # bias and groups
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("sf", ["softmax", "sigmoid"])
-def test_bias(R, sf):
+def test_bias(R, path, sf):
     for E, K in ((64, 4), (256, 8), (512, 22), (2304, 36)):
         case = make_case(513, E, K, seed=E, with_bias=True, bias_range=0.1)
         run_and_check_topk(R, case, K, sf, c=2.5, bias=case.expert_bias)
@@ -284,7 +284,7 @@ GROUPED = [  # (E, num_groups, group_topk, K)
 
 
 @pytest.mark.parametrize("E,G,gk,K", GROUPED, ids=[f"E{e}-G{g}-gk{k}-K{K}" for e, g, k, K in GROUPED])
-def test_grouped(R, E, G, gk, K):
+def test_grouped(R, path, E, G, gk, K):
     for dt in ("f32", "bf16"):
         case = make_case(300, E, K, dtype=dt, seed=E + G, with_bias=True)
         for sf in ("sigmoid", "softmax"):
