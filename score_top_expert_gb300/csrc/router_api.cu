@@ -353,6 +353,13 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
     int lpg = 1;
     while (lpg * 2 * num_groups <= lanes) lpg *= 2;
     a.lanes_per_group = lpg;
+    // staged path: groups of a power-of-two number of 4-expert chunks (at
+    // most a warp) with at most 4 keys summed are scored in registers
+    const int gl = a.group_size / 4;
+    a.group_chunk_lanes = (staged && a.group_size % 4 == 0 && gl >= 1 && gl <= 32 &&
+                           (gl & (gl - 1)) == 0 && a.per_group <= kTopMRegs)
+                              ? gl
+                              : 0;
   }
   if (staged)
     return launch_staged_any(score_func, dtype, a, 0, km, reinterpret_cast<cudaStream_t>(stream));

@@ -52,6 +52,9 @@ struct FwdArgs {
   int group_size;         // E / num_groups
   int per_group;          // K / group_topk
   int lanes_per_group;    // power of two, SEG / lanes_per_group >= 1
+  int group_chunk_lanes;  // staged path: lanes holding one group (group_size / 4,
+                          // a power of two <= 32) when groups align with chunks
+                          // and per_group <= 4; else 0 (shared-memory scan)
   float inv_group_size;   // 1 / group_size (exact enough for idx < 4096)
   float scaling;
 };

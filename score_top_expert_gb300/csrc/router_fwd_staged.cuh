@@ -214,13 +214,13 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
   }
 }
 
-// Registers of the 18-chunk bf16 kernels are capped so that they keep 16
+// Registers of the 18-chunk bf16 logit-keyed kernels are capped so that they keep 16
 // warps per SM (their shared memory would allow 21; uncapped they need 160).
-template <int DT, int NC>
-constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18) ? 128 : 168; }
+template <int DT, int NC, int KM>
+constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18 && KM == 0) ? 128 : 168; }
 
 template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
-__global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC>()))
+__global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC, KM>()))
 router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   constexpr int CAP = kCandPerLane * SEG;
   constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
@@ -358,6 +358,13 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         }
         xinv = 1.0f / seg_sum<SEG>(sm0 + sm1);
       }
+      // groups that align with chunks: a group is L = group_size / 4 lanes of
+      // one chunk column j; its top-M sum is a butterfly merge of the lanes'
+      // top-M lists in registers
+      const int L = a.group_chunk_lanes;
+      const bool fast_groups = a.num_groups > 1 && L > 0;
+      const int M = a.per_group;
+      float gsum[NC];
 #pragma unroll
       for (int j = 0; j < NC; ++j) {
         const int c = li + SEG * j;
@@ -371,8 +378,78 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           k[u] = (FULL || c < nchunks) ? sc + bb[u] : -INFINITY;
         }
         sts_f4(work + 4 * c, make_float4(k[0], k[1], k[2], k[3]));
+        if (fast_groups && M <= 2) {
+          // top-2 pair (t0 >= t1); M == 1 uses t0 only
+          float t0 = fmaxf(fmaxf(k[0], k[1]), fmaxf(k[2], k[3]));
+          float t1 = fmaxf(fmaxf(fminf(k[0], k[1]), fminf(k[2], k[3])),
+                           fminf(fmaxf(k[0], k[1]), fmaxf(k[2], k[3])));
+          for (int o = L / 2; o > 0; o >>= 1) {
+            const float p0 = __shfl_xor_sync(smask, t0, o);
+            const float p1 = __shfl_xor_sync(smask, t1, o);
+            t1 = fmaxf(fminf(t0, p0), fmaxf(t1, p1));
+            t0 = fmaxf(t0, p0);
+          }
+          gsum[j] = M == 1 ? t0 : t0 + t1;
+        } else if (fast_groups) {
+          float top[kTopMRegs];
+#pragma unroll
+          for (int i = 0; i < kTopMRegs; ++i) top[i] = -INFINITY;
+          auto insert = [&](float w) {
+#pragma unroll
+            for (int i = 0; i < kTopMRegs; ++i) {
+              if (i < M) {
+                const float hi = fmaxf(top[i], w);
+                w = fminf(top[i], w);
+                top[i] = hi;
+              }
+            }
+          };
+#pragma unroll
+          for (int u = 0; u < 4; ++u) insert(k[u]);
+          for (int o = L / 2; o > 0; o >>= 1) {
+            float other[kTopMRegs];
+#pragma unroll
+            for (int i = 0; i < kTopMRegs; ++i) other[i] = __shfl_xor_sync(smask, top[i], o);
+#pragma unroll
+            for (int i = 0; i < kTopMRegs; ++i) insert(other[i]);
+          }
+          float g = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kTopMRegs; ++i)
+            if (i < M) g += top[i];
+          gsum[j] = g;
+        }
       }
-      if (a.num_groups > 1) {
+      if (fast_groups) {
+        // rank every group against all others (ties: lower group index) by
+        // reading each group's score from its first lane; drop the keys of
+        // groups outside the group_topk best
+        const int gpj = SEG / L;  // groups per chunk column
+        int grank[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) grank[j] = 0;
+#pragma unroll
+        for (int jj = 0; jj < NC; ++jj) {
+          for (int q = 0; q < gpj; ++q) {
+            const int h = jj * gpj + q;
+            const float hv = __shfl_sync(smask, gsum[jj], q * L);
+            if (h < a.num_groups) {
+#pragma unroll
+              for (int j = 0; j < NC; ++j) {
+                const int g = j * gpj + li / L;
+                grank[j] += (hv > gsum[j]) || (hv == gsum[j] && h < g);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          const int g = j * gpj + li / L;
+          if (g < a.num_groups && grank[j] >= a.group_topk)
+            sts_f4(work + 4 * (li + SEG * j),
+                   make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY));
+        }
+      } else if (a.num_groups > 1) {
         __syncwarp(smask);
         group_select<SEG>(a, work, gs, kept);
 #pragma unroll

@@ -280,6 +280,8 @@ GROUPED = [  # (E, num_groups, group_topk, K)
     (256, 8, 4, 8), (256, 8, 1, 8), (256, 8, 8, 8), (256, 4, 2, 12), (256, 16, 4, 8),
     (256, 32, 8, 16), (64, 2, 1, 6), (512, 8, 2, 22 - 22 % 2), (2304, 16, 4, 36),
     (2304, 8, 1, 36), (120, 3, 2, 10), (12, 4, 2, 2), (60, 5, 5, 15), (1000, 10, 3, 30),
+    # groups that align with 4-expert chunks (scored in registers on the staged path)
+    (512, 16, 4, 8), (1024, 32, 4, 16), (384, 12, 4, 8), (2304, 18, 9, 36), (256, 32, 2, 8),
 ]
 
 
