@@ -219,6 +219,17 @@ MR_API int moe_router_force_fwd_lanes(int lanes);
  */
 MR_API int moe_router_device_status(int* status);
 
+/*
+ * Diagnostic for the failure path above: enqueue one small kernel that waits,
+ * with the same bounded wait the router kernels use, for a barrier phase that
+ * nothing completes.  After about timeout_us microseconds (1..1000000) the
+ * wait gives up and the device status word becomes 1, which
+ * moe_router_device_status then reports (and clears).  No fault, trap or hang
+ * is involved: the kernel simply returns.  MR_ERR_INVALID for timeout_us out
+ * of range.
+ */
+MR_API int moe_router_selftest_bounded_wait(unsigned timeout_us, mr_stream_t stream);
+
 /* Library ABI version: 100 * major + minor. */
 MR_API int moe_router_version(void);
 

@@ -16,6 +16,21 @@ using namespace moe_router;
 // Status word the kernels write when a bounded wait gives up (one per device).
 __device__ int g_mr_device_status;
 
+// Diagnostic: one warp waits, with a bounded wait, for an mbarrier phase
+// that nothing completes; the wait gives up after limit_ns and the status
+// word records the timeout, exactly as a router kernel does when a bulk copy
+// never lands.
+__global__ void selftest_bounded_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar, 0u, limit_ns));
+  if (!ok && threadIdx.x == 0) atomicExch(status, kDeviceWaitTimeout);
+}
+
 namespace {
 
 constexpr int kVersion = 100;
@@ -486,6 +501,15 @@ int moe_router_device_status(int* status) {
   }
   *status = v;
   return MR_OK;
+}
+
+int moe_router_selftest_bounded_wait(unsigned timeout_us, mr_stream_t stream) {
+  if (timeout_us == 0 || timeout_us > 1000000u) return MR_ERR_INVALID;
+  DeviceInfo di{};
+  if (!device_info(&di)) return MR_ERR_CUDA;
+  selftest_bounded_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      di.status, 1000ull * timeout_us);
+  return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
 int moe_router_version(void) { return kVersion; }

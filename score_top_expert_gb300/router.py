@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.moe_router_force_fwd_lanes.argtypes = [i]
         L.moe_router_version.argtypes = []
         L.moe_router_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        L.moe_router_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+        L.moe_router_selftest_bounded_wait.restype = ctypes.c_int
         L.moe_router_strerror.argtypes = [i]
         L.moe_router_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -219,3 +221,12 @@ def device_status() -> int:
     v = ctypes.c_int(0)
     _check("moe_router_device_status", lib().moe_router_device_status(ctypes.byref(v)))
     return v.value
+
+
+def selftest_bounded_wait(timeout_us: int, device=None) -> None:
+    """Enqueue the diagnostic kernel whose bounded wait always runs out (see
+    moe_router_selftest_bounded_wait in the header)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check("moe_router_selftest_bounded_wait",
+               lib().moe_router_selftest_bounded_wait(int(timeout_us), _stream(dev)))

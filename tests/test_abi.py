@@ -124,3 +124,8 @@ def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(r._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         r.lib()
+
+
+def test_selftest_rejects_out_of_range_timeouts(L):
+    assert L.moe_router_selftest_bounded_wait(0, None) == -1
+    assert L.moe_router_selftest_bounded_wait(1000001, None) == -1

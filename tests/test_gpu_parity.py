@@ -387,3 +387,18 @@ def test_adversarial_rows(R, path, E, K):
             run_and_check_topk(R, case, K, sf, c=2.0)
             if dt == "f32":
                 run_and_check_aux(R, case, K, sf)
+
+
+def test_bounded_wait_reports_a_timeout(R):
+    """The bounded mbarrier wait gives up, reports status 1, and the context
+    stays usable: a wait that nothing can complete runs out after 2 ms."""
+    assert R.device_status() == 0
+    R.selftest_bounded_wait(2000)
+    torch.cuda.synchronize()
+    assert R.device_status() == 1
+    assert R.device_status() == 0          # reading cleared it
+    case = make_case(64, 512, 8, seed=11)   # the router still works afterwards
+    run_and_check_topk(R, case, 8, "softmax")
+    assert R.device_status() == 0
+    with pytest.raises(R.RouterError):
+        R.selftest_bounded_wait(0)
