@@ -52,7 +52,14 @@ extern "C" {
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st* mr_stream_t;
 
-typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1 } mr_score_func;
+/*
+ * MR_SOFTMAX_POST is the post-softmax router (TransformerEngine PR #3012's
+ * review names the ScoreFunc x use_pre_softmax combinations; onnxruntime PR
+ * #33366 calls it normalize_routing_weights): it selects and scores like
+ * MR_SOFTMAX, and its probs are the softmax of the K selected logits.  The
+ * aux-score calls take MR_SOFTMAX and MR_SIGMOID only.
+ */
+typedef enum { MR_SOFTMAX = 0, MR_SIGMOID = 1, MR_SOFTMAX_POST = 2 } mr_score_func;
 typedef enum { MR_F32 = 0, MR_BF16 = 1 } mr_dtype;
 
 typedef enum {
@@ -84,7 +91,8 @@ typedef enum {
  *             the group_topk best groups stay selectable
  *   select    the K largest keys among selectable experts (ties: lower index)
  *   probs     softmax: c * s on selected experts, 0 elsewhere (no renormalising)
- *             sigmoid: c * s / (sum of s over the selected), 0 elsewhere
+ *             sigmoid and post-softmax: c * s / (sum of s over the selected),
+ *             0 elsewhere
  *   scores    s (fp32), every expert
  * with c = scaling_factor.
  *
@@ -120,6 +128,8 @@ MR_API int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int
  *   softmax: D = c * sum_j m_j g_j s_j;   gx_j = s_j * (c m_j g_j - D)
  *   sigmoid: S = sum_j m_j s_j, D = sum_j m_j g_j s_j;
  *            gx_j = m_j * (c / S) * (g_j - D / S) * s_j * (1 - s_j)
+ *   post-softmax (s the full softmax): S, D as for sigmoid;
+ *            gx_j = m_j * (c / S) * (g_j - D / S) * s_j
  *
  * grad_probs   [T,E] dtype, input
  * routing_map  [T,E] uint8 (nonzero = selected), input from router_topk_fwd
@@ -152,7 +162,8 @@ MR_API int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,
  * intermediate  [T,E] float, output sig (sigmoid: required; softmax: may be
  *               NULL, and if given receives q again)
  *
- * Errors: as router_topk_fwd for T, E, K, dtype, score_func; when T > 0, NULL
+ * Errors: as router_topk_fwd for T, E, K, dtype, score_func (MR_SOFTMAX_POST
+ *   is MR_ERR_INVALID here); when T > 0, NULL
  *   logits, scores or routing_map, or NULL intermediate with sigmoid:
  *   MR_ERR_INVALID.
  */

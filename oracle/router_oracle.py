@@ -26,6 +26,10 @@ notes):
   pre-softmax order) and the selected probabilities are not renormalised;
 * sigmoid probabilities are renormalised over the K selected experts with the
   unbiased scores: p_i = c * s_i / sum_sel s_j, with no epsilon;
+* the post-softmax variant ("softmax_post", TransformerEngine's
+  use_pre_softmax = false, onnxruntime's normalize_routing_weights) selects
+  like softmax and renormalises the softmax over the K selected experts:
+  p_i = c * s_i / sum_sel s_j (= c * softmax of the selected logits);
 * the selection key is s_i + b_i (b = optional per-expert bias, selection
   only); ties go to the lower expert index, and -0.0 equals +0.0;
 * group-limited selection: E splits into num_groups contiguous groups; a
@@ -44,6 +48,7 @@ import numpy as np
 
 SOFTMAX = "softmax"
 SIGMOID = "sigmoid"
+SOFTMAX_POST = "softmax_post"
 
 # A row is a near tie when the keys on either side of its top-K boundary are
 # distinct but within this relative distance of each other.
@@ -56,11 +61,12 @@ NEAR_TIE_REL = 1e-6
 def score_row(x: np.ndarray, score_func: str) -> np.ndarray:
     """Per-expert score of one token row, in float64.
 
-    softmax: s_i = exp(x_i - max x) / sum_j exp(x_j - max x) over all E.
+    softmax (and softmax_post): s_i = exp(x_i - max x) / sum_j exp(x_j - max x)
+    over all E.
     sigmoid: s_i = 1 / (1 + exp(-x_i)).
     """
     x = np.asarray(x, dtype=np.float64)
-    if score_func == SOFTMAX:
+    if score_func in (SOFTMAX, SOFTMAX_POST):
         e = np.exp(x - x.max())
         return e / e.sum()
     if score_func == SIGMOID:
@@ -142,7 +148,7 @@ def topk_fwd_row(x, K, score_func, num_groups=0, group_topk=0,
 
     if score_func == SOFTMAX:                                      # step 5
         probs = np.where(m, scaling_factor * s, 0.0)
-    else:
+    else:  # sigmoid, softmax_post: renormalised over the selected
         probs = np.where(m, scaling_factor * s / s[sel].sum(), 0.0)
 
     near = False
@@ -185,6 +191,9 @@ def topk_bwd_row(g, m, s, score_func, scaling_factor=1.0):
     softmax (p = c m s):       D = c sum_j m_j g_j s_j,  gx_j = s_j (c m_j g_j - D)
     sigmoid (p = c m s / S):   S = sum_j m_j s_j,  D = sum_j m_j g_j s_j,
                                gx_j = m_j (c / S) (g_j - D / S) s_j (1 - s_j)
+    softmax_post (p = c m s / S with s the full softmax, i.e. c times the
+                  softmax of the selected logits):
+                               gx_j = m_j (c / S) (g_j - D / S) s_j
     """
     g = np.asarray(g, dtype=np.float64)
     s = np.asarray(s, dtype=np.float64)
@@ -197,6 +206,10 @@ def topk_bwd_row(g, m, s, score_func, scaling_factor=1.0):
         S = np.sum(m * s)                      # pass 1
         D = np.sum(m * g * s)
         return m * (c / S) * (g - D / S) * s * (1.0 - s)   # pass 2
+    if score_func == SOFTMAX_POST:
+        S = np.sum(m * s)                      # pass 1
+        D = np.sum(m * g * s)
+        return m * (c / S) * (g - D / S) * s               # pass 2
     raise ValueError(score_func)
 
 

@@ -134,6 +134,9 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km) {
 int occupancy_any(int sf, int dt, const StagedPlan& p) {
   if (sf == MR_SOFTMAX)
     return dt == MR_F32 ? occupancy_staged_softmax_f32(p) : occupancy_staged_softmax_bf16(p);
+  if (sf == MR_SOFTMAX_POST)
+    return dt == MR_F32 ? occupancy_staged_softmaxpost_f32(p)
+                        : occupancy_staged_softmaxpost_bf16(p);
   return dt == MR_F32 ? occupancy_staged_sigmoid_f32(p) : occupancy_staged_sigmoid_bf16(p);
 }
 
@@ -216,6 +219,9 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStre
   if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_staged_softmax_f32(a, p, di.status, st)
                      : launch_staged_softmax_bf16(a, p, di.status, st);
+  } else if (sf == MR_SOFTMAX_POST) {
+    e = dt == MR_F32 ? launch_staged_softmaxpost_f32(a, p, di.status, st)
+                     : launch_staged_softmaxpost_bf16(a, p, di.status, st);
   } else {
     e = dt == MR_F32 ? launch_staged_sigmoid_f32(a, p, di.status, st)
                      : launch_staged_sigmoid_bf16(a, p, di.status, st);
@@ -225,7 +231,7 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStre
 
 int check_shape(int dtype, int T, int E, int K, int sf) {
   if (dtype != MR_F32 && dtype != MR_BF16) return MR_ERR_INVALID;
-  if (sf != MR_SOFTMAX && sf != MR_SIGMOID) return MR_ERR_INVALID;
+  if (sf != MR_SOFTMAX && sf != MR_SIGMOID && sf != MR_SOFTMAX_POST) return MR_ERR_INVALID;
   if (T < 0 || E < 1 || K < 1 || K > E) return MR_ERR_INVALID;
   if (static_cast<long long>(T) * static_cast<long long>(E) > INT_MAX) return MR_ERR_INVALID;
   if (E > MR_MAX_EXPERTS || K > MR_MAX_TOPK) return MR_ERR_UNSUPPORTED;
@@ -311,6 +317,9 @@ int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStr
   cudaError_t e;
   if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_fwd_softmax_f32(a, c, st) : launch_fwd_softmax_bf16(a, c, st);
+  } else if (sf == MR_SOFTMAX_POST) {
+    e = dt == MR_F32 ? launch_fwd_softmaxpost_f32(a, c, st)
+                     : launch_fwd_softmaxpost_bf16(a, c, st);
   } else {
     e = dt == MR_F32 ? launch_fwd_sigmoid_f32(a, c, st) : launch_fwd_sigmoid_bf16(a, c, st);
   }
@@ -414,6 +423,7 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
                           mr_stream_t stream) {
   const int rc = check_shape(dtype, T, E, K, score_func);
   if (rc != MR_OK) return rc;
+  if (score_func == MR_SOFTMAX_POST) return MR_ERR_INVALID;  // aux scores: softmax or sigmoid
   if (T > 0 && (logits == nullptr || scores == nullptr || routing_map == nullptr ||
                 (score_func == MR_SIGMOID && intermediate == nullptr)))
     return MR_ERR_INVALID;
@@ -444,6 +454,7 @@ int router_aux_scores_bwd(const float* grad_scores, const float* saved, mr_dtype
                           void* grad_logits, mr_stream_t stream) {
   const int rc = check_shape(dtype, T, E, K, score_func);
   if (rc != MR_OK) return rc;
+  if (score_func == MR_SOFTMAX_POST) return MR_ERR_INVALID;
   if (T > 0 && (grad_scores == nullptr || saved == nullptr || grad_logits == nullptr))
     return MR_ERR_INVALID;
   if (T == 0) return MR_OK;

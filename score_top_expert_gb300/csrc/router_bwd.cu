@@ -8,6 +8,10 @@ cudaError_t launch_bwd_any(int sf, int dt, const BwdArgs& a, const BwdConfig& c,
     return dt == DT_F32 ? launch_bwd<SF_SOFTMAX, DT_F32>(a, c, st)
                         : launch_bwd<SF_SOFTMAX, DT_BF16>(a, c, st);
   }
+  if (sf == SF_SOFTMAX_POST) {
+    return dt == DT_F32 ? launch_bwd<SF_SOFTMAX_POST, DT_F32>(a, c, st)
+                        : launch_bwd<SF_SOFTMAX_POST, DT_BF16>(a, c, st);
+  }
   return dt == DT_F32 ? launch_bwd<SF_SIGMOID, DT_F32>(a, c, st)
                       : launch_bwd<SF_SIGMOID, DT_BF16>(a, c, st);
 }

@@ -10,6 +10,8 @@
 // OP 0, top-K (g = grad_probs, m = routing_map, s = saved scores):
 //   softmax: D = c sum m g s;             gx = s (c m g - D)
 //   sigmoid: S = sum m s, D = sum m g s;  gx = m (c / S)(g - D / S) s (1 - s)
+//   post-softmax (p = c m s / S, s the full softmax):
+//            S = sum m s, D = sum m g s;  gx = m (c / S)(g - D / S) s
 // OP 1, aux scores (g = grad_scores):
 //   softmax (saved q):     A = sum g q;             gx = q (g - A)
 //   sigmoid (saved sig):   Z = sum sig, B = sum g sig;
@@ -134,8 +136,10 @@ router_bwd_kernel(const BwdArgs a) {
       const float s = v[j][u];
       if constexpr (OP == 0 && SF == SF_SOFTMAX) {
         gx[u] = s * ((m[j][u] ? c * g[j][u] : 0.0f) - k0);
-      } else if constexpr (OP == 0) {
+      } else if constexpr (OP == 0 && SF == SF_SIGMOID) {
         gx[u] = m[j][u] ? k0 * (g[j][u] - k1) * (s * (1.0f - s)) : 0.0f;
+      } else if constexpr (OP == 0) {  // post-softmax
+        gx[u] = m[j][u] ? k0 * (g[j][u] - k1) * s : 0.0f;
       } else if constexpr (SF == SF_SOFTMAX) {
         gx[u] = s * (g[j][u] - k0);
       } else {

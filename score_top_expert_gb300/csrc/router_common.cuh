@@ -9,7 +9,9 @@
 
 namespace moe_router {
 
-enum { SF_SOFTMAX = 0, SF_SIGMOID = 1 };
+// SF_SOFTMAX_POST scores like softmax (over all E) and renormalises the
+// selected probabilities like sigmoid (the softmax of the selected logits).
+enum { SF_SOFTMAX = 0, SF_SIGMOID = 1, SF_SOFTMAX_POST = 2 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
 // ---------------------------------------------------------------------------

@@ -223,7 +223,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
       if (elem_ok(j, u)) hmax[half_of<NC>(j, u)] = fmaxf(hmax[half_of<NC>(j, u)], v[j][u]);
 
   float row_max = 0.0f, inv_sum = 1.0f;
-  if constexpr (SF == SF_SOFTMAX) {
+  if constexpr (SF != SF_SIGMOID) {
     row_max = seg_max<SEG>(fmaxf(hmax[0], hmax[1])) * kLog2e;
     float sum = 0.0f;
 #pragma unroll
@@ -263,7 +263,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
       if (has_bias && chunk_ok(j)) load4_f32<VEC>(a.bias, 0, 4 * (li + SEG * j), E, b);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if constexpr (SF == SF_SOFTMAX) v[j][u] *= inv_sum;
+        if constexpr (SF != SF_SIGMOID) v[j][u] *= inv_sum;
         else v[j][u] = sigmoid_f32(v[j][u]);
         kk[j][u] = elem_ok(j, u) ? ordered_key(v[j][u] + b[u]) : 0u;
       }
@@ -302,7 +302,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
   };
   auto score_at = [&](int j, int u) -> float {  // the score s of the element
     if constexpr (KM == 1) return v[j][u];
-    else if constexpr (SF == SF_SOFTMAX) return exp_shifted(v[j][u], row_max) * inv_sum;
+    else if constexpr (SF != SF_SIGMOID) return exp_shifted(v[j][u], row_max) * inv_sum;
     else return sigmoid_f32(v[j][u]);
   };
 
@@ -326,7 +326,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
 
   unsigned long long thr = 0ull;  // the K-th largest packed word of the row
   float sel_sum = 0.0f;           // sum of s over the selected (sigmoid top-K)
-  constexpr bool kNeedSelSum = (OP == 0 && SF == SF_SIGMOID);
+  constexpr bool kNeedSelSum = (OP == 0 && SF != SF_SOFTMAX);  // renormalised probs
   if (total <= CAP) {
     int pos = seg_exclusive_scan<SEG>(my_cnt);
 #pragma unroll

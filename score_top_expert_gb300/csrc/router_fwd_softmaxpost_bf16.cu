@@ -1,0 +1,8 @@
+// Instantiations of the router forwards: post-softmax score, bf16 logits.
+#include "router_launch.cuh"
+
+namespace moe_router {
+cudaError_t launch_fwd_softmaxpost_bf16(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  return launch_fwd<SF_SOFTMAX_POST, DT_BF16>(a, c, st);
+}
+}  // namespace moe_router

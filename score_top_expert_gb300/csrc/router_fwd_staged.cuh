@@ -225,9 +225,9 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   constexpr int CAP = kCandPerLane * SEG;
   constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
   constexpr int D = DT == DT_F32 ? 4 : 2;
-  constexpr bool kSigTopk = (OP == 0 && SF == SF_SIGMOID);
+  constexpr bool kSigTopk = (OP == 0 && SF != SF_SOFTMAX);  // probs renormalised over the K
   constexpr bool kStore = (DT == DT_F32 && KM == 0);  // scores kept over the fp32 logits
-  constexpr bool kNeedSum = (SF == SF_SOFTMAX || OP == 1) && KM == 0;
+  constexpr bool kNeedSum = (SF != SF_SIGMOID || OP == 1) && KM == 0;
   constexpr int KDT = KM == 0 ? DT : DT_F32;  // type of the selection keys
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
@@ -338,7 +338,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           for (int u = 0; u < 4; ++u) x[u] = okc ? x[u] : -INFINITY;
         }
       };
-      if constexpr (SF == SF_SOFTMAX) {
+      if constexpr (SF != SF_SIGMOID) {
         float mx = -INFINITY;
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
@@ -374,7 +374,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float sc = (SF == SF_SOFTMAX) ? exp_shifted(x[u], xmax_l2e) * xinv : sigmoid_f32(x[u]);
+          const float sc = (SF != SF_SIGMOID) ? exp_shifted(x[u], xmax_l2e) * xinv : sigmoid_f32(x[u]);
           k[u] = (FULL || c < nchunks) ? sc + bb[u] : -INFINITY;
         }
         sts_f4(work + 4 * c, make_float4(k[0], k[1], k[2], k[3]));
@@ -588,10 +588,13 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         }
       }
     }
-    // the score s of a selected candidate (sigmoid top-K sums them)
+    // the unnormalised score of a selected candidate (renormalising top-K
+    // sums them): sigmoid s, or e = exp(x - max) for the post-softmax
+    const float sel_max_l2e = KM == 1 ? xmax_l2e : row_max * kLog2e;
     auto score_of = [&](int idx, uint32_t key) -> float {
-      if constexpr (KM == 1) return sigmoid_f32(stage_x1<DT>(stage, idx));
-      else return sigmoid_f32(key_to_float(key));
+      const float x = KM == 1 ? stage_x1<DT>(stage, idx) : key_to_float(key);
+      if constexpr (SF == SF_SIGMOID) return sigmoid_f32(x);
+      else return exp_shifted(x, sel_max_l2e);
     };
     if (cand_ok) {
       compact_marked<KDT, SEG, NC>(KM == 1 ? reinterpret_cast<const unsigned char*>(work) : stage,
@@ -667,7 +670,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         load_x(stage, j, x);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          if constexpr (SF == SF_SOFTMAX) s[u] = exp_shifted(x[u], max_l2e);
+          if constexpr (SF != SF_SIGMOID) s[u] = exp_shifted(x[u], max_l2e);
           else s[u] = sigmoid_f32(x[u]);
         }
         if constexpr (kNeedSum) {
@@ -698,7 +701,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           stage_x<DT>(stage, c, x);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            if constexpr (SF == SF_SOFTMAX) w[u] = exp_shifted(x[u], max_l2e);
+            if constexpr (SF != SF_SIGMOID) w[u] = exp_shifted(x[u], max_l2e);
             else w[u] = sigmoid_f32(x[u]);
           }
         }
@@ -707,7 +710,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         __stcs(reinterpret_cast<unsigned int*>(a.map + off + 4 * c), mapw);
         float s[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) s[u] = (SF == SF_SOFTMAX) ? w[u] * inv : w[u];
+        for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? w[u] * inv : w[u];
         if constexpr (OP == 0) {
           float p[4];
 #pragma unroll

@@ -52,7 +52,9 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
 
 template <int SF, int DT, int SEG, int NC, bool VEC>
 cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
+  if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
+    if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
+  }
   if (c.km == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 0>(a, c, st);
   return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 0>(a, c, st);
 }
@@ -82,12 +84,17 @@ template <int SF, int DT>
 cudaError_t launch_bwd(const BwdArgs& a, const BwdConfig& c, cudaStream_t st) {
 #define MR_BWD_CASE(S, W, N)                                                     \
   if (c.seg == S && c.w == W && c.nc == N) {                                     \
-    if (c.vec) {                                                                 \
-      return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, true, 0>(a, st)        \
-                       : launch_bwd_inst<SF, DT, S, W, N, true, 1>(a, st);       \
+    if constexpr (SF == SF_SOFTMAX_POST) {                                       \
+      return c.vec ? launch_bwd_inst<SF, DT, S, W, N, true, 0>(a, st)            \
+                   : launch_bwd_inst<SF, DT, S, W, N, false, 0>(a, st);          \
+    } else {                                                                     \
+      if (c.vec) {                                                               \
+        return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, true, 0>(a, st)      \
+                         : launch_bwd_inst<SF, DT, S, W, N, true, 1>(a, st);     \
+      }                                                                          \
+      return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, false, 0>(a, st)       \
+                       : launch_bwd_inst<SF, DT, S, W, N, false, 1>(a, st);      \
     }                                                                            \
-    return c.op == 0 ? launch_bwd_inst<SF, DT, S, W, N, false, 0>(a, st)         \
-                     : launch_bwd_inst<SF, DT, S, W, N, false, 1>(a, st);        \
   }
   MR_BWD_CONFIGS(MR_BWD_CASE)
 #undef MR_BWD_CASE
@@ -156,9 +163,11 @@ template <int SF, int DT>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
 #define MR_STAGED_CASE(S, N)                                                               \
   if (p.seg == S && p.nc == N) {                                                           \
-    if (p.op == 1)                                                                         \
-      return p.full ? launch_staged_inst<SF, DT, S, N, 1, true, 0>(a, p, status, st)       \
-                    : launch_staged_inst<SF, DT, S, N, 1, false, 0>(a, p, status, st);     \
+    if constexpr (SF != SF_SOFTMAX_POST) {                                                 \
+      if (p.op == 1)                                                                       \
+        return p.full ? launch_staged_inst<SF, DT, S, N, 1, true, 0>(a, p, status, st)     \
+                      : launch_staged_inst<SF, DT, S, N, 1, false, 0>(a, p, status, st);   \
+    }                                                                                      \
     if (p.km == 1)                                                                         \
       return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 1>(a, p, status, st)       \
                     : launch_staged_inst<SF, DT, S, N, 0, false, 1>(a, p, status, st);     \
@@ -177,9 +186,11 @@ int staged_occupancy(const StagedPlan& p) {
 #define MR_STAGED_OCC(S, N)                                                                \
   if (p.seg == S && p.nc == N) {                                                           \
     const int w = p.warps_per_block;                                                       \
-    if (p.op == 1)                                                                         \
-      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 1, true, 0>(w, smem)              \
-                    : staged_blocks_per_sm<SF, DT, S, N, 1, false, 0>(w, smem);            \
+    if constexpr (SF != SF_SOFTMAX_POST) {                                                 \
+      if (p.op == 1)                                                                       \
+        return p.full ? staged_blocks_per_sm<SF, DT, S, N, 1, true, 0>(w, smem)            \
+                      : staged_blocks_per_sm<SF, DT, S, N, 1, false, 0>(w, smem);          \
+    }                                                                                      \
     if (p.km == 1)                                                                         \
       return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 1>(w, smem)              \
                     : staged_blocks_per_sm<SF, DT, S, N, 0, false, 1>(w, smem);            \
@@ -202,6 +213,12 @@ int occupancy_staged_sigmoid_f32(const StagedPlan&);
 int occupancy_staged_sigmoid_bf16(const StagedPlan&);
 
 cudaError_t launch_fwd_softmax_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_softmaxpost_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_softmaxpost_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_staged_softmaxpost_f32(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+cudaError_t launch_staged_softmaxpost_bf16(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);
+int occupancy_staged_softmaxpost_f32(const StagedPlan&);
+int occupancy_staged_softmaxpost_bf16(const StagedPlan&);
 cudaError_t launch_fwd_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_fwd_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_fwd_sigmoid_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);

@@ -1,0 +1,12 @@
+// Instantiations of the staged router forward: post-softmax score, f32 logits.
+#include "router_launch.cuh"
+
+namespace moe_router {
+cudaError_t launch_staged_softmaxpost_f32(const FwdArgs& a, const StagedPlan& p, int* status,
+                                          cudaStream_t st) {
+  return launch_staged<SF_SOFTMAX_POST, DT_F32>(a, p, status, st);
+}
+int occupancy_staged_softmaxpost_f32(const StagedPlan& p) {
+  return staged_occupancy<SF_SOFTMAX_POST, DT_F32>(p);
+}
+}  // namespace moe_router

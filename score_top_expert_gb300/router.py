@@ -15,12 +15,12 @@ import torch
 
 from . import build as _build
 
-MR_SOFTMAX, MR_SIGMOID = 0, 1
+MR_SOFTMAX, MR_SIGMOID, MR_SOFTMAX_POST = 0, 1, 2
 MR_F32, MR_BF16 = 0, 1
 MR_PATH_AUTO, MR_PATH_SEGMENT, MR_PATH_STAGED = 0, 1, 2
 STATUS = {0: "MR_OK", -1: "MR_ERR_INVALID", -2: "MR_ERR_UNSUPPORTED", -3: "MR_ERR_CUDA"}
 
-_SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID}
+_SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID, "softmax_post": MR_SOFTMAX_POST}
 _DTYPE = {torch.float32: MR_F32, torch.bfloat16: MR_BF16}
 
 _lib = None

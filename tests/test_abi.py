@@ -70,7 +70,7 @@ def fwd(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(T=-1), -1), (dict(E=0), -1), (dict(K=0), -1), (dict(K=17), -1),
-    (dict(dtype=2), -1), (dict(sf=2), -1), (dict(T=1 << 20, E=4096, K=4), -1),
+    (dict(dtype=2), -1), (dict(sf=3), -1), (dict(T=1 << 20, E=4096, K=4), -1),
     (dict(logits=None), -1), (dict(probs=None), -1), (dict(rmap=None), -1),
     (dict(scores=None), -1), (dict(ng=-1), -1),
     (dict(ng=3, gk=1), -1),                   # E % num_groups != 0
@@ -106,6 +106,9 @@ def test_other_calls_reject(L):
     assert L.router_aux_scores_bwd(None, f, 0, 4, 16, 2, 0, f, None) == -1
     assert L.router_aux_scores_bwd(f, f, 1, 4, 16, 0, 0, f, None) == -1
     assert L.router_aux_scores_bwd(None, None, 1, 0, 16, 2, 1, f, None) == 0
+    # the aux scores take softmax or sigmoid only (not the post-softmax)
+    assert L.router_aux_scores_fwd(f, 0, 4, 16, 2, 2, f, f, f, None) == -1
+    assert L.router_aux_scores_bwd(f, f, 0, 4, 16, 2, 2, f, None) == -1
 
 
 def test_path_knobs(L):

@@ -111,7 +111,8 @@ def run_and_check_aux(R, case, K, sf, ref_key=None):
 # the benchmark workloads, full size
 # ---------------------------------------------------------------------------
 TOPK_CASES = [
-    ("t1024_e64_k4", "softmax", "f32"),
+    ("t1024_e64_k4", "softmax", "f32"), ("t8192_e256_k8", "softmax_post", "bf16"),
+    ("t8192_e512_k22", "softmax_post", "f32"), ("t8192_e2304_k36", "softmax_post", "f32"),
     ("t8192_e256_k4", "softmax", "f32"), ("t8192_e256_k4", "sigmoid", "f32"),
     ("t8192_e256_k8", "softmax", "f32"), ("t8192_e256_k8", "sigmoid", "f32"),
     ("t8192_e256_k4", "softmax", "bf16"), ("t8192_e256_k8", "sigmoid", "bf16"),
@@ -149,9 +150,9 @@ def test_staged_shapes(R, E, dt):
     try:
         for K in sorted({1, min(E, 4), min(E, 22), min(E, 36)}):
             case = make_case(129, E, K, dtype=dt, sigma=1.5, seed=E + K)
-            for sf in ("softmax", "sigmoid"):
+            for sf in ("softmax", "sigmoid", "softmax_post"):
                 run_and_check_topk(R, case, K, sf, c=2.5)
-                if dt == "f32":
+                if dt == "f32" and sf != "softmax_post":
                     run_and_check_aux(R, case, K, sf)
     finally:
         R.force_path(prev)
@@ -187,11 +188,12 @@ def test_decode_sweep(R, T, dt):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("E", [1, 2, 3, 5, 7, 13, 64, 100, 129, 255, 513, 1000, 2303, 2304])
 def test_odd_and_ragged_shapes(R, E):
-    for sf in ("softmax", "sigmoid"):
+    for sf in ("softmax", "sigmoid", "softmax_post"):
         for K in sorted({1, min(E, 3), min(E, 36), min(E, 17)}):
             case = make_case(37, E, K, sigma=1.5, seed=E * 31 + K)
             run_and_check_topk(R, case, K, sf, c=1.7)
-            run_and_check_aux(R, case, K, sf)
+            if sf != "softmax_post":
+                run_and_check_aux(R, case, K, sf)
 
 
 @pytest.mark.parametrize("E", [4, 16, 36])
@@ -220,7 +222,7 @@ def test_every_lane_width(R, lanes):
         for E, K in ((64, 4), (128, 16), (256, 8), (512, 22), (1000, 30), (2304, 36)):
             for dt in ("f32", "bf16"):
                 case = make_case(300, E, K, dtype=dt, seed=E + lanes)
-                for sf in ("softmax", "sigmoid"):
+                for sf in ("softmax", "sigmoid", "softmax_post"):
                     run_and_check_topk(R, case, K, sf, c=2.5)
                     run_and_check_topk(R, case, K, sf, c=2.5,
                                        bias=np.linspace(-0.05, 0.05, E).astype(np.float32))
@@ -260,16 +262,16 @@ def test_tied_logits(R, path, E):
         for dt in ("f32", "bf16"):
             case = make_case(x.shape[0], E, K, dtype=dt, seed=1)
             case.logits = x if dt == "f32" else round_to_bf16_values(x)
-            for sf in ("softmax", "sigmoid"):
+            for sf in ("softmax", "sigmoid", "softmax_post"):
                 run_and_check_topk(R, case, K, sf)
-                if dt == "f32":
+                if dt == "f32" and sf != "softmax_post":
                     run_and_check_aux(R, case, K, sf)
 
 
 # ---------------------------------------------------------------------------
 # bias and groups
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("sf", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("sf", ["softmax", "sigmoid", "softmax_post"])
 def test_bias(R, path, sf):
     for E, K in ((64, 4), (256, 8), (512, 22), (2304, 36)):
         case = make_case(513, E, K, seed=E, with_bias=True, bias_range=0.1)
@@ -289,7 +291,7 @@ GROUPED = [  # (E, num_groups, group_topk, K)
 def test_grouped(R, path, E, G, gk, K):
     for dt in ("f32", "bf16"):
         case = make_case(300, E, K, dtype=dt, seed=E + G, with_bias=True)
-        for sf in ("sigmoid", "softmax"):
+        for sf in ("sigmoid", "softmax", "softmax_post"):
             run_and_check_topk(R, case, K, sf, 2.5, G, gk, case.expert_bias)
             run_and_check_topk(R, case, K, sf, 1.0, G, gk, None)
 
@@ -383,9 +385,9 @@ def test_adversarial_rows(R, path, E, K):
         from score_top_expert_gb300.workloads import round_to_bf16_values
         case = make_case(x.shape[0], E, K, dtype=dt, seed=3)
         case.logits = x if dt == "f32" else round_to_bf16_values(x)
-        for sf in ("softmax", "sigmoid"):
+        for sf in ("softmax", "sigmoid", "softmax_post"):
             run_and_check_topk(R, case, K, sf, c=2.0)
-            if dt == "f32":
+            if dt == "f32" and sf != "softmax_post":
                 run_and_check_aux(R, case, K, sf)
 
 

@@ -193,8 +193,32 @@ def check_grouping_identities():
     assert np.array_equal(np.nonzero(m)[0], [2, 3, 4, 5])
 
 
+def check_softmax_post():
+    """Post-softmax probs equal c times the softmax of the selected logits
+    alone (computed here directly from its definition), select like softmax,
+    sum to c, and equal the pre-softmax probs when K = E."""
+    rng = np.random.default_rng(11)
+    for E, K in ((8, 3), (64, 8), (512, 22), (300, 36)):
+        x = rng.normal(0, 1.5, E)
+        p, m, s, _ = O.topk_fwd_row(x, K, "softmax_post", scaling_factor=2.5)
+        _, m_pre, s_pre, _ = O.topk_fwd_row(x, K, "softmax", scaling_factor=2.5)
+        assert np.array_equal(m, m_pre) and np.allclose(s, s_pre, rtol=0, atol=0)
+        sel = np.nonzero(m)[0]
+        xs = x[sel]
+        want = 2.5 * np.exp(xs - xs.max()) / np.exp(xs - xs.max()).sum()
+        assert np.allclose(p[sel], want, rtol=1e-13, atol=0)
+        assert abs(p.sum() - 2.5) < 1e-12 and np.all(p[~m] == 0)
+    x = rng.normal(0, 1, 20)
+    assert np.allclose(O.topk_fwd_row(x, 20, "softmax_post")[0],
+                       O.topk_fwd_row(x, 20, "softmax")[0], rtol=1e-14, atol=0)
+
+
 def test_probs_closed_forms():
     check_probs_closed_forms()
+
+
+def test_softmax_post():
+    check_softmax_post()
 
 
 def test_grouping_identities():
@@ -217,7 +241,7 @@ def check_topk_bwd_finite_differences():
     rng = np.random.default_rng(7)
     h = 1e-4
     checked = 0
-    for sf in ("softmax", "sigmoid"):
+    for sf in ("softmax", "sigmoid", "softmax_post"):
         for E, K, c, ng, gk, use_b in ((12, 1, 1.0, 0, 0, False), (12, 3, 2.5, 0, 0, True),
                                        (32, 5, 1.0, 0, 0, False), (32, 8, 2.5, 4, 2, True),
                                        (40, 40, 1.0, 0, 0, False)):
@@ -242,8 +266,10 @@ def check_topk_bwd_finite_differences():
                 assert np.max(np.abs(fd - an)) < 1e-6
                 if sf == "softmax":
                     assert abs(an.sum()) < 1e-12   # constants are in the kernel
-                if sf == "sigmoid" and K == 1:
+                if sf in ("sigmoid", "softmax_post") and K == 1:
                     assert np.all(an == 0)
+                if sf == "softmax_post":
+                    assert abs(an.sum()) < 1e-12   # invariant under a shift of x
                 checked += 1
     assert checked >= 20
 
@@ -381,6 +407,12 @@ def _wrong_bf16(x):
         .__and__(np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)  # truncation
 
 
+def _wrong_post_bwd(g, m, s, sf, c=1.0):
+    if sf == "softmax_post":
+        return _orig_topk_bwd_row(g, m, s, "sigmoid", c)   # sigmoid's extra (1 - s)
+    return _orig_topk_bwd_row(g, m, s, sf, c)
+
+
 PLANTED = [
     ("order_desc", _wrong_order, [check_topk_brute_force]),
     ("score_row", _wrong_softmax_score, [check_softmax_closed_form]),
@@ -389,6 +421,7 @@ PLANTED = [
     ("group_scores", _wrong_group_scores_max, [check_grouped_brute_force]),
     ("topk_bwd_row", _wrong_bwd_no_d, [check_topk_bwd_finite_differences]),
     ("topk_bwd_row", _wrong_bwd_sigmoid_scale, [check_topk_bwd_finite_differences]),
+    ("topk_bwd_row", _wrong_post_bwd, [check_topk_bwd_finite_differences]),
     ("topk_fwd_row", _wrong_no_renorm, [check_probs_closed_forms]),
     ("aux_scores_bwd_row", _wrong_aux_bwd, [check_aux_closed_forms_and_fd]),
     ("round_to_bf16", _wrong_bf16, [check_bf16_rounding]),
