@@ -37,6 +37,7 @@
 #ifndef MOE_ROUTER_H
 #define MOE_ROUTER_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -193,6 +194,51 @@ MR_API int router_aux_scores_bwd(const float* grad_scores, const float* saved,
                           mr_dtype dtype, int T, int E, int K,
                           mr_score_func score_func, void* grad_logits,
                           mr_stream_t stream);
+
+/*
+ * router_aux_loss_fwd — the load-balancing aux loss over the aux-score
+ * forward's outputs, with the tokens routed to each expert.
+ *
+ * Source: TransformerEngine PR #3012, Important Files Changed
+ * (fused_moe_aux_loss: the page names the op; its formula is not printed).
+ * The loss taken here is the standard load-balancing loss
+ *   loss = coeff * E * sum_e f_e * P_e,  f_e = tokens_e / (T K),
+ *   P_e = (1/T) sum_t q_te,  tokens_e = sum_t map_te,
+ * i.e. coeff * E / (K T^2) * sum_e (sum_t q_te) * tokens_e.
+ *
+ * aux_scores         [T,E] float q (router_aux_scores_fwd's scores), input
+ * routing_map        [T,E] uint8, nonzero = routed, input
+ * loss               [1] float, output (device memory)
+ * tokens_per_expert  [E] int32, output
+ * workspace          device scratch of at least
+ *                    router_aux_loss_workspace_bytes(T, E) bytes, 16-byte
+ *                    aligned, owned by the caller; its contents need no
+ *                    initialisation and are overwritten
+ *
+ * Two kernels on `stream`; the reduction order is fixed (no atomics), so
+ * repeated calls give identical bits.  T == 0 is a no-op (nothing written).
+ * MR_ERR_INVALID: T < 0, E < 1, K outside [1, E], T*E > INT_MAX, a NULL
+ * pointer when T > 0, a workspace too small or misaligned.
+ * MR_ERR_UNSUPPORTED: E > MR_MAX_EXPERTS.
+ */
+MR_API size_t router_aux_loss_workspace_bytes(int T, int E);
+MR_API int router_aux_loss_fwd(const float* aux_scores, const uint8_t* routing_map, int T, int E,
+                               int K, float coeff, float* loss, int32_t* tokens_per_expert,
+                               void* workspace, size_t workspace_bytes, mr_stream_t stream);
+
+/*
+ * router_aux_loss_bwd — gradient of the aux loss with respect to the aux
+ * scores: grad_aux_scores[t, e] = grad_loss * coeff E / (K T^2) * tokens_e
+ * (the loss is linear in q; the token counts carry no gradient).
+ *
+ * grad_loss          [1] float, device memory, input
+ * tokens_per_expert  [E] int32 from router_aux_loss_fwd, input
+ * grad_aux_scores    [T,E] float, output
+ * Errors: as router_aux_loss_fwd (no workspace).
+ */
+MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert, int T,
+                               int E, int K, float coeff, float* grad_aux_scores,
+                               mr_stream_t stream);
 
 /* Static English text for a status code (never NULL). */
 MR_API const char* moe_router_strerror(int code);

@@ -287,6 +287,33 @@ def aux_scores_bwd(grad_scores, saved, score_func=SOFTMAX):
 
 
 # --------------------------------------------------------------------------
+# load-balancing aux loss  [TE] Important Files Changed (fused_moe_aux_loss);
+# the page names the op only.  Reading: the standard load-balancing loss,
+# coeff * E * sum_e f_e * P_e with f_e = tokens_e / (T K) the share of the T K
+# assignments routed to expert e and P_e = (1/T) sum_t q_te the mean aux score.
+# --------------------------------------------------------------------------
+def aux_loss_fwd(aux_scores, routing_map, K, coeff):
+    """Returns (loss, tokens_per_expert[E]) from the aux scores q [T,E] and
+    the routing map [T,E]: loss = coeff E / (K T^2) sum_e (sum_t q_te) tokens_e."""
+    q = np.asarray(aux_scores, dtype=np.float64)
+    m = np.asarray(routing_map).astype(bool)
+    T, E = q.shape
+    tokens = m.sum(axis=0).astype(np.int64)          # tokens routed to each expert
+    colsum = q.sum(axis=0)                            # T * P_e
+    loss = coeff * E / (K * T * T) * float(np.dot(colsum, tokens))
+    return loss, tokens
+
+
+def aux_loss_bwd(grad_loss, tokens_per_expert, T, K, coeff):
+    """grad_scores [T,E]: the loss is linear in q, d loss / d q_te =
+    coeff E / (K T^2) tokens_e; the counts carry no gradient."""
+    tokens = np.asarray(tokens_per_expert, dtype=np.float64)
+    E = tokens.size
+    row = float(grad_loss) * coeff * E / (K * T * T) * tokens
+    return np.tile(row, (T, 1))
+
+
+# --------------------------------------------------------------------------
 # output rounding
 # --------------------------------------------------------------------------
 def round_to_bf16(x) -> np.ndarray:

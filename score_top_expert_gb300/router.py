@@ -62,6 +62,12 @@ def lib() -> ctypes.CDLL:
         L.moe_router_version.argtypes = []
         L.moe_router_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         L.moe_router_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+        L.router_aux_loss_workspace_bytes.argtypes = [i, i]
+        L.router_aux_loss_workspace_bytes.restype = ctypes.c_size_t
+        L.router_aux_loss_fwd.argtypes = [vp, vp, i, i, i, f, vp, vp, vp, ctypes.c_size_t, vp]
+        L.router_aux_loss_fwd.restype = ctypes.c_int
+        L.router_aux_loss_bwd.argtypes = [vp, vp, i, i, i, f, vp, vp]
+        L.router_aux_loss_bwd.restype = ctypes.c_int
         L.moe_router_selftest_bounded_wait.restype = ctypes.c_int
         L.moe_router_strerror.argtypes = [i]
         L.moe_router_strerror.restype = ctypes.c_char_p
@@ -230,3 +236,47 @@ def selftest_bounded_wait(timeout_us: int, device=None) -> None:
     with torch.cuda.device(dev):
         _check("moe_router_selftest_bounded_wait",
                lib().moe_router_selftest_bounded_wait(int(timeout_us), _stream(dev)))
+
+
+def router_aux_loss_fwd(aux_scores: torch.Tensor, routing_map: torch.Tensor, K: int,
+                        coeff: float, *, loss=None, tokens_per_expert=None, workspace=None):
+    """Load-balancing aux loss.  Returns (loss [1] float32, tokens_per_expert
+    [E] int32).  The workspace (a uint8 CUDA tensor) is allocated here when
+    not given."""
+    aux_scores = _as_input(aux_scores, "aux_scores", (torch.float32,))
+    routing_map = _as_input(routing_map, "routing_map", (torch.bool, torch.uint8))
+    if routing_map.shape != aux_scores.shape:
+        raise ValueError("aux_scores and routing_map must have the same shape")
+    T, E = aux_scores.shape
+    dev = aux_scores.device
+    loss = _out(loss, (1,), torch.float32, dev, "loss")
+    tokens_per_expert = _out(tokens_per_expert, (E,), torch.int32, dev, "tokens_per_expert")
+    nbytes = lib().router_aux_loss_workspace_bytes(T, E)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().router_aux_loss_fwd(_ptr(aux_scores), _ptr(routing_map), T, E, int(K),
+                                       float(coeff), _ptr(loss), _ptr(tokens_per_expert),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(dev))
+    _check("router_aux_loss_fwd", rc)
+    return loss, tokens_per_expert
+
+
+def router_aux_loss_bwd(grad_loss: torch.Tensor, tokens_per_expert: torch.Tensor, T: int, K: int,
+                        coeff: float, *, grad_aux_scores=None):
+    """Gradient of the aux loss with respect to the aux scores, [T, E] float32."""
+    if not grad_loss.is_cuda or grad_loss.dtype != torch.float32 or grad_loss.numel() != 1:
+        raise ValueError("grad_loss must be a CUDA float32 tensor with one element")
+    if not tokens_per_expert.is_cuda or tokens_per_expert.dtype != torch.int32:
+        raise ValueError("tokens_per_expert must be a CUDA int32 tensor")
+    E = tokens_per_expert.numel()
+    dev = tokens_per_expert.device
+    grad_loss = grad_loss.contiguous()
+    tokens_per_expert = tokens_per_expert.contiguous()
+    grad_aux_scores = _out(grad_aux_scores, (T, E), torch.float32, dev, "grad_aux_scores")
+    with torch.cuda.device(dev):
+        rc = lib().router_aux_loss_bwd(_ptr(grad_loss), _ptr(tokens_per_expert), int(T), E, int(K),
+                                       float(coeff), _ptr(grad_aux_scores), _stream(dev))
+    _check("router_aux_loss_bwd", rc)
+    return grad_aux_scores

@@ -132,3 +132,23 @@ def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
 def test_selftest_rejects_out_of_range_timeouts(L):
     assert L.moe_router_selftest_bounded_wait(0, None) == -1
     assert L.moe_router_selftest_bounded_wait(1000001, None) == -1
+
+
+def test_aux_loss_argument_checks(L):
+    L.router_aux_loss_workspace_bytes.restype = ctypes.c_size_t
+    assert L.router_aux_loss_workspace_bytes(8192, 2304) == 256 * 2304 * 8
+    assert L.router_aux_loss_workspace_bytes(10, 64) == 10 * 64 * 8
+    assert L.router_aux_loss_workspace_bytes(0, 64) == 0
+    f, c = FAKE, ctypes.c_float(0.01)
+    big = ctypes.c_size_t(1 << 30)
+    fwd = L.router_aux_loss_fwd
+    assert fwd(f, f, 4, 16, 17, c, f, f, f, big, None) == -1          # K > E
+    assert fwd(f, f, -1, 16, 2, c, f, f, f, big, None) == -1
+    assert fwd(f, f, 4, 4000, 2, c, f, f, f, big, None) == -2
+    assert fwd(f, f, 4, 16, 2, c, None, f, f, big, None) == -1        # no loss output
+    assert fwd(f, f, 4, 16, 2, c, f, f, f, ctypes.c_size_t(16), None) == -1  # workspace too small
+    assert fwd(f, f, 4, 16, 2, c, f, f, ctypes.c_void_p(0x1001), big, None) == -1  # misaligned
+    assert fwd(None, None, 0, 16, 2, c, None, None, None, ctypes.c_size_t(0), None) == 0
+    bwd = L.router_aux_loss_bwd
+    assert bwd(f, None, 4, 16, 2, c, f, None) == -1
+    assert bwd(None, None, 0, 16, 2, c, None, None) == 0

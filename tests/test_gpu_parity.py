@@ -404,3 +404,49 @@ def test_bounded_wait_reports_a_timeout(R):
     assert R.device_status() == 0
     with pytest.raises(R.RouterError):
         R.selftest_bounded_wait(0)
+
+
+# ---------------------------------------------------------------------------
+# load-balancing aux loss
+# ---------------------------------------------------------------------------
+AUX_LOSS_REL = 1e-5  # fp32 column partials over <= 32 rows, summed in double
+
+
+@pytest.mark.parametrize("T,E,K", [(8192, 512, 22), (8192, 2304, 36), (1000, 257, 5), (77, 64, 4),
+                                   (300, 2304, 36), (1, 8, 1)])
+def test_aux_loss(R, T, E, K):
+    case = make_case(T, E, K, seed=T + E)
+    for sf in ("softmax", "sigmoid"):
+        q, amap, inter = R.router_aux_scores_fwd(to_dev(case.logits), K, sf)
+        loss, tokens = R.router_aux_loss_fwd(q, amap, K, 0.01)
+        loss2, tokens2 = R.router_aux_loss_fwd(q, amap, K, 0.01)
+        torch.cuda.synchronize()
+        # identical bits on a repeat (fixed reduction order)
+        assert loss.item() == loss2.item() and torch.equal(tokens, tokens2)
+        # the same inputs through the oracle
+        qn, mn = np64(q), amap.cpu().numpy()
+        ref, ref_tok = O.aux_loss_fwd(qn, mn, K, 0.01)
+        assert np.array_equal(tokens.cpu().numpy(), ref_tok)
+        assert abs(loss.item() - ref) <= AUX_LOSS_REL * abs(ref) + 1e-12, (loss.item(), ref)
+        # the whole pipeline against the oracle's own scores and map
+        o = O.aux_scores_fwd(case.logits, K, sf)
+        ref_full, _ = O.aux_loss_fwd(o["scores"], o["routing_map"], K, 0.01)
+        assert abs(loss.item() - ref_full) <= AUX_LOSS_REL * abs(ref_full) + 1e-12
+        # backward
+        gl = torch.tensor([1.7], device=DEV)
+        g = R.router_aux_loss_bwd(gl, tokens, T, K, 0.01)
+        gref = O.aux_loss_bwd(1.7, ref_tok, T, K, 0.01)
+        assert np.max(np.abs(np64(g) - gref) - 1e-6 * np.abs(gref)) <= 0.0
+
+
+def test_aux_loss_unaligned_backward(R):
+    T, E, K = 33, 100, 3
+    case = make_case(T, E, K, seed=5)
+    q, amap, _ = R.router_aux_scores_fwd(to_dev(case.logits), K, "softmax")
+    loss, tokens = R.router_aux_loss_fwd(q, amap, K, 0.5)
+    buf = torch.zeros(T * E + 1, device=DEV)
+    g = R.router_aux_loss_bwd(torch.tensor([2.0], device=DEV), tokens, T, K, 0.5,
+                              grad_aux_scores=buf[1:].view(T, E))
+    gref = O.aux_loss_bwd(2.0, tokens.cpu().numpy(), T, K, 0.5)
+    assert np.max(np.abs(np64(g) - gref) - 1e-6 * np.abs(gref)) <= 0.0
+    assert buf[0].item() == 0.0

@@ -213,6 +213,50 @@ def check_softmax_post():
                        O.topk_fwd_row(x, 20, "softmax")[0], rtol=1e-14, atol=0)
 
 
+def check_aux_loss():
+    """Perfectly balanced routing with uniform scores gives exactly coeff (the
+    loss's minimum for balanced assignments); a hand-worked 2 x 2 case; the
+    gradient matches central differences; routing every token to one expert
+    with all its score there gives coeff * E."""
+    T, E, K = 8, 4, 2
+    q = np.full((T, E), 1.0 / E)
+    m = np.zeros((T, E), bool)
+    for t in range(T):                       # each expert gets T K / E tokens
+        m[t, [t % E, (t + 1) % E]] = True
+    loss, tok = O.aux_loss_fwd(q, m, K, 0.01)
+    assert np.array_equal(tok, [4, 4, 4, 4]) and abs(loss - 0.01) < 1e-15
+    # 2 tokens x 2 experts, K = 1: tokens = (2, 0), sum_t q = (1.3, 0.7):
+    # loss = c * 2 / (1 * 4) * (1.3 * 2 + 0.7 * 0) = c * 1.3
+    q = np.array([[0.6, 0.4], [0.7, 0.3]])
+    m = np.array([[1, 0], [1, 0]], bool)
+    loss, tok = O.aux_loss_fwd(q, m, 1, 2.0)
+    assert np.array_equal(tok, [2, 0]) and abs(loss - 2.6) < 1e-15
+    # all tokens on expert 0 with q concentrated there: coeff * E
+    q = np.zeros((5, 6)); q[:, 0] = 1.0
+    m = np.zeros((5, 6), bool); m[:, 0] = True
+    assert abs(O.aux_loss_fwd(q, m, 1, 0.5)[0] - 0.5 * 6) < 1e-14
+    # gradient
+    rng = np.random.default_rng(12)
+    T, E, K = 6, 5, 2
+    q = rng.random((T, E))
+    m = np.zeros((T, E), bool)
+    for t in range(T):
+        m[t, rng.choice(E, K, replace=False)] = True
+    _, tok = O.aux_loss_fwd(q, m, K, 0.3)
+    g = O.aux_loss_bwd(1.7, tok, T, K, 0.3)
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            qp = q.copy(); qp[t, e] += h
+            qm = q.copy(); qm[t, e] -= h
+            fd = 1.7 * (O.aux_loss_fwd(qp, m, K, 0.3)[0] - O.aux_loss_fwd(qm, m, K, 0.3)[0]) / (2 * h)
+            assert abs(fd - g[t, e]) < 1e-8
+
+
+def test_aux_loss():
+    check_aux_loss()
+
+
 def test_probs_closed_forms():
     check_probs_closed_forms()
 
@@ -413,6 +457,14 @@ def _wrong_post_bwd(g, m, s, sf, c=1.0):
     return _orig_topk_bwd_row(g, m, s, sf, c)
 
 
+_orig_aux_loss = O.aux_loss_fwd
+
+
+def _wrong_aux_loss(q, m, K, coeff):   # divides by T instead of T^2
+    loss, tok = _orig_aux_loss(q, m, K, coeff)
+    return loss * np.asarray(q).shape[0], tok
+
+
 PLANTED = [
     ("order_desc", _wrong_order, [check_topk_brute_force]),
     ("score_row", _wrong_softmax_score, [check_softmax_closed_form]),
@@ -425,6 +477,7 @@ PLANTED = [
     ("topk_fwd_row", _wrong_no_renorm, [check_probs_closed_forms]),
     ("aux_scores_bwd_row", _wrong_aux_bwd, [check_aux_closed_forms_and_fd]),
     ("round_to_bf16", _wrong_bf16, [check_bf16_rounding]),
+    ("aux_loss_fwd", _wrong_aux_loss, [check_aux_loss]),
 ]
 
 
