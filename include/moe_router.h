@@ -240,6 +240,43 @@ MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per
                                int E, int K, float coeff, float* grad_aux_scores,
                                mr_stream_t stream);
 
+/*
+ * router_aux_loss_fwd_noalloc — router_aux_loss_fwd without a workspace.
+ * The paper has no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at the point of the call.  Examples: a
+ * runtime whose memory plan reserves all device memory up front, so that a
+ * cudaMalloc fails or bypasses its accounting; a plain C caller with no
+ * allocator to hand a workspace from; code that must not pay the implicit
+ * device synchronisation of cudaFree after the call.
+ *
+ * The column partials go to a fixed device array inside this library of
+ * MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES (1,179,648 bytes: up to
+ * MR_AUX_LOSS_NOALLOC_BLOCKS partial rows for E up to MR_MAX_EXPERTS).  Every
+ * GPU that loads the library holds that array until the process exits.  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  The caller still owns and passes every input and output.
+ *
+ * Arguments, layouts, results and errors are those of router_aux_loss_fwd
+ * without workspace/workspace_bytes; E beyond what the array holds returns
+ * MR_ERR_UNSUPPORTED.  The loss and tokens equal router_aux_loss_fwd's up to
+ * the order of fp32 partial sums (fewer, longer partial rows); repeated
+ * calls on the same inputs give the same bits.
+ *
+ * Set-up: the first call on a device (that device current) looks up the
+ * array's device address, once per device; make that first call before any
+ * stream capture begins.  Sharing: every call on a device uses the same
+ * array, which keeps the last call's contents (nothing needs clearing: each
+ * call writes every partial it reads before reading it).  Calls whose work
+ * overlaps on the GPU — on two streams, or from two host threads — race on
+ * the array and give wrong results; order them on one stream or with
+ * events.
+ */
+#define MR_AUX_LOSS_NOALLOC_BLOCKS 64
+#define MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES ((size_t)MR_AUX_LOSS_NOALLOC_BLOCKS * MR_MAX_EXPERTS * 8u)
+MR_API int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T,
+                                       int E, int K, float coeff, float* loss,
+                                       int32_t* tokens_per_expert, mr_stream_t stream);
+
 /* Static English text for a status code (never NULL). */
 MR_API const char* moe_router_strerror(int code);
 

@@ -10,9 +10,11 @@
 //      loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e.
 // Backward: grad[t, e] = grad_loss * coeff E / (K T^2) * tokens_e, a pure
 // streaming write (blocks stride over rows, threads over 16-byte chunks).
+#include <atomic>
 #include <climits>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "moe_router.h"
 #include "router_common.cuh"
@@ -132,6 +134,51 @@ int sm_count() {
 }
 
 }  // namespace
+
+// Allocation-free forward: the column partials live in this file-scope
+// array instead of a caller workspace.  Its size is fixed: up to
+// kNoAllocBlocks partial rows of MR_MAX_EXPERTS floats plus as many ints.
+// Every GPU that loads the library holds it until the process exits.
+constexpr int kNoAllocBlocks = MR_AUX_LOSS_NOALLOC_BLOCKS;
+static_assert(MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES ==
+                  static_cast<size_t>(kNoAllocBlocks) * MR_MAX_EXPERTS * 8u,
+              "scratch size stated in the header");
+static __device__ __align__(256) unsigned char
+    g_aux_noalloc_scratch[MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::atomic<void*> g_noalloc_ptr[kNoAllocMaxDevices];
+std::mutex g_noalloc_setup;
+
+// Device address of the scratch array on the current device.  In host code
+// g_aux_noalloc_scratch names a host-side stand-in, so the address comes
+// from the runtime, once per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MR_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MR_ERR_UNSUPPORTED;
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_setup);
+    p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_aux_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return MR_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return MR_OK;
+}
+
+}  // namespace
 }  // namespace moe_router
 
 using namespace moe_router;
@@ -186,6 +233,36 @@ int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert
   else
     aux_loss_bwd_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         grad_loss, tokens_per_expert, T, E, scale, grad_aux_scores);
+  return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
+
+// Same two kernels as router_aux_loss_fwd, with at most kNoAllocBlocks
+// partial rows.  Every partial the second kernel reads is written by the
+// first kernel of the same call, so nothing in the scratch has to start at
+// zero and a previous call's contents are never read.
+int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T, int E,
+                                int K, float coeff, float* loss, int32_t* tokens_per_expert,
+                                mr_stream_t stream) {
+  const int rc = aux_check(T, E, K);
+  if (rc != MR_OK) return rc;
+  const int nb = T < kNoAllocBlocks ? T : kNoAllocBlocks;
+  if (static_cast<size_t>(nb) * static_cast<size_t>(E) * 8u > sizeof(g_aux_noalloc_scratch))
+    return MR_ERR_UNSUPPORTED;
+  if (T == 0) return MR_OK;
+  if (aux_scores == nullptr || routing_map == nullptr || loss == nullptr ||
+      tokens_per_expert == nullptr)
+    return MR_ERR_INVALID;
+  void* scratch = nullptr;
+  const int sc = noalloc_scratch(&scratch);
+  if (sc != MR_OK) return sc;
+  const int rows = (T + nb - 1) / nb;
+  float* part_q = static_cast<float*>(scratch);
+  int* part_n = reinterpret_cast<int*>(part_q + static_cast<size_t>(nb) * E);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  aux_loss_partial_kernel<<<nb, kAuxThreads, 0, st>>>(aux_scores, routing_map, T, E, rows, part_q,
+                                                      part_n);
+  aux_loss_final_kernel<<<1, kAuxThreads, 0, st>>>(part_q, part_n, nb, T, E, K, coeff, loss,
+                                                   tokens_per_expert);
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 

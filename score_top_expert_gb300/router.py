@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.router_aux_loss_workspace_bytes.restype = ctypes.c_size_t
         L.router_aux_loss_fwd.argtypes = [vp, vp, i, i, i, f, vp, vp, vp, ctypes.c_size_t, vp]
         L.router_aux_loss_fwd.restype = ctypes.c_int
+        L.router_aux_loss_fwd_noalloc.argtypes = [vp, vp, i, i, i, f, vp, vp, vp]
+        L.router_aux_loss_fwd_noalloc.restype = ctypes.c_int
         L.router_aux_loss_bwd.argtypes = [vp, vp, i, i, i, f, vp, vp]
         L.router_aux_loss_bwd.restype = ctypes.c_int
         L.moe_router_selftest_bounded_wait.restype = ctypes.c_int
@@ -260,6 +262,35 @@ def router_aux_loss_fwd(aux_scores: torch.Tensor, routing_map: torch.Tensor, K: 
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(dev))
     _check("router_aux_loss_fwd", rc)
+    return loss, tokens_per_expert
+
+
+def router_aux_loss_fwd_noalloc(aux_scores: torch.Tensor, routing_map: torch.Tensor, K: int,
+                                coeff: float, *, loss: torch.Tensor,
+                                tokens_per_expert: torch.Tensor):
+    """router_aux_loss_fwd for callers that cannot allocate device memory at
+    the call: the library keeps its scratch in a fixed device array, and the
+    caller passes the outputs (loss [1] float32, tokens_per_expert [E] int32)
+    already allocated.  Calls that overlap on the GPU race on that array; the
+    first call on a device looks up its address and belongs before any stream
+    capture."""
+    aux_scores = _as_input(aux_scores, "aux_scores", (torch.float32,))
+    routing_map = _as_input(routing_map, "routing_map", (torch.bool, torch.uint8))
+    if routing_map.shape != aux_scores.shape:
+        raise ValueError("aux_scores and routing_map must have the same shape")
+    T, E = aux_scores.shape
+    dev = aux_scores.device
+    if loss.device != dev or loss.dtype != torch.float32 or loss.numel() < 1:
+        raise ValueError("loss must be a float32 tensor on the inputs' device")
+    if (tokens_per_expert.device != dev or tokens_per_expert.dtype != torch.int32
+            or tokens_per_expert.numel() != E or not tokens_per_expert.is_contiguous()):
+        raise ValueError("tokens_per_expert must be a contiguous int32 [E] tensor on the "
+                         "inputs' device")
+    with torch.cuda.device(dev):
+        rc = lib().router_aux_loss_fwd_noalloc(_ptr(aux_scores), _ptr(routing_map), T, E, int(K),
+                                               float(coeff), _ptr(loss),
+                                               _ptr(tokens_per_expert), _stream(dev))
+    _check("router_aux_loss_fwd_noalloc", rc)
     return loss, tokens_per_expert
 
 

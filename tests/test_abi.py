@@ -152,3 +152,12 @@ def test_aux_loss_argument_checks(L):
     bwd = L.router_aux_loss_bwd
     assert bwd(f, None, 4, 16, 2, c, f, None) == -1
     assert bwd(None, None, 0, 16, 2, c, None, None) == 0
+
+
+def test_aux_loss_noalloc_argument_checks(L):
+    f, c = FAKE, ctypes.c_float(0.01)
+    fwd = L.router_aux_loss_fwd_noalloc
+    assert fwd(f, f, 4, 2305, 2, c, f, f, None) == -2    # beyond the scratch array
+    assert fwd(f, f, 4, 16, 17, c, f, f, None) == -1
+    assert fwd(f, f, 4, 16, 2, c, None, f, None) == -1
+    assert fwd(None, None, 0, 16, 2, c, None, None, None) == 0
