@@ -18,6 +18,14 @@ Sources (titles of the pages the method is read from):
   single-pass finalize, and PDL overlap for NVFP4 QMoE": Description item 1
   (softmax + top-k per row, one row per warp) and the review's parity request
   (tied logits).
+* [AITER] ROCm/aiter PR #5652, "[HIP] [Perf] Fold shared-expert gate GEMV
+  into topk_softmax kernel": the review's suggested benchmark (topk_softmax
+  writing [T, K] weights, indices and token_expert_indices, with row-strided
+  views for the weights and indices) and its note on the token_expert_indices
+  width ([T, K]).
+* [TRT] NVIDIA TensorRT-LLM PR #14592, "[TRTLLM-12214][perf] DeepGemmFusedMoE:
+  fuse masked gather + finalize-scale into one Triton kernel": the
+  reverse-permute map (expanded row t + k * num_rows).
 
 Readings where the pages are silent (each one is also listed in the design
 notes):
@@ -127,11 +135,12 @@ def _near(a: float, b: float) -> bool:
 # router top-K forward  [TE] Summary, Performance
 # --------------------------------------------------------------------------
 def topk_fwd_row(x, K, score_func, num_groups=0, group_topk=0,
-                 scaling_factor=1.0, expert_bias=None):
+                 scaling_factor=1.0, expert_bias=None, ranked=False):
     """One token row of the top-K router forward.
 
     Returns (probs, routing_map, scores, near_tie) with probs and scores in
-    float64 (not yet rounded to the output dtype).
+    float64 (not yet rounded to the output dtype); with ranked=True also the
+    K selected experts in rank order (key descending, index ascending).
     """
     x = np.asarray(x, dtype=np.float64)
     E = x.size
@@ -157,6 +166,8 @@ def topk_fwd_row(x, K, score_func, num_groups=0, group_topk=0,
     if gs is not None and group_topk < num_groups:
         go = order_desc(gs)
         near = near or _near(gs[go[group_topk - 1]], gs[go[group_topk]])
+    if ranked:
+        return probs, m, s, near, sel
     return probs, m, s, near
 
 
@@ -178,6 +189,36 @@ def topk_fwd(logits, K, score_func=SOFTMAX, num_groups=0, group_topk=0,
             logits[t], K, score_func, num_groups, group_topk, scaling_factor,
             expert_bias)
     return dict(probs=probs, routing_map=rmap, scores=scores, near_tie=near)
+
+
+# --------------------------------------------------------------------------
+# compact outputs  [AITER] review of the shared-expert topk_softmax fusion
+# (the [T, K] weights / indices / token_expert_indices buffers, row-strided
+# weights and indices); [TRT] reverse-permute map (the expanded row of token
+# t's k-th choice is t + k * num_rows).  Reading: position k of a row holds
+# the expert of rank k in the selection order (key descending, index
+# ascending), with its probability as the weight.
+# --------------------------------------------------------------------------
+def topk_fwd_compact(logits, K, score_func=SOFTMAX, num_groups=0, group_topk=0,
+                     scaling_factor=1.0, expert_bias=None):
+    """Returns a dict: topk_weights [T,K] f64 (probs of the selected experts,
+    not yet rounded), topk_indices [T,K] int64, token_expert_indices [T,K]
+    int64 (k * T + t), near_tie [T] bool."""
+    logits = np.asarray(logits, dtype=np.float64)
+    T, E = logits.shape
+    w = np.zeros((T, K))
+    idx = np.zeros((T, K), dtype=np.int64)
+    tei = np.zeros((T, K), dtype=np.int64)
+    near = np.zeros(T, dtype=bool)
+    for t in range(T):
+        probs, _, _, near[t], sel = topk_fwd_row(
+            logits[t], K, score_func, num_groups, group_topk, scaling_factor,
+            expert_bias, ranked=True)
+        for k in range(K):
+            idx[t, k] = sel[k]
+            w[t, k] = probs[sel[k]]
+            tei[t, k] = k * T + t
+    return dict(topk_weights=w, topk_indices=idx, token_expert_indices=tei, near_tie=near)
 
 
 # --------------------------------------------------------------------------

@@ -253,6 +253,47 @@ def check_aux_loss():
             assert abs(fd - g[t, e]) < 1e-8
 
 
+def check_compact():
+    """Compact outputs: a hand-worked row (ties to the lower index), an
+    all-equal row, a biased row whose rank order differs from the weight
+    order, the expanded-row index k T + t, and agreement with the dense map
+    on random grouped/biased rows (keys non-increasing along k, equal keys in
+    increasing index order)."""
+    x = np.array([[1.0, 3.0, 3.0, 0.0, 2.0], [0.0, 0.0, 0.0, 0.0, 0.0]])
+    o = O.topk_fwd_compact(x, 3, "softmax")
+    assert o["topk_indices"].tolist() == [[1, 2, 4], [0, 1, 2]]
+    z = np.exp(x[0] - 3.0).sum()
+    assert np.allclose(o["topk_weights"][0], np.exp(np.array([3.0, 3.0, 2.0]) - 3.0) / z,
+                       rtol=1e-15, atol=0)
+    assert np.allclose(o["topk_weights"][1], 0.2, rtol=1e-15, atol=0)
+    assert o["token_expert_indices"].tolist() == [[0, 2, 4], [1, 3, 5]]
+    # softmax scores (0.665, 0.245, 0.090), bias (0, 1, 0): keys put expert 1
+    # first although its weight is the smaller
+    o = O.topk_fwd_compact(np.array([[2.0, 1.0, 0.0]]), 2, "softmax",
+                           expert_bias=np.array([0.0, 1.0, 0.0]))
+    assert o["topk_indices"].tolist() == [[1, 0]]
+    assert o["topk_weights"][0, 0] < o["topk_weights"][0, 1]
+    rng = np.random.default_rng(13)
+    T, E, K = 7, 24, 6
+    for sf in ("softmax", "sigmoid", "softmax_post"):
+        x = rng.integers(-3, 4, (T, E)).astype(float)      # many ties
+        b = rng.uniform(-0.1, 0.1, E)
+        d = O.topk_fwd(x, K, sf, 4, 2, 1.5, b)
+        o = O.topk_fwd_compact(x, K, sf, 4, 2, 1.5, b)
+        assert sorted(o["token_expert_indices"].ravel().tolist()) == list(range(T * K))
+        for t in range(T):
+            idx = o["topk_indices"][t]
+            assert sorted(idx.tolist()) == np.nonzero(d["routing_map"][t])[0].tolist()
+            assert np.array_equal(o["topk_weights"][t], d["probs"][t][idx])
+            key = d["scores"][t][idx] + b[idx]
+            for k in range(K - 1):
+                assert key[k] > key[k + 1] or (key[k] == key[k + 1] and idx[k] < idx[k + 1])
+
+
+def test_compact():
+    check_compact()
+
+
 def test_aux_loss():
     check_aux_loss()
 
@@ -465,7 +506,27 @@ def _wrong_aux_loss(q, m, K, coeff):   # divides by T instead of T^2
     return loss * np.asarray(q).shape[0], tok
 
 
+_orig_compact = O.topk_fwd_compact
+
+
+def _wrong_compact_by_weight(logits, K, sf="softmax", ng=0, gk=0, c=1.0, expert_bias=None):
+    o = _orig_compact(logits, K, sf, ng, gk, c, expert_bias)   # ranks by weight, not key
+    order = np.argsort(-o["topk_weights"], axis=1, kind="stable")
+    o["topk_indices"] = np.take_along_axis(o["topk_indices"], order, 1)
+    o["topk_weights"] = np.take_along_axis(o["topk_weights"], order, 1)
+    return o
+
+
+def _wrong_compact_tei(logits, K, sf="softmax", ng=0, gk=0, c=1.0, expert_bias=None):
+    o = _orig_compact(logits, K, sf, ng, gk, c, expert_bias)   # t K + k instead of k T + t
+    T = np.asarray(logits).shape[0]
+    o["token_expert_indices"] = np.arange(T * K).reshape(T, K)
+    return o
+
+
 PLANTED = [
+    ("topk_fwd_compact", _wrong_compact_by_weight, [check_compact]),
+    ("topk_fwd_compact", _wrong_compact_tei, [check_compact]),
     ("order_desc", _wrong_order, [check_topk_brute_force]),
     ("score_row", _wrong_softmax_score, [check_softmax_closed_form]),
     ("score_row", _wrong_sigmoid_sign, [check_sigmoid_closed_form]),
