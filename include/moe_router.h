@@ -119,6 +119,40 @@ MR_API int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int
                     uint8_t* routing_map, float* scores, mr_stream_t stream);
 
 /*
+ * router_topk_fwd_compact — the same router forward with compact outputs:
+ * per token, the K selected experts and their probabilities as [T, K] rows,
+ * written alongside or instead of the dense [T, E] tensors.
+ *
+ * Source: ROCm/aiter PR #5652, "[HIP] [Perf] Fold shared-expert gate GEMV
+ * into topk_softmax kernel", review (topk_softmax writes [T, K] weights,
+ * indices and token_expert_indices; the weights and indices are addressed
+ * through a row stride so that a caller can pass column views of wider
+ * buffers; token_expert_indices is [T, K]); NVIDIA TensorRT-LLM PR #14592,
+ * "[TRTLLM-12214][perf] DeepGemmFusedMoE: fuse masked gather +
+ * finalize-scale into one Triton kernel" (the expanded row of token t's k-th
+ * choice is t + k * num_rows).
+ *
+ * Row t, position k (0 <= k < K) holds the expert of rank k in the selection
+ * order (key s + bias descending, index ascending):
+ *   topk_weights[t * ld_weights + k]  its probability (as in probs), fp32
+ *   topk_indices[t * ld_indices + k]  its index, int32
+ *   token_expert_indices[t * K + k]   k * T + t (int32), when not NULL
+ * Columns K .. ld - 1 of the weights and indices are left untouched.
+ * probs, routing_map and scores are as in router_topk_fwd, each written only
+ * when its pointer is not NULL (the values are identical).
+ *
+ * Errors: as router_topk_fwd, with probs, routing_map and scores optional;
+ * MR_ERR_INVALID also for ld_weights < K, ld_indices < K, or NULL
+ * logits / topk_weights / topk_indices when T > 0.
+ */
+MR_API int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, int E, int K,
+                                   mr_score_func score_func, int num_groups, int group_topk,
+                                   float scaling_factor, const float* expert_bias,
+                                   float* topk_weights, int ld_weights, int32_t* topk_indices,
+                                   int ld_indices, int32_t* token_expert_indices, void* probs,
+                                   uint8_t* routing_map, float* scores, mr_stream_t stream);
+
+/*
  * router_topk_bwd — gradient of the forward's probs with respect to logits.
  *
  * Source: TransformerEngine PR #3012, Backward kernels (pass 1: per-row sums

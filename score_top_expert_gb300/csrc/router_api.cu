@@ -132,6 +132,16 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km) {
 }
 
 int occupancy_any(int sf, int dt, const StagedPlan& p) {
+  if (p.op == 2) {
+    if (sf == MR_SOFTMAX)
+      return dt == MR_F32 ? occupancy_staged_compact_softmax_f32(p)
+                          : occupancy_staged_compact_softmax_bf16(p);
+    if (sf == MR_SOFTMAX_POST)
+      return dt == MR_F32 ? occupancy_staged_compact_softmaxpost_f32(p)
+                          : occupancy_staged_compact_softmaxpost_bf16(p);
+    return dt == MR_F32 ? occupancy_staged_compact_sigmoid_f32(p)
+                        : occupancy_staged_compact_sigmoid_bf16(p);
+  }
   if (sf == MR_SOFTMAX)
     return dt == MR_F32 ? occupancy_staged_softmax_f32(p) : occupancy_staged_softmax_bf16(p);
   if (sf == MR_SOFTMAX_POST)
@@ -216,7 +226,17 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStre
   StagedPlan p{};
   if (!staged_plan(di, sf, dt, op, km, a.E, a.K, &p)) return MR_ERR_CUDA;
   cudaError_t e;
-  if (sf == MR_SOFTMAX) {
+  if (op == 2) {
+    if (sf == MR_SOFTMAX)
+      e = dt == MR_F32 ? launch_staged_compact_softmax_f32(a, p, di.status, st)
+                       : launch_staged_compact_softmax_bf16(a, p, di.status, st);
+    else if (sf == MR_SOFTMAX_POST)
+      e = dt == MR_F32 ? launch_staged_compact_softmaxpost_f32(a, p, di.status, st)
+                       : launch_staged_compact_softmaxpost_bf16(a, p, di.status, st);
+    else
+      e = dt == MR_F32 ? launch_staged_compact_sigmoid_f32(a, p, di.status, st)
+                       : launch_staged_compact_sigmoid_bf16(a, p, di.status, st);
+  } else if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_staged_softmax_f32(a, p, di.status, st)
                      : launch_staged_softmax_bf16(a, p, di.status, st);
   } else if (sf == MR_SOFTMAX_POST) {
@@ -315,7 +335,17 @@ bool choose_bwd(int E, int op, BwdConfig* c) {
 
 int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   cudaError_t e;
-  if (sf == MR_SOFTMAX) {
+  if (c.op == 2) {
+    if (sf == MR_SOFTMAX)
+      e = dt == MR_F32 ? launch_fwd_compact_softmax_f32(a, c, st)
+                       : launch_fwd_compact_softmax_bf16(a, c, st);
+    else if (sf == MR_SOFTMAX_POST)
+      e = dt == MR_F32 ? launch_fwd_compact_softmaxpost_f32(a, c, st)
+                       : launch_fwd_compact_softmaxpost_bf16(a, c, st);
+    else
+      e = dt == MR_F32 ? launch_fwd_compact_sigmoid_f32(a, c, st)
+                       : launch_fwd_compact_sigmoid_bf16(a, c, st);
+  } else if (sf == MR_SOFTMAX) {
     e = dt == MR_F32 ? launch_fwd_softmax_f32(a, c, st) : launch_fwd_softmax_bf16(a, c, st);
   } else if (sf == MR_SOFTMAX_POST) {
     e = dt == MR_F32 ? launch_fwd_softmaxpost_f32(a, c, st)
@@ -326,37 +356,31 @@ int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStr
   return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
-                    mr_score_func score_func, int num_groups, int group_topk,
-                    float scaling_factor, const float* expert_bias, void* probs,
-                    uint8_t* routing_map, float* scores, mr_stream_t stream) {
-  int rc = check_shape(dtype, T, E, K, score_func);
-  if (rc != MR_OK) return rc;
-  rc = check_groups(E, K, num_groups, group_topk);
-  if (rc != MR_OK) return rc;
-  if (T > 0 && (logits == nullptr || probs == nullptr || routing_map == nullptr ||
-                scores == nullptr))
-    return MR_ERR_INVALID;
-  if (T == 0) return MR_OK;
-
+// The top-K router forward behind router_topk_fwd (op 0: dense outputs) and
+// router_topk_fwd_compact (op 2: compact outputs, dense ones optional);
+// arguments already checked.
+int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, int score_func,
+                    int num_groups, int group_topk, float scaling_factor,
+                    const float* expert_bias, void* probs, uint8_t* routing_map, float* scores,
+                    float* topk_w, long long ld_w, int32_t* topk_i, long long ld_i,
+                    int32_t* tei, mr_stream_t stream) {
+  auto aligned_or_null = [](const void* p) { return p == nullptr || aligned16(p); };
   const bool grouped = num_groups > 1;
-  const bool vec = (E % 4 == 0) && aligned16(logits) && aligned16(probs) &&
-                   aligned16(routing_map) && aligned16(scores) &&
-                   (expert_bias == nullptr || aligned16(expert_bias));
+  const bool vec = (E % 4 == 0) && aligned16(logits) && aligned_or_null(probs) &&
+                   aligned_or_null(routing_map) && aligned_or_null(scores) &&
+                   aligned_or_null(expert_bias);
   const int km = (expert_bias != nullptr || grouped) ? 1 : 0;
   const bool staged = use_staged(E, dtype, vec);
   FwdConfig c{};
   if (!staged && !choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;
-  c.op = 0;
+  c.op = op;
   c.km = km;
   c.extra_smem = (grouped && !staged)
                      ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float)
                      : 0;
+  if (op == 2 && !staged)  // per segment: K selected words and weights
+    c.extra_smem += static_cast<size_t>(kFwdThreads / c.seg) * MR_MAX_TOPK * 12;
 
   FwdArgs a{};
   a.logits = logits;
@@ -365,6 +389,11 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
   a.map = routing_map;
   a.scores = scores;
   a.intermediate = nullptr;
+  a.topk_w = topk_w;
+  a.topk_i = topk_i;
+  a.tei = tei;
+  a.ld_w = ld_w;
+  a.ld_i = ld_i;
   a.T = T; a.E = E; a.K = K;
   a.scaling = scaling_factor;
   a.num_groups = grouped ? num_groups : 0;
@@ -386,8 +415,48 @@ int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
                               : 0;
   }
   if (staged)
-    return launch_staged_any(score_func, dtype, a, 0, km, reinterpret_cast<cudaStream_t>(stream));
+    return launch_staged_any(score_func, dtype, a, op, km, reinterpret_cast<cudaStream_t>(stream));
   return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int K,
+                    mr_score_func score_func, int num_groups, int group_topk,
+                    float scaling_factor, const float* expert_bias, void* probs,
+                    uint8_t* routing_map, float* scores, mr_stream_t stream) {
+  int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  rc = check_groups(E, K, num_groups, group_topk);
+  if (rc != MR_OK) return rc;
+  if (T > 0 && (logits == nullptr || probs == nullptr || routing_map == nullptr ||
+                scores == nullptr))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  return topk_fwd_launch(0, logits, dtype, T, E, K, score_func, num_groups, group_topk,
+                         scaling_factor, expert_bias, probs, routing_map, scores, nullptr, 0,
+                         nullptr, 0, nullptr, stream);
+}
+
+int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, int E, int K,
+                            mr_score_func score_func, int num_groups, int group_topk,
+                            float scaling_factor, const float* expert_bias,
+                            float* topk_weights, int ld_weights, int32_t* topk_indices,
+                            int ld_indices, int32_t* token_expert_indices, void* probs,
+                            uint8_t* routing_map, float* scores, mr_stream_t stream) {
+  int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  rc = check_groups(E, K, num_groups, group_topk);
+  if (rc != MR_OK) return rc;
+  if (ld_weights < K || ld_indices < K) return MR_ERR_INVALID;
+  if (T > 0 && (logits == nullptr || topk_weights == nullptr || topk_indices == nullptr))
+    return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  return topk_fwd_launch(2, logits, dtype, T, E, K, score_func, num_groups, group_topk,
+                         scaling_factor, expert_bias, probs, routing_map, scores, topk_weights,
+                         ld_weights, topk_indices, ld_indices, token_expert_indices, stream);
 }
 
 int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,

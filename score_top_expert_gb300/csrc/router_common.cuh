@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe_router.h"
+
 namespace moe_router {
 
 // SF_SOFTMAX_POST scores like softmax (over all E) and renormalises the

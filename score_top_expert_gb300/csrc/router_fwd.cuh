@@ -33,6 +33,10 @@
 //
 // OP 0: top-K router (probs, routing_map, scores).
 // OP 1: aux-loss scores (scores = q, routing_map, intermediate = sigmoid).
+// OP 2: top-K router with compact outputs: per row the K selected experts in
+//   rank order (key descending, index ascending) with their probabilities,
+//   and the expanded row k T + t of each; probs, map and scores are written
+//   too where their pointers are set.
 #pragma once
 
 #include "router_common.cuh"
@@ -46,6 +50,10 @@ struct FwdArgs {
   uint8_t* map;           // [T,E]
   float* scores;          // [T,E]: OP 0 s, OP 1 q
   float* intermediate;    // OP 1: [T,E] sigmoid (may be null for softmax)
+  float* topk_w;          // OP 2: [T, ld_w] probabilities in rank order
+  int32_t* topk_i;        // OP 2: [T, ld_i] expert indices in rank order
+  int32_t* tei;           // OP 2: [T, K] expanded rows k T + t, or null
+  long long ld_w, ld_i;   // OP 2: row strides (elements) of topk_w / topk_i
   int T, E, K;
   int num_groups;         // > 1 only when grouping is on (KM 1)
   int group_topk;
@@ -63,6 +71,31 @@ constexpr int kFwdThreads = 256;
 constexpr int kCandPerLane = 4;
 constexpr int kMaxGroups = 32;
 constexpr int kTopMRegs = 4;  // grouped top-M sums up to this M use an insertion list
+
+// Compact outputs of one row (OP 2): rank every selected word among the K
+// selected words of the segment's list (K <= MR_MAX_TOPK) and write position
+// rank of the row.  words[i] = (ordered key << 32 | ~index), p[i] its weight.
+template <int SEG>
+__device__ __forceinline__ void write_compact_row(const FwdArgs& a, int row, int li,
+                                                  const unsigned long long* words,
+                                                  const float* p) {
+  constexpr int kPerLane = (MR_MAX_TOPK + SEG - 1) / SEG;
+  const int K = a.K;
+#pragma unroll
+  for (int r = 0; r < kPerLane; ++r) {
+    const int i = r * SEG + li;
+    if (i < K) {
+      const unsigned long long w = words[i];
+      int rank = 0;
+#pragma unroll 4
+      for (int c = 0; c < K; ++c) rank += words[c] > w;
+      const size_t t = static_cast<size_t>(row);
+      a.topk_w[t * a.ld_w + rank] = p[i];
+      a.topk_i[t * a.ld_i + rank] = static_cast<int32_t>(~static_cast<uint32_t>(w));
+      if (a.tei != nullptr) a.tei[t * K + rank] = rank * a.T + row;
+    }
+  }
+}
 
 template <int SEG>
 struct FwdSegSmem {
@@ -326,7 +359,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
 
   unsigned long long thr = 0ull;  // the K-th largest packed word of the row
   float sel_sum = 0.0f;           // sum of s over the selected (sigmoid top-K)
-  constexpr bool kNeedSelSum = (OP == 0 && SF != SF_SOFTMAX);  // renormalised probs
+  constexpr bool kNeedSelSum = (OP != 1 && SF != SF_SOFTMAX);  // renormalised probs
   if (total <= CAP) {
     int pos = seg_exclusive_scan<SEG>(my_cnt);
 #pragma unroll
@@ -456,6 +489,40 @@ router_fwd_seg_kernel(const FwdArgs a) {
   const float tkf = key_to_float(tk);
   float pf = a.scaling;
   if constexpr (kNeedSelSum) pf = a.scaling / sel_sum;
+  auto selected = [&](int j, int u) -> bool {
+    const int e = 4 * (li + SEG * j) + u;
+    if constexpr (KM == 0) return (v[j][u] > tkf) || (v[j][u] == tkf && e <= ti);
+    else return (kk[j][u] > tk) || (kk[j][u] == tk && kk[j][u] != 0u && e <= ti);
+  };
+  if constexpr (OP == 2) {
+    // the K selected words and weights, gathered in lane order into the
+    // segment's list, then ranked
+    unsigned char* extra = reinterpret_cast<unsigned char*>(segs + SEGS_PER_BLOCK);
+    if (a.num_groups > 1) extra += static_cast<size_t>(SEGS_PER_BLOCK) * E * sizeof(float);
+    unsigned long long* words =
+        reinterpret_cast<unsigned long long*>(extra) + seg_id * MR_MAX_TOPK;
+    float* wp = reinterpret_cast<float*>(reinterpret_cast<unsigned long long*>(extra) +
+                                         SEGS_PER_BLOCK * MR_MAX_TOPK) +
+                seg_id * MR_MAX_TOPK;
+    int nsel = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) nsel += elem_ok(j, u) && selected(j, u);
+    int pos = seg_exclusive_scan<SEG>(nsel);
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (elem_ok(j, u) && selected(j, u)) {
+          words[pos] = pack_key(key_at(j, u), 4 * (li + SEG * j) + u);
+          wp[pos] = score_at(j, u) * pf;
+          ++pos;
+        }
+    __syncwarp(smask);
+    if (active) write_compact_row<SEG>(a, row, li, words, wp);
+    if (a.map == nullptr && a.probs == nullptr && a.scores == nullptr) return;
+  }
 #pragma unroll
   for (int j = 0; j < NC; ++j) {
     if (!chunk_ok(j)) continue;
@@ -464,18 +531,14 @@ router_fwd_seg_kernel(const FwdArgs a) {
     float s[4], p[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if constexpr (KM == 0) {
-        m[u] = (v[j][u] > tkf) || (v[j][u] == tkf && e0 + u <= ti);
-      } else {
-        m[u] = (kk[j][u] > tk) || (kk[j][u] == tk && kk[j][u] != 0u && e0 + u <= ti);
-      }
+      m[u] = selected(j, u);
       s[u] = score_at(j, u);
       p[u] = m[u] ? s[u] * pf : 0.0f;
     }
-    store_map4<VEC>(a.map, off, e0, E, m);
-    if constexpr (OP == 0) {
-      store4<DT, VEC>(a.probs, off, e0, E, p);
-      store4_f32<VEC>(a.scores, off, e0, E, s);
+    if (OP != 2 || a.map != nullptr) store_map4<VEC>(a.map, off, e0, E, m);
+    if constexpr (OP != 1) {
+      if (OP == 0 || a.probs != nullptr) store4<DT, VEC>(a.probs, off, e0, E, p);
+      if (OP == 0 || a.scores != nullptr) store4_f32<VEC>(a.scores, off, e0, E, s);
     } else {
       float q[4];
       if constexpr (SF == SF_SOFTMAX) {

@@ -1,4 +1,4 @@
-// Router forward, shared-memory staged path (no bias, no groups).
+// Router forward, shared-memory staged path.
 //
 // A segment of SEG lanes (16 or 32; a warp holds 32 / SEG segments) owns one
 // token row at a time and walks the rows of the batch persistently (row,
@@ -31,7 +31,11 @@
 //   4  scores: softmax e = exp(x - max) and the row sum, or sigmoid s; fp32
 //      rows store them over their logits (bf16 rows recompute them in 5).
 //   5  outputs from the scores and the bitmask: probs, map, scores (top-K)
-//      or q, map, intermediate (aux scores).
+//      or q, map, intermediate (aux scores).  Compact outputs (OP 2) gather
+//      the K selected (key, ~index) words into the candidate buffer, rank
+//      them, and write the row's K weights, indices and expanded rows; the
+//      dense outputs follow only where their pointers are set, and the
+//      logits stay in the stage (scores are recomputed, not stored).
 // Keying on the logit is exact: softmax and sigmoid are strictly increasing.
 //
 // Key mode KM 1 (top-K with a bias and/or groups): before pass 1 the row's
@@ -225,8 +229,10 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   constexpr int CAP = kCandPerLane * SEG;
   constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
   constexpr int D = DT == DT_F32 ? 4 : 2;
-  constexpr bool kSigTopk = (OP == 0 && SF != SF_SOFTMAX);  // probs renormalised over the K
-  constexpr bool kStore = (DT == DT_F32 && KM == 0);  // scores kept over the fp32 logits
+  constexpr bool kSigTopk = (OP != 1 && SF != SF_SOFTMAX);  // probs renormalised over the K
+  // scores kept over the fp32 logits (not with compact outputs, which read
+  // the logits after pass 4)
+  constexpr bool kStore = (DT == DT_F32 && KM == 0 && OP != 2);
   constexpr bool kNeedSum = (SF != SF_SIGMOID || OP == 1) && KM == 0;
   constexpr int KDT = KM == 0 ? DT : DT_F32;  // type of the selection keys
   extern __shared__ __align__(128) unsigned char smem[];
@@ -684,14 +690,48 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
     float pf = a.scaling;
     if constexpr (kSigTopk) pf = a.scaling / seg_sum<SEG>(part);
-    else if constexpr (SF == SF_SOFTMAX && OP == 0) pf = a.scaling * inv;
+    else if constexpr (SF == SF_SOFTMAX && OP != 1) pf = a.scaling * inv;
     __syncwarp(smask);
+
+    bool dense = true;  // OP 2: dense outputs requested
+    if constexpr (OP == 2) {
+      // ---- compact outputs: gather the K selected words (lane order), rank ----
+      CandMask<NC> sel;  // the lane's selected experts, bit 4 j + u
+      sel.clear();
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        const int c = li + SEG * j;
+        if (FULL || c < nchunks)
+          sel.w[(4 * j) >> 5] |= ((selmask[c >> 3] >> (4 * (c & 7))) & 0xfu) << ((4 * j) & 31);
+      }
+      int pos = seg_exclusive_scan<SEG>(sel.count());
+      float* cand_p = reinterpret_cast<float*>(cand + MR_MAX_TOPK);
+#pragma unroll
+      for (int i = 0; i < CandMask<NC>::W; ++i) {
+        uint32_t bits = sel.w[i];
+#pragma unroll 1
+        while (bits) {
+          const int b = 32 * i + __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int idx = 4 * (li + SEG * (b >> 2)) + (b & 3);
+          const float x = stage_x1<DT>(stage, idx);
+          const float key = KM == 1 ? work[idx] : x;
+          const float w = (SF != SF_SIGMOID) ? exp_shifted(x, max_l2e) : sigmoid_f32(x);
+          cand[pos] = pack_key(ordered_key(key), idx);
+          cand_p[pos] = w * pf;
+          ++pos;
+        }
+      }
+      __syncwarp(smask);
+      write_compact_row<SEG>(a, row, li, cand, cand_p);
+      dense = a.map != nullptr || a.probs != nullptr || a.scores != nullptr;
+    }
 
     // ---- 5: outputs -----------------------------------------------------------------------
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
       const int c = li + SEG * j;
-      if (FULL || c < nchunks) {
+      if (dense && (FULL || c < nchunks)) {
         float w[4];  // e (softmax) or s (sigmoid)
         if constexpr (kStore) {
           const float4 t = lds_f4(stage + 16 * c);
@@ -707,16 +747,17 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         }
         const uint32_t bits = (selmask[c >> 3] >> (4 * (c & 7))) & 0xfu;
         const uint32_t mapw = (bits * 0x00204081u) & 0x01010101u;
-        __stcs(reinterpret_cast<unsigned int*>(a.map + off + 4 * c), mapw);
+        if (OP != 2 || a.map != nullptr)
+          __stcs(reinterpret_cast<unsigned int*>(a.map + off + 4 * c), mapw);
         float s[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? w[u] * inv : w[u];
-        if constexpr (OP == 0) {
+        if constexpr (OP != 1) {
           float p[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) p[u] = (bits & (1u << u)) ? w[u] * pf : 0.0f;
-          store4<DT, true>(a.probs, off, 4 * c, E, p);
-          store4_f32<true>(a.scores, off, 4 * c, E, s);
+          if (OP == 0 || a.probs != nullptr) store4<DT, true>(a.probs, off, 4 * c, E, p);
+          if (OP == 0 || a.scores != nullptr) store4_f32<true>(a.scores, off, 4 * c, E, s);
         } else if constexpr (SF == SF_SOFTMAX) {
           store4_f32<true>(a.scores, off, 4 * c, E, s);
           if (a.intermediate != nullptr) store4_f32<true>(a.intermediate, off, 4 * c, E, s);

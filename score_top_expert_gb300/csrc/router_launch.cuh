@@ -16,7 +16,7 @@ struct FwdConfig {
   int nc;      // chunks of 4 experts per lane
   bool vec;    // aligned 16-byte rows
   int km;      // key mode (0: key = logit; 1: key = s + bias, optional groups)
-  int op;      // 0 top-K router, 1 aux scores
+  int op;      // 0 top-K router, 1 aux scores, 2 top-K with compact outputs
   size_t extra_smem;  // grouped: rows of keys staged in shared memory
 };
 
@@ -50,23 +50,31 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
   return cudaGetLastError();
 }
 
-template <int SF, int DT, int SEG, int NC, bool VEC>
+// COMPACT instantiates the compact-output router (OP 2) only; the other
+// modes live in separate translation units.
+template <int SF, int DT, int SEG, int NC, bool VEC, bool COMPACT>
 cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
-    if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
+  if constexpr (COMPACT) {
+    return c.km == 1 ? launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 2>(a, c, st)
+                     : launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 2>(a, c, st);
+  } else {
+    if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
+      if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
+    }
+    if (c.km == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 0>(a, c, st);
+    return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 0>(a, c, st);
   }
-  if (c.km == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 0>(a, c, st);
-  return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 0>(a, c, st);
 }
 
-template <int SF, int DT>
+template <int SF, int DT, bool COMPACT = false>
 cudaError_t launch_fwd(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   if (!c.vec) {
-    if (c.seg == 32 && c.nc == 18) return launch_fwd_mode<SF, DT, 32, 18, false>(a, c, st);
+    if (c.seg == 32 && c.nc == 18)
+      return launch_fwd_mode<SF, DT, 32, 18, false, COMPACT>(a, c, st);
     return cudaErrorInvalidConfiguration;
   }
 #define MR_FWD_CASE(S, N) \
-  if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true>(a, c, st);
+  if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true, COMPACT>(a, c, st);
   MR_FWD_VEC_CONFIGS(MR_FWD_CASE)
 #undef MR_FWD_CASE
   return cudaErrorInvalidConfiguration;
@@ -159,43 +167,59 @@ int staged_blocks_per_sm(int warps_per_block, size_t smem) {
   return n;
 }
 
-template <int SF, int DT>
+template <int SF, int DT, bool COMPACT = false>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
 #define MR_STAGED_CASE(S, N)                                                               \
   if (p.seg == S && p.nc == N) {                                                           \
-    if constexpr (SF != SF_SOFTMAX_POST) {                                                 \
-      if (p.op == 1)                                                                       \
-        return p.full ? launch_staged_inst<SF, DT, S, N, 1, true, 0>(a, p, status, st)     \
-                      : launch_staged_inst<SF, DT, S, N, 1, false, 0>(a, p, status, st);   \
+    if constexpr (COMPACT) {                                                               \
+      if (p.km == 1)                                                                       \
+        return p.full ? launch_staged_inst<SF, DT, S, N, 2, true, 1>(a, p, status, st)     \
+                      : launch_staged_inst<SF, DT, S, N, 2, false, 1>(a, p, status, st);   \
+      return p.full ? launch_staged_inst<SF, DT, S, N, 2, true, 0>(a, p, status, st)       \
+                    : launch_staged_inst<SF, DT, S, N, 2, false, 0>(a, p, status, st);     \
+    } else {                                                                               \
+      if constexpr (SF != SF_SOFTMAX_POST) {                                               \
+        if (p.op == 1)                                                                     \
+          return p.full ? launch_staged_inst<SF, DT, S, N, 1, true, 0>(a, p, status, st)   \
+                        : launch_staged_inst<SF, DT, S, N, 1, false, 0>(a, p, status, st); \
+      }                                                                                    \
+      if (p.km == 1)                                                                       \
+        return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 1>(a, p, status, st)     \
+                      : launch_staged_inst<SF, DT, S, N, 0, false, 1>(a, p, status, st);   \
+      return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 0>(a, p, status, st)       \
+                    : launch_staged_inst<SF, DT, S, N, 0, false, 0>(a, p, status, st);     \
     }                                                                                      \
-    if (p.km == 1)                                                                         \
-      return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 1>(a, p, status, st)       \
-                    : launch_staged_inst<SF, DT, S, N, 0, false, 1>(a, p, status, st);     \
-    return p.full ? launch_staged_inst<SF, DT, S, N, 0, true, 0>(a, p, status, st)         \
-                  : launch_staged_inst<SF, DT, S, N, 0, false, 0>(a, p, status, st);       \
   }
   MR_STAGED_SHAPES(MR_STAGED_CASE)
 #undef MR_STAGED_CASE
   return cudaErrorInvalidConfiguration;
 }
 
-template <int SF, int DT>
+template <int SF, int DT, bool COMPACT = false>
 int staged_occupancy(const StagedPlan& p) {
   const size_t smem = p.layout.head_bytes +
       static_cast<size_t>(p.warps_per_block) * (32 / p.seg) * p.layout.seg_bytes;
 #define MR_STAGED_OCC(S, N)                                                                \
   if (p.seg == S && p.nc == N) {                                                           \
     const int w = p.warps_per_block;                                                       \
-    if constexpr (SF != SF_SOFTMAX_POST) {                                                 \
-      if (p.op == 1)                                                                       \
-        return p.full ? staged_blocks_per_sm<SF, DT, S, N, 1, true, 0>(w, smem)            \
-                      : staged_blocks_per_sm<SF, DT, S, N, 1, false, 0>(w, smem);          \
+    if constexpr (COMPACT) {                                                               \
+      if (p.km == 1)                                                                       \
+        return p.full ? staged_blocks_per_sm<SF, DT, S, N, 2, true, 1>(w, smem)            \
+                      : staged_blocks_per_sm<SF, DT, S, N, 2, false, 1>(w, smem);          \
+      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 2, true, 0>(w, smem)              \
+                    : staged_blocks_per_sm<SF, DT, S, N, 2, false, 0>(w, smem);            \
+    } else {                                                                               \
+      if constexpr (SF != SF_SOFTMAX_POST) {                                               \
+        if (p.op == 1)                                                                     \
+          return p.full ? staged_blocks_per_sm<SF, DT, S, N, 1, true, 0>(w, smem)          \
+                        : staged_blocks_per_sm<SF, DT, S, N, 1, false, 0>(w, smem);        \
+      }                                                                                    \
+      if (p.km == 1)                                                                       \
+        return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 1>(w, smem)            \
+                      : staged_blocks_per_sm<SF, DT, S, N, 0, false, 1>(w, smem);          \
+      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 0>(w, smem)              \
+                    : staged_blocks_per_sm<SF, DT, S, N, 0, false, 0>(w, smem);            \
     }                                                                                      \
-    if (p.km == 1)                                                                         \
-      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 1>(w, smem)              \
-                    : staged_blocks_per_sm<SF, DT, S, N, 0, false, 1>(w, smem);            \
-    return p.full ? staged_blocks_per_sm<SF, DT, S, N, 0, true, 0>(w, smem)                \
-                  : staged_blocks_per_sm<SF, DT, S, N, 0, false, 0>(w, smem);              \
   }
   MR_STAGED_SHAPES(MR_STAGED_OCC)
 #undef MR_STAGED_OCC
@@ -223,5 +247,20 @@ cudaError_t launch_fwd_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream
 cudaError_t launch_fwd_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_fwd_sigmoid_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
 cudaError_t launch_bwd_any(int sf, int dt, const BwdArgs&, const BwdConfig&, cudaStream_t);
+
+// Compact-output router (OP 2), both paths, one (score function, dtype)
+// pair per translation unit.
+#define MR_DECLARE_COMPACT(NAME)                                                     \
+  cudaError_t launch_fwd_compact_##NAME(const FwdArgs&, const FwdConfig&, cudaStream_t); \
+  cudaError_t launch_staged_compact_##NAME(const FwdArgs&, const StagedPlan&, int*,    \
+                                           cudaStream_t);                              \
+  int occupancy_staged_compact_##NAME(const StagedPlan&);
+MR_DECLARE_COMPACT(softmax_f32)
+MR_DECLARE_COMPACT(softmax_bf16)
+MR_DECLARE_COMPACT(sigmoid_f32)
+MR_DECLARE_COMPACT(sigmoid_bf16)
+MR_DECLARE_COMPACT(softmaxpost_f32)
+MR_DECLARE_COMPACT(softmaxpost_bf16)
+#undef MR_DECLARE_COMPACT
 
 }  // namespace moe_router

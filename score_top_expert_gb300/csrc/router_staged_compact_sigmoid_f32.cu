@@ -1,0 +1,13 @@
+// Instantiations of the compact-output router forward, staged path:
+// sigmoid score, f32 logits.
+#include "router_launch.cuh"
+
+namespace moe_router {
+cudaError_t launch_staged_compact_sigmoid_f32(const FwdArgs& a, const StagedPlan& p, int* status,
+                                           cudaStream_t st) {
+  return launch_staged<SF_SIGMOID, DT_F32, true>(a, p, status, st);
+}
+int occupancy_staged_compact_sigmoid_f32(const StagedPlan& p) {
+  return staged_occupancy<SF_SIGMOID, DT_F32, true>(p);
+}
+}  // namespace moe_router

@@ -49,10 +49,13 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(path)
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.router_topk_fwd.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, vp, vp, vp]
+        L.router_topk_fwd_compact.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, i, vp, i, vp,
+                                              vp, vp, vp, vp]
         L.router_topk_bwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.router_aux_scores_fwd.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
         L.router_aux_scores_bwd.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
-        for fn in ("router_topk_fwd", "router_topk_bwd", "router_aux_scores_fwd",
+        for fn in ("router_topk_fwd", "router_topk_fwd_compact", "router_topk_bwd",
+                   "router_aux_scores_fwd",
                    "router_aux_scores_bwd", "moe_router_force_path",
                    "moe_router_force_fwd_lanes", "moe_router_version",
                    "moe_router_device_status"):
@@ -140,6 +143,68 @@ def router_topk_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax",
                                    _ptr(routing_map), _ptr(scores), _stream(dev))
     _check("router_topk_fwd", rc)
     return probs, routing_map, scores
+
+
+def _rows_out(t, T, K, dtype, device, name):
+    """A [T, >= K] output addressed by row stride (unit column stride): a
+    column view of a wider buffer is written in place."""
+    if t is None:
+        return torch.empty((T, K), dtype=dtype, device=device)
+    if t.dim() != 2 or t.shape[0] != T or t.shape[1] < K or t.dtype != dtype \
+            or t.device != device or (T > 1 and t.stride(1) != 1) or t.stride(0) < K:
+        raise ValueError(f"{name} must be a {dtype} [T, >= K] tensor with unit column "
+                         f"stride and row stride >= K")
+    return t
+
+
+def router_topk_fwd_compact(logits: torch.Tensor, K: int, score_func: str = "softmax",
+                            num_groups: int = 0, group_topk: int = 0,
+                            scaling_factor: float = 1.0,
+                            expert_bias: torch.Tensor | None = None, *, topk_weights=None,
+                            topk_indices=None, token_expert_indices=True, dense=False,
+                            probs=None, routing_map=None, scores=None):
+    """Top-K router forward with compact outputs.  Returns (topk_weights
+    [T,K] float32, topk_indices [T,K] int32, token_expert_indices [T,K] int32
+    or None, probs, routing_map, scores); row t, column k holds the expert of
+    rank k (selection key descending, index ascending).  topk_weights and
+    topk_indices may be column views of wider buffers (written in place).
+    token_expert_indices: True to allocate, False/None to skip, or a
+    contiguous [T,K] int32 tensor.  The dense outputs are None unless
+    dense=True or given."""
+    logits = _as_input(logits, "logits", _DTYPE)
+    T, E = logits.shape
+    dev = logits.device
+    K = int(K)
+    if expert_bias is not None:
+        if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
+                or expert_bias.device != dev:
+            raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
+        expert_bias = expert_bias.contiguous()
+    topk_weights = _rows_out(topk_weights, T, K, torch.float32, dev, "topk_weights")
+    topk_indices = _rows_out(topk_indices, T, K, torch.int32, dev, "topk_indices")
+    if token_expert_indices is True:
+        token_expert_indices = torch.empty((T, K), dtype=torch.int32, device=dev)
+    elif token_expert_indices is False:
+        token_expert_indices = None
+    elif token_expert_indices is not None:
+        token_expert_indices = _out(token_expert_indices, (T, K), torch.int32, dev,
+                                    "token_expert_indices")
+    if dense or probs is not None:
+        probs = _out(probs, (T, E), logits.dtype, dev, "probs")
+    if dense or routing_map is not None:
+        routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
+    if dense or scores is not None:
+        scores = _out(scores, (T, E), torch.float32, dev, "scores")
+    ld_w = topk_weights.stride(0) if T > 0 else K
+    ld_i = topk_indices.stride(0) if T > 0 else K
+    with torch.cuda.device(dev):
+        rc = lib().router_topk_fwd_compact(
+            _ptr(logits), _DTYPE[logits.dtype], T, E, K, _score(score_func), int(num_groups),
+            int(group_topk), float(scaling_factor), _ptr(expert_bias), _ptr(topk_weights),
+            ld_w, _ptr(topk_indices), ld_i, _ptr(token_expert_indices), _ptr(probs),
+            _ptr(routing_map), _ptr(scores), _stream(dev))
+    _check("router_topk_fwd_compact", rc)
+    return topk_weights, topk_indices, token_expert_indices, probs, routing_map, scores
 
 
 def router_topk_bwd(grad_probs: torch.Tensor, routing_map: torch.Tensor,

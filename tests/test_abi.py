@@ -161,3 +161,19 @@ def test_aux_loss_noalloc_argument_checks(L):
     assert fwd(f, f, 4, 16, 17, c, f, f, None) == -1
     assert fwd(f, f, 4, 16, 2, c, None, f, None) == -1
     assert fwd(None, None, 0, 16, 2, c, None, None, None) == 0
+
+
+def test_topk_fwd_compact_rejects(L):
+    f, c = FAKE, 1.0
+    fn = L.router_topk_fwd_compact
+    # (logits, dtype, T, E, K, sf, ng, gk, c, bias, w, ldw, idx, ldi, tei, probs, map, scores)
+    assert fn(f, 0, 4, 16, 2, 0, 0, 0, c, None, f, 1, f, 2, None, None, None, None, None) == -1
+    assert fn(f, 0, 4, 16, 2, 0, 0, 0, c, None, f, 2, f, 1, None, None, None, None, None) == -1
+    assert fn(f, 0, 4, 16, 2, 0, 0, 0, c, None, None, 2, f, 2, None, None, None, None, None) == -1
+    assert fn(f, 0, 4, 16, 2, 0, 0, 0, c, None, f, 2, None, 2, None, None, None, None, None) == -1
+    assert fn(None, 0, 4, 16, 2, 0, 0, 0, c, None, f, 2, f, 2, None, None, None, None, None) == -1
+    assert fn(f, 0, 4, 16, 17, 0, 0, 0, c, None, f, 17, f, 17, None, None, None, None, None) == -1
+    assert fn(f, 0, 4, 2305, 2, 0, 0, 0, c, None, f, 2, f, 2, None, None, None, None, None) == -2
+    assert fn(f, 0, 4, 16, 3, 0, 4, 2, c, None, f, 3, f, 3, None, None, None, None, None) == -1
+    assert fn(None, 0, 0, 16, 2, 0, 0, 0, c, None, None, 2, None, 2, None, None, None, None,
+              None) == 0
