@@ -222,6 +222,41 @@ def topk_fwd_compact(logits, K, score_func=SOFTMAX, num_groups=0, group_topk=0,
 
 
 # --------------------------------------------------------------------------
+# expert maps  [ORT] Description item 1 (the (expert, token)-sorted expert
+# maps of the top-k choices) and the review's parity request (both row maps,
+# the expert ids and the expert offsets); [TRT] reverse-permute map
+# (permuted_row = unpermuted_to_permuted[t + k * num_rows]; the expert of a
+# permuted row and its column permuted_row - expert_first_token_offset[e]).
+# Reading: the T K choices are sorted by (expert ascending, token
+# ascending); a token picks an expert at most once, so the order is unique.
+# --------------------------------------------------------------------------
+def expert_maps(topk_indices, E):
+    """Returns a dict of int64 arrays from the [T, K] expert choices:
+    expert_first_token_offset [E+1] (first permuted row of each expert; the
+    last entry is T K), permuted_to_unpermuted [T K] (the expanded row
+    t + k T of each permuted row), unpermuted_to_permuted [T K] (its
+    inverse), permuted_experts [T K] (the expert of each permuted row)."""
+    idx = np.asarray(topk_indices, dtype=np.int64)
+    T, K = idx.shape
+    choices = sorted((int(idx[t, k]), t, k) for t in range(T) for k in range(K))
+    n = T * K
+    p2u = np.zeros(n, dtype=np.int64)
+    u2p = np.zeros(n, dtype=np.int64)
+    experts = np.zeros(n, dtype=np.int64)
+    for p, (e, t, k) in enumerate(choices):
+        p2u[p] = t + k * T
+        u2p[t + k * T] = p
+        experts[p] = e
+    counts = np.zeros(E, dtype=np.int64)
+    for e, _, _ in choices:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    return dict(expert_first_token_offset=offsets, permuted_to_unpermuted=p2u,
+                unpermuted_to_permuted=u2p, permuted_experts=experts)
+
+
+# --------------------------------------------------------------------------
 # router top-K backward  [TE] Backward kernels (two passes: row sums, then
 # per-element gradients); review summary (gradient per score function)
 # --------------------------------------------------------------------------

@@ -294,6 +294,42 @@ def test_compact():
     check_compact()
 
 
+def check_expert_maps():
+    """A hand-worked 3 x 2 case (expert 0 taken by token 0 at k = 1 before
+    token 1 at k = 0: token order, not k order), then invariants on random
+    routings: the maps are inverse permutations, each permuted row's expert
+    and column recover the (t, k) choice through the reverse-permute
+    formula, offsets are the histogram's prefix sums, and tokens rise inside
+    each expert's range."""
+    m = O.expert_maps(np.array([[2, 0], [0, 1], [2, 1]]), 4)
+    assert m["permuted_to_unpermuted"].tolist() == [3, 1, 4, 5, 0, 2]
+    assert m["unpermuted_to_permuted"].tolist() == [4, 1, 5, 0, 2, 3]
+    assert m["permuted_experts"].tolist() == [0, 0, 1, 1, 2, 2]
+    assert m["expert_first_token_offset"].tolist() == [0, 2, 4, 6, 6]
+    rng = np.random.default_rng(14)
+    for T, E, K in ((1, 8, 3), (5, 6, 6), (40, 64, 8), (33, 300, 36)):
+        idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+        m = O.expert_maps(idx, E)
+        p2u, u2p = m["permuted_to_unpermuted"], m["unpermuted_to_permuted"]
+        off, ex = m["expert_first_token_offset"], m["permuted_experts"]
+        n = T * K
+        assert sorted(p2u.tolist()) == list(range(n))
+        assert np.array_equal(u2p[p2u], np.arange(n))
+        assert np.array_equal(off, np.concatenate([[0], np.cumsum(np.bincount(idx.ravel(), minlength=E))]))
+        for t in range(T):
+            for k in range(K):
+                p = u2p[t + k * T]
+                e = ex[p]
+                assert e == idx[t, k] and off[e] <= p < off[e + 1]
+        tok = p2u % T
+        for e in range(E):
+            assert np.all(np.diff(tok[off[e]:off[e + 1]]) > 0)
+
+
+def test_expert_maps():
+    check_expert_maps()
+
+
 def test_aux_loss():
     check_aux_loss()
 
@@ -524,7 +560,33 @@ def _wrong_compact_tei(logits, K, sf="softmax", ng=0, gk=0, c=1.0, expert_bias=N
     return o
 
 
+_orig_expert_maps = O.expert_maps
+
+
+def _wrong_maps_k_order(idx, E):   # sorts by (expert, k, token)
+    idx = np.asarray(idx)
+    T, K = idx.shape
+    out = _orig_expert_maps(idx, E)
+    choices = sorted((int(idx[t, k]), k, t) for t in range(T) for k in range(K))
+    out["permuted_to_unpermuted"] = np.array([t + k * T for _, k, t in choices])
+    out["unpermuted_to_permuted"][out["permuted_to_unpermuted"]] = np.arange(T * K)
+    return out
+
+
+def _wrong_maps_row_major(idx, E):   # expanded row t K + k instead of t + k T
+    idx = np.asarray(idx)
+    T, K = idx.shape
+    out = _orig_expert_maps(idx, E)
+    p2u = out["permuted_to_unpermuted"]
+    t, k = p2u % T, p2u // T
+    out["permuted_to_unpermuted"] = t * K + k
+    out["unpermuted_to_permuted"][out["permuted_to_unpermuted"]] = np.arange(T * K)
+    return out
+
+
 PLANTED = [
+    ("expert_maps", _wrong_maps_k_order, [check_expert_maps]),
+    ("expert_maps", _wrong_maps_row_major, [check_expert_maps]),
     ("topk_fwd_compact", _wrong_compact_by_weight, [check_compact]),
     ("topk_fwd_compact", _wrong_compact_tei, [check_compact]),
     ("order_desc", _wrong_order, [check_topk_brute_force]),
