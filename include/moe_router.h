@@ -153,6 +153,71 @@ MR_API int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, in
                                    uint8_t* routing_map, float* scores, mr_stream_t stream);
 
 /*
+ * router_expert_maps — the (expert, token)-sorted maps of [T, K] expert
+ * choices: the permutation that groups the T K (token, choice) rows by
+ * expert for the expert computation, and its inverse.
+ *
+ * Source: microsoft/onnxruntime PR #33366, "[CUDA] Add fused decode routing,
+ * single-pass finalize, and PDL overlap for NVFP4 QMoE", Description item 1
+ * ((expert, token)-sorted expert maps) and review (both row maps, expert ids
+ * and expert offsets); NVIDIA TensorRT-LLM PR #14592, "[TRTLLM-12214][perf]
+ * DeepGemmFusedMoE: fuse masked gather + finalize-scale into one Triton
+ * kernel" (permuted_row = unpermuted_to_permuted[t + k * num_rows]; the
+ * expert of a permuted row and its column permuted_row -
+ * expert_first_token_offset[expert]).
+ *
+ * The choice (t, k) is the expanded row u = t + k T.  Choices are ordered by
+ * expert ascending, then token ascending; permuted row p is the p-th choice.
+ *   expert_first_token_offset [E+1] int32: first permuted row of expert e;
+ *                             entry E is the number of choices placed
+ *   permuted_to_unpermuted    [T K] int32: the expanded row u of row p
+ *   unpermuted_to_permuted    [T K] int32: the permuted row of u
+ *   permuted_experts          [T K] int32: the expert of row p
+ * topk_indices [T, ld_indices] int32 (the first K columns are read), e.g.
+ * from router_topk_fwd_compact.  Each row should name K distinct experts: a
+ * repeated expert leaves the maps unspecified (never written out of range).
+ * An index outside [0, E) is skipped: its unpermuted_to_permuted entry is -1
+ * and it takes no permuted row.
+ * workspace: device memory of router_expert_maps_workspace_bytes(T, E)
+ * bytes, 16-byte aligned; its contents need no initialisation.  Three
+ * kernel launches on the stream, deterministic.
+ *
+ * MR_ERR_INVALID: T < 0, E < 1, K < 1, K > E, ld_indices < K, T*E > INT_MAX,
+ *   a NULL pointer when T > 0, a small or misaligned workspace.
+ * MR_ERR_UNSUPPORTED: E > MR_MAX_EXPERTS or K > MR_MAX_TOPK.
+ * T = 0: nothing is written.
+ */
+MR_API size_t router_expert_maps_workspace_bytes(int T, int E);
+MR_API int router_expert_maps(const int32_t* topk_indices, int ld_indices, int T, int E, int K,
+                              int32_t* expert_first_token_offset,
+                              int32_t* permuted_to_unpermuted, int32_t* unpermuted_to_permuted,
+                              int32_t* permuted_experts, void* workspace, size_t workspace_bytes,
+                              mr_stream_t stream);
+
+/*
+ * router_topk_fwd_maps — router_topk_fwd_compact followed by
+ * router_expert_maps of its indices.  Up to 8 tokens (decode) with 16-byte
+ * aligned logits (and bias), E % 4 == 0, it is one kernel launch in one
+ * block: the rows are routed by the block's warps and the block then builds
+ * the maps, as the fused decode routing of onnxruntime PR #33366 (Description
+ * item 1) does; the workspace is then not used and may be NULL.  Otherwise
+ * it is the compact forward plus the three map launches, with the workspace
+ * of router_expert_maps.
+ *
+ * Arguments and outputs: those of router_topk_fwd_compact (no dense
+ * outputs) and router_expert_maps; errors as both.
+ */
+MR_API int router_topk_fwd_maps(const void* logits, mr_dtype dtype, int T, int E, int K,
+                                mr_score_func score_func, int num_groups, int group_topk,
+                                float scaling_factor, const float* expert_bias,
+                                float* topk_weights, int ld_weights, int32_t* topk_indices,
+                                int ld_indices, int32_t* token_expert_indices,
+                                int32_t* expert_first_token_offset,
+                                int32_t* permuted_to_unpermuted,
+                                int32_t* unpermuted_to_permuted, int32_t* permuted_experts,
+                                void* workspace, size_t workspace_bytes, mr_stream_t stream);
+
+/*
  * router_topk_bwd — gradient of the forward's probs with respect to logits.
  *
  * Source: TransformerEngine PR #3012, Backward kernels (pass 1: per-row sums

@@ -335,7 +335,17 @@ bool choose_bwd(int E, int op, BwdConfig* c) {
 
 int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   cudaError_t e;
-  if (c.op == 2) {
+  if (c.op == 3) {
+    if (sf == MR_SOFTMAX)
+      e = dt == MR_F32 ? launch_fwd_maps_softmax_f32(a, c, st)
+                       : launch_fwd_maps_softmax_bf16(a, c, st);
+    else if (sf == MR_SOFTMAX_POST)
+      e = dt == MR_F32 ? launch_fwd_maps_softmaxpost_f32(a, c, st)
+                       : launch_fwd_maps_softmaxpost_bf16(a, c, st);
+    else
+      e = dt == MR_F32 ? launch_fwd_maps_sigmoid_f32(a, c, st)
+                       : launch_fwd_maps_sigmoid_bf16(a, c, st);
+  } else if (c.op == 2) {
     if (sf == MR_SOFTMAX)
       e = dt == MR_F32 ? launch_fwd_compact_softmax_f32(a, c, st)
                        : launch_fwd_compact_softmax_bf16(a, c, st);
@@ -356,21 +366,34 @@ int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStr
   return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
-// The top-K router forward behind router_topk_fwd (op 0: dense outputs) and
-// router_topk_fwd_compact (op 2: compact outputs, dense ones optional);
-// arguments already checked.
+// Expert-map outputs of the fused decode router (op 3).
+struct MapsOut {
+  int32_t* offsets;
+  int32_t* p2u;
+  int32_t* u2p;
+  int32_t* pexp;
+};
+
+// Rows of the fused decode router (op 3): one block of the segment path.
+constexpr int kFusedMapsMaxTokens = 8;
+
+// The top-K router forward behind router_topk_fwd (op 0: dense outputs),
+// router_topk_fwd_compact (op 2: compact outputs, dense ones optional) and
+// the fused decode router_topk_fwd_maps (op 3: op 2 + expert maps, one
+// block); arguments already checked.
 int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, int score_func,
                     int num_groups, int group_topk, float scaling_factor,
                     const float* expert_bias, void* probs, uint8_t* routing_map, float* scores,
                     float* topk_w, long long ld_w, int32_t* topk_i, long long ld_i,
-                    int32_t* tei, mr_stream_t stream) {
+                    int32_t* tei, mr_stream_t stream, const MapsOut* maps = nullptr) {
   auto aligned_or_null = [](const void* p) { return p == nullptr || aligned16(p); };
   const bool grouped = num_groups > 1;
   const bool vec = (E % 4 == 0) && aligned16(logits) && aligned_or_null(probs) &&
                    aligned_or_null(routing_map) && aligned_or_null(scores) &&
                    aligned_or_null(expert_bias);
   const int km = (expert_bias != nullptr || grouped) ? 1 : 0;
-  const bool staged = use_staged(E, dtype, vec);
+  const bool staged = op != 3 && use_staged(E, dtype, vec);
+  if (op == 3 && (!vec || T > kFusedMapsMaxTokens)) return MR_ERR_UNSUPPORTED;
   FwdConfig c{};
   if (!staged && !choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;
@@ -379,8 +402,10 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
   c.extra_smem = (grouped && !staged)
                      ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float)
                      : 0;
-  if (op == 2 && !staged)  // per segment: K selected words and weights
+  if (op >= 2 && !staged)  // per segment: K selected words and weights
     c.extra_smem += static_cast<size_t>(kFwdThreads / c.seg) * MR_MAX_TOPK * 12;
+  if (op == 3)  // the block's expert maps: token masks, offsets, scan slots
+    c.extra_smem += static_cast<size_t>(2 * E + 16) * sizeof(int);
 
   FwdArgs a{};
   a.logits = logits;
@@ -394,6 +419,12 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
   a.tei = tei;
   a.ld_w = ld_w;
   a.ld_i = ld_i;
+  if (maps != nullptr) {
+    a.maps_offsets = maps->offsets;
+    a.maps_p2u = maps->p2u;
+    a.maps_u2p = maps->u2p;
+    a.maps_pexp = maps->pexp;
+  }
   a.T = T; a.E = E; a.K = K;
   a.scaling = scaling_factor;
   a.num_groups = grouped ? num_groups : 0;
@@ -457,6 +488,45 @@ int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, int E, in
   return topk_fwd_launch(2, logits, dtype, T, E, K, score_func, num_groups, group_topk,
                          scaling_factor, expert_bias, probs, routing_map, scores, topk_weights,
                          ld_weights, topk_indices, ld_indices, token_expert_indices, stream);
+}
+
+int router_topk_fwd_maps(const void* logits, mr_dtype dtype, int T, int E, int K,
+                         mr_score_func score_func, int num_groups, int group_topk,
+                         float scaling_factor, const float* expert_bias, float* topk_weights,
+                         int ld_weights, int32_t* topk_indices, int ld_indices,
+                         int32_t* token_expert_indices, int32_t* expert_first_token_offset,
+                         int32_t* permuted_to_unpermuted, int32_t* unpermuted_to_permuted,
+                         int32_t* permuted_experts, void* workspace, size_t workspace_bytes,
+                         mr_stream_t stream) {
+  int rc = check_shape(dtype, T, E, K, score_func);
+  if (rc != MR_OK) return rc;
+  rc = check_groups(E, K, num_groups, group_topk);
+  if (rc != MR_OK) return rc;
+  if (ld_weights < K || ld_indices < K) return MR_ERR_INVALID;
+  if (T == 0) return MR_OK;
+  if (logits == nullptr || topk_weights == nullptr || topk_indices == nullptr ||
+      expert_first_token_offset == nullptr || permuted_to_unpermuted == nullptr ||
+      unpermuted_to_permuted == nullptr || permuted_experts == nullptr)
+    return MR_ERR_INVALID;
+  const MapsOut maps{expert_first_token_offset, permuted_to_unpermuted, unpermuted_to_permuted,
+                     permuted_experts};
+  const bool fused = T <= kFusedMapsMaxTokens && E % 4 == 0 && aligned16(logits) &&
+                     (expert_bias == nullptr || aligned16(expert_bias));
+  if (fused)
+    return topk_fwd_launch(3, logits, dtype, T, E, K, score_func, num_groups, group_topk,
+                           scaling_factor, expert_bias, nullptr, nullptr, nullptr, topk_weights,
+                           ld_weights, topk_indices, ld_indices, token_expert_indices, stream,
+                           &maps);
+  if (workspace == nullptr || workspace_bytes < maps_workspace_bytes(T, E) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+    return MR_ERR_INVALID;
+  rc = topk_fwd_launch(2, logits, dtype, T, E, K, score_func, num_groups, group_topk,
+                       scaling_factor, expert_bias, nullptr, nullptr, nullptr, topk_weights,
+                       ld_weights, topk_indices, ld_indices, token_expert_indices, stream);
+  if (rc != MR_OK) return rc;
+  return launch_expert_maps(topk_indices, ld_indices, T, E, K, expert_first_token_offset,
+                            permuted_to_unpermuted, unpermuted_to_permuted, permuted_experts,
+                            workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,

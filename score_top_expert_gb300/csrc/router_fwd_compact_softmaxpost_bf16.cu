@@ -4,6 +4,6 @@
 
 namespace moe_router {
 cudaError_t launch_fwd_compact_softmaxpost_bf16(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  return launch_fwd<SF_SOFTMAX_POST, DT_BF16, true>(a, c, st);
+  return launch_fwd<SF_SOFTMAX_POST, DT_BF16, 2>(a, c, st);
 }
 }  // namespace moe_router

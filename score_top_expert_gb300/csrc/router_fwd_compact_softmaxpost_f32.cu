@@ -4,6 +4,6 @@
 
 namespace moe_router {
 cudaError_t launch_fwd_compact_softmaxpost_f32(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  return launch_fwd<SF_SOFTMAX_POST, DT_F32, true>(a, c, st);
+  return launch_fwd<SF_SOFTMAX_POST, DT_F32, 2>(a, c, st);
 }
 }  // namespace moe_router

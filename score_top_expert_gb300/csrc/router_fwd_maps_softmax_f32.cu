@@ -1,0 +1,9 @@
+// Instantiations of the fused decode router with expert maps (segment path):
+// softmax score, f32 logits.
+#include "router_launch.cuh"
+
+namespace moe_router {
+cudaError_t launch_fwd_maps_softmax_f32(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
+  return launch_fwd<SF_SOFTMAX, DT_F32, 3>(a, c, st);
+}
+}  // namespace moe_router

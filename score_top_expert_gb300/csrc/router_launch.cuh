@@ -50,13 +50,14 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
   return cudaGetLastError();
 }
 
-// COMPACT instantiates the compact-output router (OP 2) only; the other
-// modes live in separate translation units.
-template <int SF, int DT, int SEG, int NC, bool VEC, bool COMPACT>
+// MODE 0 instantiates the top-K (OP 0) and aux (OP 1) forwards, MODE 2 the
+// compact-output router (OP 2), MODE 3 the fused decode router with expert
+// maps (OP 3); the modes live in separate translation units.
+template <int SF, int DT, int SEG, int NC, bool VEC, int MODE>
 cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  if constexpr (COMPACT) {
-    return c.km == 1 ? launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, 2>(a, c, st)
-                     : launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 2>(a, c, st);
+  if constexpr (MODE >= 2) {
+    return c.km == 1 ? launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, MODE>(a, c, st)
+                     : launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, MODE>(a, c, st);
   } else {
     if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
       if (c.op == 1) return launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, 1>(a, c, st);
@@ -66,15 +67,19 @@ cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
   }
 }
 
-template <int SF, int DT, bool COMPACT = false>
+template <int SF, int DT, int MODE = 0>
 cudaError_t launch_fwd(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   if (!c.vec) {
-    if (c.seg == 32 && c.nc == 18)
-      return launch_fwd_mode<SF, DT, 32, 18, false, COMPACT>(a, c, st);
-    return cudaErrorInvalidConfiguration;
+    if constexpr (MODE == 3) {  // the fused decode router takes aligned rows only
+      return cudaErrorInvalidConfiguration;
+    } else {
+      if (c.seg == 32 && c.nc == 18)
+        return launch_fwd_mode<SF, DT, 32, 18, false, MODE>(a, c, st);
+      return cudaErrorInvalidConfiguration;
+    }
   }
 #define MR_FWD_CASE(S, N) \
-  if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true, COMPACT>(a, c, st);
+  if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true, MODE>(a, c, st);
   MR_FWD_VEC_CONFIGS(MR_FWD_CASE)
 #undef MR_FWD_CASE
   return cudaErrorInvalidConfiguration;
@@ -262,5 +267,19 @@ MR_DECLARE_COMPACT(sigmoid_bf16)
 MR_DECLARE_COMPACT(softmaxpost_f32)
 MR_DECLARE_COMPACT(softmaxpost_bf16)
 #undef MR_DECLARE_COMPACT
+
+// Fused decode router with expert maps (OP 3, segment path, aligned rows).
+cudaError_t launch_fwd_maps_softmax_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_maps_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_maps_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_maps_sigmoid_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_maps_softmaxpost_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
+cudaError_t launch_fwd_maps_softmaxpost_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+
+// Stand-alone expert maps (three launches) and their workspace size.
+size_t maps_workspace_bytes(int T, int E);
+int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, int32_t* offsets,
+                       int32_t* p2u, int32_t* u2p, int32_t* pexp, void* workspace,
+                       cudaStream_t st);
 
 }  // namespace moe_router

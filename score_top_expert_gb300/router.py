@@ -51,10 +51,17 @@ def lib() -> ctypes.CDLL:
         L.router_topk_fwd.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, vp, vp, vp]
         L.router_topk_fwd_compact.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, i, vp, i, vp,
                                               vp, vp, vp, vp]
+        L.router_expert_maps_workspace_bytes.argtypes = [i, i]
+        L.router_expert_maps_workspace_bytes.restype = ctypes.c_size_t
+        L.router_expert_maps.argtypes = [vp, i, i, i, i, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                         vp]
+        L.router_topk_fwd_maps.argtypes = [vp, i, i, i, i, i, i, i, f, vp, vp, i, vp, i, vp, vp,
+                                           vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.router_topk_bwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.router_aux_scores_fwd.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
         L.router_aux_scores_bwd.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
-        for fn in ("router_topk_fwd", "router_topk_fwd_compact", "router_topk_bwd",
+        for fn in ("router_topk_fwd", "router_topk_fwd_compact", "router_topk_fwd_maps",
+                   "router_expert_maps", "router_topk_bwd",
                    "router_aux_scores_fwd",
                    "router_aux_scores_bwd", "moe_router_force_path",
                    "moe_router_force_fwd_lanes", "moe_router_version",
@@ -205,6 +212,90 @@ def router_topk_fwd_compact(logits: torch.Tensor, K: int, score_func: str = "sof
             _ptr(routing_map), _ptr(scores), _stream(dev))
     _check("router_topk_fwd_compact", rc)
     return topk_weights, topk_indices, token_expert_indices, probs, routing_map, scores
+
+
+def _maps_outputs(T, E, K, dev, out):
+    n = T * K
+    names = ("expert_first_token_offset", "permuted_to_unpermuted", "unpermuted_to_permuted",
+             "permuted_experts")
+    shapes = ((E + 1,), (n,), (n,), (n,))
+    out = out or {}
+    return tuple(_out(out.get(nm), sh, torch.int32, dev, nm) for nm, sh in zip(names, shapes))
+
+
+def _workspace(nbytes, workspace, dev):
+    if workspace is None:
+        return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    return workspace
+
+
+def router_expert_maps(topk_indices: torch.Tensor, E: int, *, out=None, workspace=None):
+    """(expert, token)-sorted maps of [T, K] expert choices (int32, unit
+    column stride; a column view of a wider buffer is fine).  Returns
+    (expert_first_token_offset [E+1], permuted_to_unpermuted [T K],
+    unpermuted_to_permuted [T K], permuted_experts [T K]), all int32; the
+    choice (t, k) is the expanded row t + k T.  ``out`` may hold any of the
+    four by name; the workspace is allocated here when not given."""
+    if not topk_indices.is_cuda or topk_indices.dtype != torch.int32 or topk_indices.dim() != 2:
+        raise ValueError("topk_indices must be a CUDA int32 [T, K] tensor")
+    T, K = topk_indices.shape
+    if T > 1 and topk_indices.stride(1) != 1:
+        raise ValueError("topk_indices needs a unit column stride")
+    dev = topk_indices.device
+    ld = topk_indices.stride(0) if T > 0 else K
+    offsets, p2u, u2p, pexp = _maps_outputs(T, int(E), K, dev, out)
+    workspace = _workspace(lib().router_expert_maps_workspace_bytes(T, int(E)), workspace, dev)
+    with torch.cuda.device(dev):
+        rc = lib().router_expert_maps(_ptr(topk_indices), ld, T, int(E), K, _ptr(offsets),
+                                      _ptr(p2u), _ptr(u2p), _ptr(pexp), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(dev))
+    _check("router_expert_maps", rc)
+    return offsets, p2u, u2p, pexp
+
+
+def router_topk_fwd_maps(logits: torch.Tensor, K: int, score_func: str = "softmax",
+                         num_groups: int = 0, group_topk: int = 0, scaling_factor: float = 1.0,
+                         expert_bias: torch.Tensor | None = None, *, topk_weights=None,
+                         topk_indices=None, token_expert_indices=True, out=None,
+                         workspace=None):
+    """Compact router forward plus the expert maps of its choices (one
+    launch for up to 8 aligned tokens).  Returns (topk_weights, topk_indices,
+    token_expert_indices or None, expert_first_token_offset,
+    permuted_to_unpermuted, unpermuted_to_permuted, permuted_experts)."""
+    logits = _as_input(logits, "logits", _DTYPE)
+    T, E = logits.shape
+    dev = logits.device
+    K = int(K)
+    if expert_bias is not None:
+        if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
+                or expert_bias.device != dev:
+            raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
+        expert_bias = expert_bias.contiguous()
+    topk_weights = _rows_out(topk_weights, T, K, torch.float32, dev, "topk_weights")
+    topk_indices = _rows_out(topk_indices, T, K, torch.int32, dev, "topk_indices")
+    if token_expert_indices is True:
+        token_expert_indices = torch.empty((T, K), dtype=torch.int32, device=dev)
+    elif token_expert_indices is False:
+        token_expert_indices = None
+    elif token_expert_indices is not None:
+        token_expert_indices = _out(token_expert_indices, (T, K), torch.int32, dev,
+                                    "token_expert_indices")
+    offsets, p2u, u2p, pexp = _maps_outputs(T, E, K, dev, out)
+    workspace = _workspace(lib().router_expert_maps_workspace_bytes(T, E), workspace, dev)
+    ld_w = topk_weights.stride(0) if T > 0 else K
+    ld_i = topk_indices.stride(0) if T > 0 else K
+    with torch.cuda.device(dev):
+        rc = lib().router_topk_fwd_maps(
+            _ptr(logits), _DTYPE[logits.dtype], T, E, K, _score(score_func), int(num_groups),
+            int(group_topk), float(scaling_factor), _ptr(expert_bias), _ptr(topk_weights), ld_w,
+            _ptr(topk_indices), ld_i, _ptr(token_expert_indices), _ptr(offsets), _ptr(p2u),
+            _ptr(u2p), _ptr(pexp), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(dev))
+    _check("router_topk_fwd_maps", rc)
+    return topk_weights, topk_indices, token_expert_indices, offsets, p2u, u2p, pexp
 
 
 def router_topk_bwd(grad_probs: torch.Tensor, routing_map: torch.Tensor,

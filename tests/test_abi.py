@@ -177,3 +177,28 @@ def test_topk_fwd_compact_rejects(L):
     assert fn(f, 0, 4, 16, 3, 0, 4, 2, c, None, f, 3, f, 3, None, None, None, None, None) == -1
     assert fn(None, 0, 0, 16, 2, 0, 0, 0, c, None, None, 2, None, 2, None, None, None, None,
               None) == 0
+
+
+def test_expert_maps_rejects(L):
+    f, big = FAKE, ctypes.c_size_t(1 << 30)
+    L.router_expert_maps_workspace_bytes.restype = ctypes.c_size_t
+    assert L.router_expert_maps_workspace_bytes(8192, 2304) == (32 + 1) * 2304 * 4
+    assert L.router_expert_maps_workspace_bytes(0, 64) == 0
+    fn = L.router_expert_maps
+    assert fn(f, 4, 10, 64, 8, f, f, f, f, f, big, None) == -1        # ld < K
+    assert fn(f, 8, 10, 64, 65, f, f, f, f, f, big, None) == -1       # K > E
+    assert fn(f, 8, 10, 4000, 8, f, f, f, f, f, big, None) == -2
+    assert fn(f, 8, 10, 64, 8, f, None, f, f, f, big, None) == -1
+    assert fn(f, 8, 10, 64, 8, f, f, f, f, f, ctypes.c_size_t(64), None) == -1
+    assert fn(f, 8, 10, 64, 8, f, f, f, f, ctypes.c_void_p(0x1008), big, None) == -1
+    assert fn(None, 8, 0, 64, 8, None, None, None, None, None, ctypes.c_size_t(0), None) == 0
+    m = L.router_topk_fwd_maps
+    # (logits, dt, T, E, K, sf, ng, gk, c, bias, w, ldw, idx, ldi, tei, off, p2u, u2p, pexp, ws, wsb)
+    assert m(f, 0, 4, 64, 8, 0, 0, 0, 1.0, None, f, 8, f, 8, None, None, f, f, f, None,
+             ctypes.c_size_t(0), None) == -1                          # no offsets
+    assert m(f, 0, 40, 63, 8, 0, 0, 0, 1.0, None, f, 8, f, 8, None, f, f, f, f, None,
+             ctypes.c_size_t(0), None) == -1                          # composed path, no workspace
+    assert m(f, 0, 4, 64, 8, 0, 0, 0, 1.0, None, f, 7, f, 8, None, f, f, f, f, None,
+             ctypes.c_size_t(0), None) == -1
+    assert m(None, 0, 0, 64, 8, 0, 0, 0, 1.0, None, None, 8, None, 8, None, None, None, None,
+             None, None, ctypes.c_size_t(0), None) == 0
