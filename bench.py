@@ -64,6 +64,19 @@ def bytes_per_launch(op: str, T: int, E: int, d: int, sf: str = "softmax",
     raise ValueError(op)
 
 
+def next_row_bytes(op: str, T: int, E: int, K: int, d: int) -> int:
+    """Algorithmic bytes of the compact, maps and aux-loss launches."""
+    if op == "compact_fwd":      # logits in; weights, indices, expanded rows out
+        return T * E * d + T * K * 12
+    if op == "expert_maps":      # indices in; offsets and three [T K] maps out
+        return T * K * 4 + (E + 1) * 4 + 3 * T * K * 4
+    if op == "aux_loss_fwd":     # aux scores and map in; tokens and the loss out
+        return T * E * 5 + E * 4 + 4
+    if op == "aux_loss_bwd":     # tokens and grad in; grad [T, E] out
+        return T * E * 4 + E * 4 + 4
+    raise ValueError(op)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "score_top_expert_gb300", "csrc")
@@ -367,7 +380,10 @@ def gpu_arm(a, world, rank, local):
     }
     if not a.no_extra:
         out["breakdown"] = breakdown(torch, R, stream, flush, dev, peak)
+        out["steady_state"] = steady_state(torch, R, stream, dev, peak, l2)
+        out["next_rows"] = next_rows(torch, R, stream, flush, dev, peak)
         out["decode_us"] = decode_latency(torch, R, stream, dev)
+        out["decode_maps_us"] = decode_latency(torch, R, stream, dev, maps=True)
     out["cpu_baseline"] = cpu_baseline(a.cpu_seconds)
     return out
 
@@ -437,9 +453,116 @@ def breakdown(torch, R, stream, flush, dev, peak):
     return res
 
 
-def decode_latency(torch, R, stream, dev):
+def steady_state(torch, R, stream, dev, peak, l2):
+    """Back-to-back launches: a CUDA graph of R launches of one kernel over N
+    rotating buffer sets whose bytes per launch total more than 3x L2 (no
+    flush; each launch also pays the write-backs its predecessors left in
+    L2), median of 10 replays; and the same for whole steps of the four
+    kernels on the headline workload."""
+    from score_top_expert_gb300.workloads import make_workload
+    res = {"protocol": "CUDA graph of 3N back-to-back launches over N rotating buffer sets "
+                       "(> 3x L2 of bytes per launch), median of 10 replays, no flush"}
+
+    def graph_us(fns, reps_per_fn):
+        g = torch.cuda.CUDAGraph()
+        for fn in fns:
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in fns * reps_per_fn:
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        del g
+        return statistics.median(times) / (len(fns) * reps_per_fn)
+
+    for name in ("t8192_e512_k22", "t8192_e2304_k36"):
+        case, args = make_workload(name)
+        first = Step(R, torch, case, args, dev, "softmax")
+        per_launch = min(first.bytes(n) for n, _ in first.ops())
+        nsets = max(2, -(-3 * l2 // per_launch))
+        steps = [first] + [Step(R, torch, case, args, dev, "softmax") for _ in range(nsets - 1)]
+        row = {"buffer_sets": nsets}
+        for i, (n, _) in enumerate(first.ops()):
+            us = graph_us([st.ops()[i][1] for st in steps], 3)
+            gbs = first.bytes(n) / (us * 1e-6) / 1e9
+            row[n] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+        if name == WORKLOAD:
+            step_fns = [fn for st in steps for _, fn in st.ops()]
+            us = graph_us(step_fns, 3) * len(first.ops())
+            step_bytes = sum(first.bytes(n) for n, _ in first.ops())
+            res["step"] = {"workload": name, "us": round(us, 2),
+                           "gbs": round(step_bytes / (us * 1e-6) / 1e9, 1),
+                           "frac": round(step_bytes / (us * 1e-6) / 1e9 / peak, 3)}
+        res[name] = row
+        del steps, first
+        torch.cuda.empty_cache()
+    return res
+
+
+def next_rows(torch, R, stream, flush, dev, peak):
+    """The compact forward, the expert maps and the aux loss on the benchmark
+    workloads, timed like the headline kernels (L2 flushed before each
+    launch; median of 20)."""
+    from score_top_expert_gb300.workloads import make_workload
+    res = {}
+    for name in ("t8192_e512_k22", "t8192_e2304_k36"):
+        case, args = make_workload(name)
+        T, E, K = case.logits.shape[0], case.logits.shape[1], args["K"]
+        x = torch.from_numpy(case.logits).to(dev)
+        w = torch.empty(T, K, device=dev)
+        idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        tei = torch.empty(T, K, dtype=torch.int32, device=dev)
+        maps_out = {"expert_first_token_offset": torch.empty(E + 1, dtype=torch.int32, device=dev)}
+        for nm in ("permuted_to_unpermuted", "unpermuted_to_permuted", "permuted_experts"):
+            maps_out[nm] = torch.empty(T * K, dtype=torch.int32, device=dev)
+        ws = torch.empty(R.lib().router_expert_maps_workspace_bytes(T, E), dtype=torch.uint8,
+                         device=dev)
+        q, amap, _ = R.router_aux_scores_fwd(x, K, "softmax")
+        loss = torch.empty(1, device=dev)
+        tok = torch.empty(E, dtype=torch.int32, device=dev)
+        lws = torch.empty(max(16, R.lib().router_aux_loss_workspace_bytes(T, E)),
+                          dtype=torch.uint8, device=dev)
+        gl = torch.ones(1, device=dev)
+        gq = torch.empty(T, E, device=dev)
+        ops = [
+            ("compact_fwd", lambda: R.router_topk_fwd_compact(
+                x, K, "softmax", topk_weights=w, topk_indices=idx, token_expert_indices=tei)),
+            ("expert_maps", lambda: R.router_expert_maps(idx, E, out=maps_out, workspace=ws)),
+            ("aux_loss_fwd", lambda: R.router_aux_loss_fwd(
+                q, amap, K, 0.01, loss=loss, tokens_per_expert=tok, workspace=lws)),
+            ("aux_loss_bwd", lambda: R.router_aux_loss_bwd(gl, tok, T, K, 0.01,
+                                                           grad_aux_scores=gq)),
+        ]
+        t = time_ops(torch, stream, flush, ops, 20, 3)
+        row = {}
+        for i, (n, _) in enumerate(ops):
+            med = statistics.median(t[i])
+            b = next_row_bytes(n, T, E, K, 4)
+            gbs = b / (med * 1e-3) / 1e9
+            row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
+                      "frac": round(gbs / peak, 3), "bytes": b}
+        row["expert_maps"]["launches"] = 3
+        res[f"{name}/softmax/f32"] = row
+        del x, q, amap, gq
+        torch.cuda.empty_cache()
+    return res
+
+
+def decode_latency(torch, R, stream, dev, maps=False):
     """Decode sweep: 1, 2, 4 rows x 512 experts, softmax, K in 1..10: device
-    time per launch from a CUDA graph of 100 launches (L2-warm)."""
+    time per launch from a CUDA graph of 100 launches (L2-warm).  With maps:
+    the router with expert maps (one fused launch) instead of the top-K
+    forward."""
     from score_top_expert_gb300.workloads import make_case
     res = {}
     for T in (1, 2, 4):
@@ -448,9 +571,22 @@ def decode_latency(torch, R, stream, dev):
         p = torch.empty(T, 512, device=dev)
         m = torch.empty(T, 512, dtype=torch.bool, device=dev)
         s = torch.empty(T, 512, device=dev)
+        ws = torch.empty(R.lib().router_expert_maps_workspace_bytes(T, 512), dtype=torch.uint8,
+                         device=dev)
         for K in (1, 2, 4, 6, 8, 10):
+            w = torch.empty(T, K, device=dev)
+            idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+            mo = {"expert_first_token_offset": torch.empty(513, dtype=torch.int32, device=dev)}
+            for nm in ("permuted_to_unpermuted", "unpermuted_to_permuted", "permuted_experts"):
+                mo[nm] = torch.empty(T * K, dtype=torch.int32, device=dev)
+
             def launch():
-                R.router_topk_fwd(x, K, "softmax", probs=p, routing_map=m, scores=s)
+                if maps:
+                    R.router_topk_fwd_maps(x, K, "softmax", topk_weights=w, topk_indices=idx,
+                                           token_expert_indices=False, out=mo,
+                                           workspace=ws)
+                else:
+                    R.router_topk_fwd(x, K, "softmax", probs=p, routing_map=m, scores=s)
             launch()
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()

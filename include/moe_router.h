@@ -197,12 +197,12 @@ MR_API int router_expert_maps(const int32_t* topk_indices, int ld_indices, int T
 /*
  * router_topk_fwd_maps — router_topk_fwd_compact followed by
  * router_expert_maps of its indices.  Up to 8 tokens (decode) with 16-byte
- * aligned logits (and bias), E % 4 == 0, it is one kernel launch in one
- * block: the rows are routed by the block's warps and the block then builds
- * the maps, as the fused decode routing of onnxruntime PR #33366 (Description
- * item 1) does; the workspace is then not used and may be NULL.  Otherwise
- * it is the compact forward plus the three map launches, with the workspace
- * of router_expert_maps.
+ * aligned logits (and bias) and E % 4 == 0 (fp32) or E % 8 == 0 (bf16), it is
+ * one kernel launch in one block: the rows are routed by the block's warps
+ * and the block then builds the maps, as the fused decode routing of
+ * onnxruntime PR #33366 (Description item 1) does; the workspace is then not
+ * used and may be NULL.  Otherwise it is the compact forward plus the three
+ * map launches, with the workspace of router_expert_maps.
  *
  * Arguments and outputs: those of router_topk_fwd_compact (no dense
  * outputs) and router_expert_maps; errors as both.
@@ -349,8 +349,9 @@ MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per
  * device synchronisation of cudaFree after the call.
  *
  * The column partials go to a fixed device array inside this library of
- * MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES (1,179,648 bytes: up to
- * MR_AUX_LOSS_NOALLOC_BLOCKS partial rows for E up to MR_MAX_EXPERTS).  Every
+ * MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES (1,180,688 bytes: up to
+ * MR_AUX_LOSS_NOALLOC_BLOCKS partial rows for E up to MR_MAX_EXPERTS, and a
+ * small tail for the reduction's last step).  Every
  * GPU that loads the library holds that array until the process exits.  The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The caller still owns and passes every input and output.
@@ -365,13 +366,15 @@ MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per
  * array's device address, once per device; make that first call before any
  * stream capture begins.  Sharing: every call on a device uses the same
  * array, which keeps the last call's contents (nothing needs clearing: each
- * call writes every partial it reads before reading it).  Calls whose work
+ * call writes every partial it reads before reading it and zeroes its own
+ * completion counter).  Calls whose work
  * overlaps on the GPU — on two streams, or from two host threads — race on
  * the array and give wrong results; order them on one stream or with
  * events.
  */
 #define MR_AUX_LOSS_NOALLOC_BLOCKS 64
-#define MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES ((size_t)MR_AUX_LOSS_NOALLOC_BLOCKS * MR_MAX_EXPERTS * 8u)
+#define MR_AUX_LOSS_NOALLOC_SCRATCH_BYTES \
+  ((size_t)MR_AUX_LOSS_NOALLOC_BLOCKS * MR_MAX_EXPERTS * 8u + 1040u)
 MR_API int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T,
                                        int E, int K, float coeff, float* loss,
                                        int32_t* tokens_per_expert, mr_stream_t stream);
@@ -386,7 +389,8 @@ MR_API const char* moe_router_strerror(int code);
  *   MR_PATH_STAGED: each warp streams rows through shared memory with bulk
  *     copies (no bias, no groups; E % 4 == 0 for fp32, E % 8 == 0 for bf16;
  *     16-byte aligned tensors).
- * MR_PATH_AUTO takes the staged path from E = 256 up where it applies.  A
+ * MR_PATH_AUTO takes the staged path where it applies, except for batches of
+ * 8192 or more tokens with E < 128 (the segment path is faster there).  A
  * forced path that does not apply to a call falls back to the automatic
  * choice.  Process-wide; meant for tests and benchmarks.  The environment
  * variable MOE_ROUTER_FORCE_PATH (auto|segment|staged) sets the initial

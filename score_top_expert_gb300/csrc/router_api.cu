@@ -132,6 +132,16 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km) {
 }
 
 int occupancy_any(int sf, int dt, const StagedPlan& p) {
+  if (p.op == 3) {
+    if (sf == MR_SOFTMAX)
+      return dt == MR_F32 ? occupancy_staged_maps_softmax_f32(p)
+                          : occupancy_staged_maps_softmax_bf16(p);
+    if (sf == MR_SOFTMAX_POST)
+      return dt == MR_F32 ? occupancy_staged_maps_softmaxpost_f32(p)
+                          : occupancy_staged_maps_softmaxpost_bf16(p);
+    return dt == MR_F32 ? occupancy_staged_maps_sigmoid_f32(p)
+                        : occupancy_staged_maps_sigmoid_bf16(p);
+  }
   if (p.op == 2) {
     if (sf == MR_SOFTMAX)
       return dt == MR_F32 ? occupancy_staged_compact_softmax_f32(p)
@@ -173,6 +183,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
   p.layout = staged_layout(p.seg, p.nc, dt, km);
   p.op = op;
   p.km = km;
+  p.tail_bytes = op == 3 ? (2 * E + 16) * 4 : 0;  // the block's expert maps
   const int warp_bytes = (32 / p.seg) * p.layout.seg_bytes;
   int best_warps = 0;
   // tuning override: MOE_ROUTER_STAGED_WARPS caps the resident warps per SM
@@ -182,7 +193,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
     if (v > 0) cap_warps = v;
   }
   for (int w = 1; w <= kStagedMaxWarps; ++w) {
-    const int smem = p.layout.head_bytes + w * warp_bytes;
+    const int smem = p.layout.head_bytes + w * warp_bytes + p.tail_bytes;
     if (smem > di.smem_per_block) break;
     int blocks = di.smem_per_sm / (smem + 1024);
     blocks = blocks < 2048 / (32 * w) ? blocks : 2048 / (32 * w);
@@ -211,13 +222,17 @@ bool staged_shape_ok(int E, int dt) {
   return E % 4 == 0 && (dt == MR_F32 || E % 8 == 0) && E <= 2304;
 }
 
-// The staged path serves rows from 256 experts up unless a path is forced.
-bool use_staged(int E, int dt, bool aligned) {
+// The staged path serves every aligned row shape unless a path is forced,
+// except batches of 8192 or more rows of fewer than 128 experts, where the
+// register-resident segment path measured faster (T = 16384, E = 64:
+// 16.6 us against 18.9 us; at T <= 4096 the staged path is 2 to 4 times
+// faster, its single-row latency being 3 us against 7).
+bool use_staged(int E, int dt, bool aligned, int T) {
   if (!aligned || !staged_shape_ok(E, dt)) return false;
   const int path = current_path();
   if (path == MR_PATH_SEGMENT) return false;
   if (path == MR_PATH_STAGED) return true;
-  return E >= 256;
+  return E >= 128 || T < 8192;
 }
 
 int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStream_t st) {
@@ -225,8 +240,19 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStre
   if (!device_info(&di)) return MR_ERR_CUDA;
   StagedPlan p{};
   if (!staged_plan(di, sf, dt, op, km, a.E, a.K, &p)) return MR_ERR_CUDA;
+  if (op == 3 && a.T > p.warps_per_block * (32 / p.seg)) return MR_ERR_UNSUPPORTED;
   cudaError_t e;
-  if (op == 2) {
+  if (op == 3) {
+    if (sf == MR_SOFTMAX)
+      e = dt == MR_F32 ? launch_staged_maps_softmax_f32(a, p, di.status, st)
+                       : launch_staged_maps_softmax_bf16(a, p, di.status, st);
+    else if (sf == MR_SOFTMAX_POST)
+      e = dt == MR_F32 ? launch_staged_maps_softmaxpost_f32(a, p, di.status, st)
+                       : launch_staged_maps_softmaxpost_bf16(a, p, di.status, st);
+    else
+      e = dt == MR_F32 ? launch_staged_maps_sigmoid_f32(a, p, di.status, st)
+                       : launch_staged_maps_sigmoid_bf16(a, p, di.status, st);
+  } else if (op == 2) {
     if (sf == MR_SOFTMAX)
       e = dt == MR_F32 ? launch_staged_compact_softmax_f32(a, p, di.status, st)
                        : launch_staged_compact_softmax_bf16(a, p, di.status, st);
@@ -335,17 +361,7 @@ bool choose_bwd(int E, int op, BwdConfig* c) {
 
 int launch_fwd_any(int sf, int dt, const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   cudaError_t e;
-  if (c.op == 3) {
-    if (sf == MR_SOFTMAX)
-      e = dt == MR_F32 ? launch_fwd_maps_softmax_f32(a, c, st)
-                       : launch_fwd_maps_softmax_bf16(a, c, st);
-    else if (sf == MR_SOFTMAX_POST)
-      e = dt == MR_F32 ? launch_fwd_maps_softmaxpost_f32(a, c, st)
-                       : launch_fwd_maps_softmaxpost_bf16(a, c, st);
-    else
-      e = dt == MR_F32 ? launch_fwd_maps_sigmoid_f32(a, c, st)
-                       : launch_fwd_maps_sigmoid_bf16(a, c, st);
-  } else if (c.op == 2) {
+  if (c.op == 2) {
     if (sf == MR_SOFTMAX)
       e = dt == MR_F32 ? launch_fwd_compact_softmax_f32(a, c, st)
                        : launch_fwd_compact_softmax_bf16(a, c, st);
@@ -374,13 +390,14 @@ struct MapsOut {
   int32_t* pexp;
 };
 
-// Rows of the fused decode router (op 3): one block of the segment path.
+// Rows of the fused decode router (op 3): one block of the staged path.
 constexpr int kFusedMapsMaxTokens = 8;
 
 // The top-K router forward behind router_topk_fwd (op 0: dense outputs),
 // router_topk_fwd_compact (op 2: compact outputs, dense ones optional) and
-// the fused decode router_topk_fwd_maps (op 3: op 2 + expert maps, one
-// block); arguments already checked.
+// the fused decode router_topk_fwd_maps (op 3: op 2 + expert maps, one block
+// of the staged path; MR_ERR_UNSUPPORTED when the batch does not qualify);
+// arguments already checked.
 int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, int score_func,
                     int num_groups, int group_topk, float scaling_factor,
                     const float* expert_bias, void* probs, uint8_t* routing_map, float* scores,
@@ -392,8 +409,8 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
                    aligned_or_null(routing_map) && aligned_or_null(scores) &&
                    aligned_or_null(expert_bias);
   const int km = (expert_bias != nullptr || grouped) ? 1 : 0;
-  const bool staged = op != 3 && use_staged(E, dtype, vec);
-  if (op == 3 && (!vec || T > kFusedMapsMaxTokens)) return MR_ERR_UNSUPPORTED;
+  const bool staged = op == 3 ? (vec && staged_shape_ok(E, dtype)) : use_staged(E, dtype, vec, T);
+  if (op == 3 && (!staged || T > kFusedMapsMaxTokens)) return MR_ERR_UNSUPPORTED;
   FwdConfig c{};
   if (!staged && !choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = vec;
@@ -402,10 +419,8 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
   c.extra_smem = (grouped && !staged)
                      ? static_cast<size_t>(kFwdThreads / c.seg) * E * sizeof(float)
                      : 0;
-  if (op >= 2 && !staged)  // per segment: K selected words and weights
+  if (op == 2 && !staged)  // per segment: K selected words and weights
     c.extra_smem += static_cast<size_t>(kFwdThreads / c.seg) * MR_MAX_TOPK * 12;
-  if (op == 3)  // the block's expert maps: token masks, offsets, scan slots
-    c.extra_smem += static_cast<size_t>(2 * E + 16) * sizeof(int);
 
   FwdArgs a{};
   a.logits = logits;
@@ -510,13 +525,13 @@ int router_topk_fwd_maps(const void* logits, mr_dtype dtype, int T, int E, int K
     return MR_ERR_INVALID;
   const MapsOut maps{expert_first_token_offset, permuted_to_unpermuted, unpermuted_to_permuted,
                      permuted_experts};
-  const bool fused = T <= kFusedMapsMaxTokens && E % 4 == 0 && aligned16(logits) &&
-                     (expert_bias == nullptr || aligned16(expert_bias));
-  if (fused)
-    return topk_fwd_launch(3, logits, dtype, T, E, K, score_func, num_groups, group_topk,
-                           scaling_factor, expert_bias, nullptr, nullptr, nullptr, topk_weights,
-                           ld_weights, topk_indices, ld_indices, token_expert_indices, stream,
-                           &maps);
+  if (T <= kFusedMapsMaxTokens) {
+    rc = topk_fwd_launch(3, logits, dtype, T, E, K, score_func, num_groups, group_topk,
+                         scaling_factor, expert_bias, nullptr, nullptr, nullptr, topk_weights,
+                         ld_weights, topk_indices, ld_indices, token_expert_indices, stream,
+                         &maps);
+    if (rc != MR_ERR_UNSUPPORTED) return rc;  // else: the composed launches below
+  }
   if (workspace == nullptr || workspace_bytes < maps_workspace_bytes(T, E) ||
       (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
     return MR_ERR_INVALID;
@@ -577,7 +592,7 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.intermediate = intermediate;
   a.T = T; a.E = E; a.K = K;
   a.scaling = 1.0f;
-  if (use_staged(E, dtype, vec))
+  if (use_staged(E, dtype, vec, T))
     return launch_staged_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));
   FwdConfig c{};
   if (!choose_fwd(E, K, vec, &c)) return MR_ERR_UNSUPPORTED;

@@ -37,12 +37,9 @@
 //   rank order (key descending, index ascending) with their probabilities,
 //   and the expanded row k T + t of each; probs, map and scores are written
 //   too where their pointers are set.
-// OP 3: OP 2 for a batch that fits one block (decode), followed by the
-//   (expert, token)-sorted expert maps of the batch, built by the block.
 #pragma once
 
 #include "router_common.cuh"
-#include "router_maps.cuh"
 
 namespace moe_router {
 
@@ -57,10 +54,10 @@ struct FwdArgs {
   int32_t* topk_i;        // OP 2: [T, ld_i] expert indices in rank order
   int32_t* tei;           // OP 2: [T, K] expanded rows k T + t, or null
   long long ld_w, ld_i;   // OP 2: row strides (elements) of topk_w / topk_i
-  int32_t* maps_offsets;  // OP 3: [E+1] first permuted row of each expert
-  int32_t* maps_p2u;      // OP 3: [T K] expanded row of each permuted row
-  int32_t* maps_u2p;      // OP 3: [T K] permuted row of each expanded row
-  int32_t* maps_pexp;     // OP 3: [T K] expert of each permuted row
+  int32_t* maps_offsets;  // staged OP 3: [E+1] first permuted row of each expert
+  int32_t* maps_p2u;      // staged OP 3: [T K] expanded row of each permuted row
+  int32_t* maps_u2p;      // staged OP 3: [T K] permuted row of each expanded row
+  int32_t* maps_pexp;     // staged OP 3: [T K] expert of each permuted row
   int T, E, K;
   int num_groups;         // > 1 only when grouping is on (KM 1)
   int group_topk;
@@ -501,7 +498,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
     if constexpr (KM == 0) return (v[j][u] > tkf) || (v[j][u] == tkf && e <= ti);
     else return (kk[j][u] > tk) || (kk[j][u] == tk && kk[j][u] != 0u && e <= ti);
   };
-  if constexpr (OP >= 2) {
+  if constexpr (OP == 2) {
     // the K selected words and weights, gathered in lane order into the
     // segment's list, then ranked
     unsigned char* extra = reinterpret_cast<unsigned char*>(segs + SEGS_PER_BLOCK);
@@ -528,8 +525,7 @@ router_fwd_seg_kernel(const FwdArgs a) {
         }
     __syncwarp(smask);
     if (active) write_compact_row<SEG>(a, row, li, words, wp);
-    if constexpr (OP == 2)
-      if (a.map == nullptr && a.probs == nullptr && a.scores == nullptr) return;
+    if (a.map == nullptr && a.probs == nullptr && a.scores == nullptr) return;
   }
   const bool dense = OP < 2 || a.map != nullptr || a.probs != nullptr || a.scores != nullptr;
 #pragma unroll
@@ -560,15 +556,6 @@ router_fwd_seg_kernel(const FwdArgs a) {
       store4_f32<VEC>(a.scores, off, e0, E, q);
       if (a.intermediate != nullptr) store4_f32<VEC>(a.intermediate, off, e0, E, s);
     }
-  }
-  if constexpr (OP == 3) {
-    // the whole batch is this block's: its compact indices are written
-    __syncthreads();
-    unsigned char* mp = reinterpret_cast<unsigned char*>(segs + SEGS_PER_BLOCK);
-    if (a.num_groups > 1) mp += static_cast<size_t>(SEGS_PER_BLOCK) * E * sizeof(float);
-    mp += static_cast<size_t>(SEGS_PER_BLOCK) * MR_MAX_TOPK * 12;
-    expert_maps_block<kFwdThreads>(a.topk_i, a.ld_i, a.T, E, K, reinterpret_cast<int*>(mp),
-                                   a.maps_offsets, a.maps_p2u, a.maps_u2p, a.maps_pexp);
   }
 }
 

@@ -35,7 +35,9 @@
 //      the K selected (key, ~index) words into the candidate buffer, rank
 //      them, and write the row's K weights, indices and expanded rows; the
 //      dense outputs follow only where their pointers are set, and the
-//      logits stay in the stage (scores are recomputed, not stored).
+//      logits stay in the stage (scores are recomputed, not stored).  OP 3
+//      (a batch that fits one block: decode) then builds the batch's
+//      (expert, token)-sorted expert maps in the block after the last row.
 // Keying on the logit is exact: softmax and sigmoid are strictly increasing.
 //
 // Key mode KM 1 (top-K with a bias and/or groups): before pass 1 the row's
@@ -49,6 +51,7 @@
 
 #include "router_common.cuh"
 #include "router_fwd.cuh"
+#include "router_maps.cuh"
 #include "router_tma.cuh"
 
 namespace moe_router {
@@ -232,7 +235,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   constexpr bool kSigTopk = (OP != 1 && SF != SF_SOFTMAX);  // probs renormalised over the K
   // scores kept over the fp32 logits (not with compact outputs, which read
   // the logits after pass 4)
-  constexpr bool kStore = (DT == DT_F32 && KM == 0 && OP != 2);
+  constexpr bool kStore = (DT == DT_F32 && KM == 0 && OP < 2);
   constexpr bool kNeedSum = (SF != SF_SIGMOID || OP == 1) && KM == 0;
   constexpr int KDT = KM == 0 ? DT : DT_F32;  // type of the selection keys
   extern __shared__ __align__(128) unsigned char smem[];
@@ -299,6 +302,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   // The loop is uniform over the warp: the segments of a warp process rows
   // in step and meet at full-warp barriers after the copy wait and after the
   // selection, so that their paths reconverge.
+  bool failed = false;     // a bounded wait gave up (OP 3 leaves the loop)
   bool have_spec = false;  // a threshold carried over from the previous row
   float spec_t = 0.0f;
   uint32_t phase = 0;
@@ -317,7 +321,12 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         if (row + nsegs < T) mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
       }
       __syncwarp();
-      return;
+      if constexpr (OP == 3) {  // the block meets once more below
+        failed = true;
+        break;
+      } else {
+        return;
+      }
     }
     if (!active) {  // this segment has no row left; its partner still has one
       __syncwarp();
@@ -693,8 +702,8 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     else if constexpr (SF == SF_SOFTMAX && OP != 1) pf = a.scaling * inv;
     __syncwarp(smask);
 
-    bool dense = true;  // OP 2: dense outputs requested
-    if constexpr (OP == 2) {
+    bool dense = true;  // OP 2, 3: dense outputs requested
+    if constexpr (OP >= 2) {
       // ---- compact outputs: gather the K selected words (lane order), rank ----
       CandMask<NC> sel;  // the lane's selected experts, bit 4 j + u
       sel.clear();
@@ -747,7 +756,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
         }
         const uint32_t bits = (selmask[c >> 3] >> (4 * (c & 7))) & 0xfu;
         const uint32_t mapw = (bits * 0x00204081u) & 0x01010101u;
-        if (OP != 2 || a.map != nullptr)
+        if (OP < 2 || a.map != nullptr)
           __stcs(reinterpret_cast<unsigned int*>(a.map + off + 4 * c), mapw);
         float s[4];
 #pragma unroll
@@ -775,6 +784,15 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     if (li == 0) {
       const int nr = row + 2 * nsegs;
       if (nr < T) bulk_load(stage, src + static_cast<size_t>(nr) * row_bytes, row_bytes, &bars[b]);
+    }
+  }
+  if constexpr (OP == 3) {
+    // the whole batch is this block's (one launch of one block): its compact
+    // indices are written; the maps region follows the segments' slices
+    if (!__syncthreads_or(failed)) {
+      int* maps_smem = reinterpret_cast<int*>(smem + L.head_bytes + spb * L.seg_bytes);
+      expert_maps_block(a.topk_i, a.ld_i, T, E, K, maps_smem, a.maps_offsets, a.maps_p2u,
+                        a.maps_u2p, a.maps_pexp);
     }
   }
 }

@@ -51,11 +51,11 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
 }
 
 // MODE 0 instantiates the top-K (OP 0) and aux (OP 1) forwards, MODE 2 the
-// compact-output router (OP 2), MODE 3 the fused decode router with expert
-// maps (OP 3); the modes live in separate translation units.
+// compact-output router (OP 2); the modes live in separate translation
+// units.
 template <int SF, int DT, int SEG, int NC, bool VEC, int MODE>
 cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
-  if constexpr (MODE >= 2) {
+  if constexpr (MODE == 2) {
     return c.km == 1 ? launch_fwd_inst<SF, DT, SEG, NC, VEC, 1, MODE>(a, c, st)
                      : launch_fwd_inst<SF, DT, SEG, NC, VEC, 0, MODE>(a, c, st);
   } else {
@@ -70,13 +70,8 @@ cudaError_t launch_fwd_mode(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
 template <int SF, int DT, int MODE = 0>
 cudaError_t launch_fwd(const FwdArgs& a, const FwdConfig& c, cudaStream_t st) {
   if (!c.vec) {
-    if constexpr (MODE == 3) {  // the fused decode router takes aligned rows only
-      return cudaErrorInvalidConfiguration;
-    } else {
-      if (c.seg == 32 && c.nc == 18)
-        return launch_fwd_mode<SF, DT, 32, 18, false, MODE>(a, c, st);
-      return cudaErrorInvalidConfiguration;
-    }
+    if (c.seg == 32 && c.nc == 18) return launch_fwd_mode<SF, DT, 32, 18, false, MODE>(a, c, st);
+    return cudaErrorInvalidConfiguration;
   }
 #define MR_FWD_CASE(S, N) \
   if (c.seg == S && c.nc == N) return launch_fwd_mode<SF, DT, S, N, true, MODE>(a, c, st);
@@ -125,6 +120,7 @@ struct StagedPlan {
   int op;
   int km;          // key mode: 0 logits, 1 s + bias (and groups), top-K only
   bool full;       // E == 4 * seg * nc: no padding chunks
+  int tail_bytes;  // after the slices: the block's expert maps (op 3)
 };
 
 // compiled (SEG, NC) pairs of the staged forward
@@ -135,7 +131,8 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
                                cudaStream_t st) {
   auto kern = router_fwd_staged_kernel<SF, DT, SEG, NC, OP, FULL, KM>;
   const size_t smem = p.layout.head_bytes +
-                      static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes;
+                      static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes +
+                      p.tail_bytes;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -172,16 +169,18 @@ int staged_blocks_per_sm(int warps_per_block, size_t smem) {
   return n;
 }
 
-template <int SF, int DT, bool COMPACT = false>
+// MODE 0: top-K (OP 0) and aux (OP 1); MODE 2: compact outputs (OP 2);
+// MODE 3: compact outputs and expert maps of a one-block batch (OP 3).
+template <int SF, int DT, int MODE = 0>
 cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cudaStream_t st) {
 #define MR_STAGED_CASE(S, N)                                                               \
   if (p.seg == S && p.nc == N) {                                                           \
-    if constexpr (COMPACT) {                                                               \
+    if constexpr (MODE >= 2) {                                                             \
       if (p.km == 1)                                                                       \
-        return p.full ? launch_staged_inst<SF, DT, S, N, 2, true, 1>(a, p, status, st)     \
-                      : launch_staged_inst<SF, DT, S, N, 2, false, 1>(a, p, status, st);   \
-      return p.full ? launch_staged_inst<SF, DT, S, N, 2, true, 0>(a, p, status, st)       \
-                    : launch_staged_inst<SF, DT, S, N, 2, false, 0>(a, p, status, st);     \
+        return p.full ? launch_staged_inst<SF, DT, S, N, MODE, true, 1>(a, p, status, st)  \
+                      : launch_staged_inst<SF, DT, S, N, MODE, false, 1>(a, p, status, st);\
+      return p.full ? launch_staged_inst<SF, DT, S, N, MODE, true, 0>(a, p, status, st)    \
+                    : launch_staged_inst<SF, DT, S, N, MODE, false, 0>(a, p, status, st);  \
     } else {                                                                               \
       if constexpr (SF != SF_SOFTMAX_POST) {                                               \
         if (p.op == 1)                                                                     \
@@ -200,19 +199,19 @@ cudaError_t launch_staged(const FwdArgs& a, const StagedPlan& p, int* status, cu
   return cudaErrorInvalidConfiguration;
 }
 
-template <int SF, int DT, bool COMPACT = false>
+template <int SF, int DT, int MODE = 0>
 int staged_occupancy(const StagedPlan& p) {
   const size_t smem = p.layout.head_bytes +
-      static_cast<size_t>(p.warps_per_block) * (32 / p.seg) * p.layout.seg_bytes;
+      static_cast<size_t>(p.warps_per_block) * (32 / p.seg) * p.layout.seg_bytes + p.tail_bytes;
 #define MR_STAGED_OCC(S, N)                                                                \
   if (p.seg == S && p.nc == N) {                                                           \
     const int w = p.warps_per_block;                                                       \
-    if constexpr (COMPACT) {                                                               \
+    if constexpr (MODE >= 2) {                                                             \
       if (p.km == 1)                                                                       \
-        return p.full ? staged_blocks_per_sm<SF, DT, S, N, 2, true, 1>(w, smem)            \
-                      : staged_blocks_per_sm<SF, DT, S, N, 2, false, 1>(w, smem);          \
-      return p.full ? staged_blocks_per_sm<SF, DT, S, N, 2, true, 0>(w, smem)              \
-                    : staged_blocks_per_sm<SF, DT, S, N, 2, false, 0>(w, smem);            \
+        return p.full ? staged_blocks_per_sm<SF, DT, S, N, MODE, true, 1>(w, smem)         \
+                      : staged_blocks_per_sm<SF, DT, S, N, MODE, false, 1>(w, smem);       \
+      return p.full ? staged_blocks_per_sm<SF, DT, S, N, MODE, true, 0>(w, smem)           \
+                    : staged_blocks_per_sm<SF, DT, S, N, MODE, false, 0>(w, smem);         \
     } else {                                                                               \
       if constexpr (SF != SF_SOFTMAX_POST) {                                               \
         if (p.op == 1)                                                                     \
@@ -268,13 +267,18 @@ MR_DECLARE_COMPACT(softmaxpost_f32)
 MR_DECLARE_COMPACT(softmaxpost_bf16)
 #undef MR_DECLARE_COMPACT
 
-// Fused decode router with expert maps (OP 3, segment path, aligned rows).
-cudaError_t launch_fwd_maps_softmax_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
-cudaError_t launch_fwd_maps_softmax_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
-cudaError_t launch_fwd_maps_sigmoid_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
-cudaError_t launch_fwd_maps_sigmoid_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
-cudaError_t launch_fwd_maps_softmaxpost_f32(const FwdArgs&, const FwdConfig&, cudaStream_t);
-cudaError_t launch_fwd_maps_softmaxpost_bf16(const FwdArgs&, const FwdConfig&, cudaStream_t);
+// Fused decode router with expert maps (OP 3, staged path, one block).
+#define MR_DECLARE_MAPS(NAME)                                                          \
+  cudaError_t launch_staged_maps_##NAME(const FwdArgs&, const StagedPlan&, int*,       \
+                                        cudaStream_t);                                 \
+  int occupancy_staged_maps_##NAME(const StagedPlan&);
+MR_DECLARE_MAPS(softmax_f32)
+MR_DECLARE_MAPS(softmax_bf16)
+MR_DECLARE_MAPS(sigmoid_f32)
+MR_DECLARE_MAPS(sigmoid_bf16)
+MR_DECLARE_MAPS(softmaxpost_f32)
+MR_DECLARE_MAPS(softmaxpost_bf16)
+#undef MR_DECLARE_MAPS
 
 // Stand-alone expert maps (three launches) and their workspace size.
 size_t maps_workspace_bytes(int T, int E);

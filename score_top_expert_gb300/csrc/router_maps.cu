@@ -2,15 +2,16 @@
 // kernels).  Declarations and contracts: moe_router.h.
 //
 // Three launches, deterministic (no global atomics):
-//   1  count: a block takes 256 tokens (a warp per 32); every warp builds one
-//      32-bit token mask per expert in shared memory; the block writes its
-//      per-expert counts (popcounts summed over its warps).
-//   2  column prefix: per expert, the counts of the blocks before each block
-//      (in place) and the expert's total.
-//   3  scatter: every block rebuilds its masks, scans the totals into the
-//      expert offsets, and places each choice at
-//        offset[e] + (earlier blocks) + (earlier warps) + (earlier lanes),
-//      the last two from the masks.
+//   1  count: a block takes a tile of 64 tokens (a thread per token and per
+//      quarter of its K choices); it builds one 64-bit token mask per
+//      expert in shared memory and writes its per-expert counts (popcounts).
+//   2  column prefix: per expert (a lane each), the counts of the tiles
+//      before each tile (in place; 8 warps split the tiles, then add the
+//      sums of the warps before them) and the expert's total; the last
+//      block to finish (a counter in the workspace, zeroed by launch 1)
+//      scans the totals into the expert offsets.
+//   3  scatter: every block rebuilds its masks and places each choice at
+//        offset[e] + (earlier tiles) + popcount(mask[e] below its token).
 #include <climits>
 #include <cstddef>
 #include <cstdint>
@@ -21,24 +22,24 @@
 namespace moe_router {
 
 constexpr int kMapsThreads = 256;
-constexpr int kMapsWarps = kMapsThreads / 32;
+constexpr int kMapsTile = 64;                           // tokens per block
+constexpr int kMapsSlots = kMapsThreads / kMapsTile;    // threads per token
 
-__host__ __device__ inline int maps_blocks(int T) { return (T + kMapsThreads - 1) / kMapsThreads; }
+__host__ __device__ inline int maps_blocks(int T) { return (T + kMapsTile - 1) / kMapsTile; }
 
-// Token masks of the block's warps: masks[w * E + e] bit l = token
-// blockIdx.x * 256 + 32 w + l chose expert e.  Entries outside [0, E) are
-// left out.
+// masks[e] bit l: token blockIdx.x * 64 + l chose expert e.  Entries outside
+// [0, E) are left out.
 __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, long long ld, int T,
-                                            int E, int K, uint32_t* masks) {
-  for (int i = threadIdx.x; i < kMapsWarps * E; i += kMapsThreads) masks[i] = 0u;
+                                            int E, int K, unsigned long long* masks) {
+  for (int e = threadIdx.x; e < E; e += kMapsThreads) masks[e] = 0ull;
   __syncthreads();
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kMapsThreads + threadIdx.x;
+  const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
+  const int t = blockIdx.x * kMapsTile + tl;
   if (t < T) {
     const int32_t* row = idx + static_cast<size_t>(t) * ld;
-    for (int k = 0; k < K; ++k) {
+    for (int k = slot; k < K; k += kMapsSlots) {
       const int e = row[k];
-      if (e >= 0 && e < E) atomicOr(&masks[w * E + e], 1u << lane);
+      if (e >= 0 && e < E) atomicOr(&masks[e], 1ull << tl);
     }
   }
   __syncthreads();
@@ -46,77 +47,114 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, lon
 
 __global__ void __launch_bounds__(kMapsThreads)
 maps_count_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, int K,
-                  int* __restrict__ counts) {
+                  int* __restrict__ counts, unsigned int* __restrict__ counter) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* masks = reinterpret_cast<uint32_t*>(smem);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
+  unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
   build_masks(idx, ld, T, E, K, masks);
-  for (int e = threadIdx.x; e < E; e += kMapsThreads) {
-    int c = 0;
-#pragma unroll
-    for (int w = 0; w < kMapsWarps; ++w) c += __popc(masks[w * E + e]);
-    counts[static_cast<size_t>(blockIdx.x) * E + e] = c;
-  }
+  for (int e = threadIdx.x; e < E; e += kMapsThreads)
+    counts[static_cast<size_t>(blockIdx.x) * E + e] = __popcll(masks[e]);
 }
 
 __global__ void __launch_bounds__(kMapsThreads)
-maps_colscan_kernel(int* __restrict__ counts, int nb, int E, int* __restrict__ totals) {
-  const int e = blockIdx.x * kMapsThreads + threadIdx.x;
-  if (e >= E) return;
+maps_colscan_kernel(int* __restrict__ counts, int nb, int E, int* __restrict__ totals,
+                    unsigned int* __restrict__ counter, int32_t* __restrict__ offsets) {
+  constexpr int W = kMapsThreads / 32;
+  constexpr int kBatch = 8;  // loads issued before the stores that depend on them
+  __shared__ int wsum[W][32];
+  __shared__ bool last;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int per = (nb + W - 1) / W;
+  const int b0 = w * per, b1 = min(nb, b0 + per);
   int run = 0;
-#pragma unroll 4
-  for (int b = 0; b < nb; ++b) {
-    const size_t i = static_cast<size_t>(b) * E + e;
-    const int c = counts[i];
-    counts[i] = run;
-    run += c;
+  if (e < E) {
+    for (int b = b0; b < b1; b += kBatch) {
+      int c[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        c[j] = b + j < b1 ? counts[static_cast<size_t>(b + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (b + j < b1) counts[static_cast<size_t>(b + j) * E + e] = run;
+        run += c[j];
+      }
+    }
   }
-  totals[e] = run;
+  wsum[w][lane] = run;
+  __syncthreads();
+  int base = 0;
+  for (int v = 0; v < w; ++v) base += wsum[v][lane];
+  if (e < E) {
+    if (base != 0) {
+      for (int b = b0; b < b1; b += kBatch) {
+        int c[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+          c[j] = b + j < b1 ? counts[static_cast<size_t>(b + j) * E + e] : 0;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+          if (b + j < b1) counts[static_cast<size_t>(b + j) * E + e] = c[j] + base;
+      }
+    }
+    if (w == W - 1) totals[e] = base + run;
+  }
+  // the last block scans the experts' totals into their offsets
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  extern __shared__ __align__(16) unsigned char smem[];
+  int* off = reinterpret_cast<int*>(smem);
+  int* tmp = off + E;
+  for (int i = threadIdx.x; i < E; i += kMapsThreads) off[i] = __ldcg(totals + i);
+  __syncthreads();
+  const int total = block_exclusive_scan(off, E, tmp);
+  for (int i = threadIdx.x; i <= E; i += kMapsThreads) offsets[i] = i < E ? off[i] : total;
 }
 
 __global__ void __launch_bounds__(kMapsThreads)
 maps_scatter_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, int K,
-                    const int* __restrict__ colbase, const int* __restrict__ totals,
-                    int32_t* __restrict__ offsets, int32_t* __restrict__ p2u,
-                    int32_t* __restrict__ u2p, int32_t* __restrict__ pexp) {
+                    const int* __restrict__ colbase, const int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ p2u, int32_t* __restrict__ u2p,
+                    int32_t* __restrict__ pexp) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* masks = reinterpret_cast<uint32_t*>(smem);
-  int* off = reinterpret_cast<int*>(masks + kMapsWarps * E);
-  int* tmp = off + E;
-  for (int e = threadIdx.x; e < E; e += kMapsThreads) off[e] = totals[e];
-  build_masks(idx, ld, T, E, K, masks);  // its barriers also publish off[]
-  const int total = block_exclusive_scan<kMapsThreads>(off, E, tmp);
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e <= E; e += kMapsThreads) offsets[e] = e < E ? off[e] : total;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kMapsThreads + threadIdx.x;
+  unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
+  build_masks(idx, ld, T, E, K, masks);
+  const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
+  const int t = blockIdx.x * kMapsTile + tl;
   if (t >= T) return;
   const int32_t* row = idx + static_cast<size_t>(t) * ld;
   const int* base = colbase + static_cast<size_t>(blockIdx.x) * E;
-  const uint32_t below = (1u << lane) - 1u;
-  for (int k = 0; k < K; ++k) {
+  const unsigned long long below = (1ull << tl) - 1ull;
+  for (int k = slot; k < K; k += kMapsSlots) {
     const int e = row[k];
     const int u = t + k * T;
     if (e < 0 || e >= E) {
       u2p[u] = -1;
       continue;
     }
-    int p = off[e] + base[e] + __popc(masks[w * E + e] & below);
-    for (int v = 0; v < w; ++v) p += __popc(masks[v * E + e]);
+    const int p = offsets[e] + base[e] + __popcll(masks[e] & below);
     p2u[p] = u;
     u2p[u] = p;
     pexp[p] = e;
   }
 }
 
-size_t maps_smem_count(int E) { return static_cast<size_t>(kMapsWarps) * E * 4; }
-size_t maps_smem_scatter(int E) {
-  return static_cast<size_t>(kMapsWarps) * E * 4 + static_cast<size_t>(E) * 4 +
-         (kMapsWarps + 1) * 4;
+size_t maps_smem_count(int E) { return static_cast<size_t>(E) * 8; }
+size_t maps_smem_colscan(int E) {
+  return static_cast<size_t>(E) * 4 + (kMapsThreads / 32 + 1) * 4;
 }
+size_t maps_smem_scatter(int E) { return static_cast<size_t>(E) * 8; }
 
-// workspace: nb rows of E ints (counts, then column prefixes), then E totals
+// workspace: nb rows of E ints (counts, then column prefixes), E totals,
+// and the completion counter
 size_t maps_workspace_bytes(int T, int E) {
-  return (static_cast<size_t>(maps_blocks(T)) + 1) * static_cast<size_t>(E) * 4u;
+  return (static_cast<size_t>(maps_blocks(T)) + 1) * static_cast<size_t>(E) * 4u + 16u;
 }
 
 int maps_check(int T, int E, int K, int ld) {
@@ -133,20 +171,14 @@ int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, in
   const int nb = maps_blocks(T);
   int* counts = static_cast<int*>(workspace);
   int* totals = counts + static_cast<size_t>(nb) * E;
-  const size_t s1 = maps_smem_count(E), s3 = maps_smem_scatter(E);
-  if (s1 > 48 * 1024 && cudaFuncSetAttribute(maps_count_kernel,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(s1)) != cudaSuccess)
-    return MR_ERR_CUDA;
-  if (s3 > 48 * 1024 && cudaFuncSetAttribute(maps_scatter_kernel,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(s3)) != cudaSuccess)
-    return MR_ERR_CUDA;
-  maps_count_kernel<<<nb, kMapsThreads, s1, st>>>(idx, ld, T, E, K, counts);
-  maps_colscan_kernel<<<(E + kMapsThreads - 1) / kMapsThreads, kMapsThreads, 0, st>>>(
-      counts, nb, E, totals);
-  maps_scatter_kernel<<<nb, kMapsThreads, s3, st>>>(idx, ld, T, E, K, counts, totals, offsets,
-                                                    p2u, u2p, pexp);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(totals + E);
+  // shared memory: at most 18 KB (E <= 2304), no opt-in needed
+  maps_count_kernel<<<nb, kMapsThreads, maps_smem_count(E), st>>>(idx, ld, T, E, K, counts,
+                                                                  counter);
+  maps_colscan_kernel<<<(E + 31) / 32, kMapsThreads, maps_smem_colscan(E), st>>>(
+      counts, nb, E, totals, counter, offsets);
+  maps_scatter_kernel<<<nb, kMapsThreads, maps_smem_scatter(E), st>>>(idx, ld, T, E, K, counts,
+                                                                      offsets, p2u, u2p, pexp);
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 

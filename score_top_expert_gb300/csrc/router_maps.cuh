@@ -14,11 +14,12 @@
 namespace moe_router {
 
 // Exclusive prefix sums of v[0..n) in place (shared memory); every thread of
-// the block calls it.  Thread i owns the contiguous run i*per .. i*per+per-1.
-// tmp: THREADS / 32 + 1 ints of shared memory.  Returns the total.
-template <int THREADS>
+// the block (a multiple of 32 threads, at most 1024) calls it.  Thread i owns
+// the contiguous run i*per .. i*per+per-1.  tmp: blockDim.x / 32 + 1 ints of
+// shared memory.  Returns the total.
 __device__ __forceinline__ int block_exclusive_scan(int* v, int n, int* tmp) {
-  const int per = (n + THREADS - 1) / THREADS;
+  const int nthreads = blockDim.x;
+  const int per = (n + nthreads - 1) / nthreads;
   const int b0 = threadIdx.x * per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int local = 0;
@@ -32,8 +33,8 @@ __device__ __forceinline__ int block_exclusive_scan(int* v, int n, int* tmp) {
   }
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
+  const int W = nthreads / 32;
   if (warp == 0) {
-    constexpr int W = THREADS / 32;
     const int w = lane < W ? tmp[lane] : 0;
     int s = w;
 #pragma unroll
@@ -53,15 +54,14 @@ __device__ __forceinline__ int block_exclusive_scan(int* v, int n, int* tmp) {
       run += c;
     }
   }
-  const int total = tmp[THREADS / 32];
+  const int total = tmp[W];
   __syncthreads();
   return total;
 }
 
 // Maps of at most 32 tokens in one block (the fused decode forward).  idx:
 // the block's own compact indices ([T, ld_i], written before a
-// __syncthreads); smem: 2 E + THREADS / 32 + 1 ints.
-template <int THREADS>
+// __syncthreads); smem: 2 E + blockDim.x / 32 + 1 ints.
 __device__ __forceinline__ void expert_maps_block(const int32_t* idx, long long ld_i, int T,
                                                   int E, int K, int* smem, int32_t* offsets,
                                                   int32_t* p2u, int32_t* u2p, int32_t* pexp) {
@@ -69,18 +69,19 @@ __device__ __forceinline__ void expert_maps_block(const int32_t* idx, long long 
   int* off = smem + E;                                 // [E]
   int* tmp = smem + 2 * E;
   const int n = T * K;
-  for (int e = threadIdx.x; e < E; e += THREADS) mask[e] = 0u;
+  const int nthreads = blockDim.x;
+  for (int e = threadIdx.x; e < E; e += nthreads) mask[e] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += THREADS) {
+  for (int i = threadIdx.x; i < n; i += nthreads) {
     const int t = i / K, k = i - t * K;
     atomicOr(&mask[idx[t * ld_i + k]], 1u << t);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += THREADS) off[e] = __popc(mask[e]);
+  for (int e = threadIdx.x; e < E; e += nthreads) off[e] = __popc(mask[e]);
   __syncthreads();
-  const int total = block_exclusive_scan<THREADS>(off, E, tmp);
-  for (int e = threadIdx.x; e <= E; e += THREADS) offsets[e] = e < E ? off[e] : total;
-  for (int i = threadIdx.x; i < n; i += THREADS) {
+  const int total = block_exclusive_scan(off, E, tmp);
+  for (int e = threadIdx.x; e <= E; e += nthreads) offsets[e] = e < E ? off[e] : total;
+  for (int i = threadIdx.x; i < n; i += nthreads) {
     const int t = i / K, k = i - t * K;
     const int e = idx[t * ld_i + k];
     const int p = off[e] + __popc(mask[e] & ((1u << t) - 1u));

@@ -5,9 +5,9 @@
 namespace moe_router {
 cudaError_t launch_staged_compact_softmax_bf16(const FwdArgs& a, const StagedPlan& p, int* status,
                                            cudaStream_t st) {
-  return launch_staged<SF_SOFTMAX, DT_BF16, true>(a, p, status, st);
+  return launch_staged<SF_SOFTMAX, DT_BF16, 2>(a, p, status, st);
 }
 int occupancy_staged_compact_softmax_bf16(const StagedPlan& p) {
-  return staged_occupancy<SF_SOFTMAX, DT_BF16, true>(p);
+  return staged_occupancy<SF_SOFTMAX, DT_BF16, 2>(p);
 }
 }  // namespace moe_router

@@ -136,8 +136,8 @@ def test_selftest_rejects_out_of_range_timeouts(L):
 
 def test_aux_loss_argument_checks(L):
     L.router_aux_loss_workspace_bytes.restype = ctypes.c_size_t
-    assert L.router_aux_loss_workspace_bytes(8192, 2304) == 256 * 2304 * 8
-    assert L.router_aux_loss_workspace_bytes(10, 64) == 10 * 64 * 8
+    assert L.router_aux_loss_workspace_bytes(8192, 2304) == 256 * 2304 * 8 + 1040
+    assert L.router_aux_loss_workspace_bytes(10, 64) == 10 * 64 * 8 + 1040
     assert L.router_aux_loss_workspace_bytes(0, 64) == 0
     f, c = FAKE, ctypes.c_float(0.01)
     big = ctypes.c_size_t(1 << 30)
@@ -182,7 +182,7 @@ def test_topk_fwd_compact_rejects(L):
 def test_expert_maps_rejects(L):
     f, big = FAKE, ctypes.c_size_t(1 << 30)
     L.router_expert_maps_workspace_bytes.restype = ctypes.c_size_t
-    assert L.router_expert_maps_workspace_bytes(8192, 2304) == (32 + 1) * 2304 * 4
+    assert L.router_expert_maps_workspace_bytes(8192, 2304) == (128 + 1) * 2304 * 4 + 16
     assert L.router_expert_maps_workspace_bytes(0, 64) == 0
     fn = L.router_expert_maps
     assert fn(f, 4, 10, 64, 8, f, f, f, f, f, big, None) == -1        # ld < K
