@@ -675,7 +675,9 @@ def reference_arm(a, world, rank):
 
 
 def profile_run(a):
-    """Untimed steps for an ncu capture: every op once per step, no flush."""
+    """Untimed steps for an ncu capture, no flush.  --profile-ops step: the
+    four router ops once per step; next: the compact forward, the expert
+    maps (three kernels), the aux-loss forward (two kernels) and backward."""
     import torch
 
     import score_top_expert_gb300.router as R
@@ -684,12 +686,37 @@ def profile_run(a):
     build.build()
     dev = torch.device("cuda", 0)
     case, args = make_workload(a.profile)
-    st = Step(R, torch, case, args, dev, a.profile_score)
+    if a.profile_ops == "step":
+        st = Step(R, torch, case, args, dev, a.profile_score)
+        ops = [fn for _, fn in st.ops()]
+    else:
+        T, E = case.logits.shape
+        K = args["K"]
+        x = torch.from_numpy(case.logits).to(dev)
+        w = torch.empty(T, K, device=dev)
+        idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        tei = torch.empty(T, K, dtype=torch.int32, device=dev)
+        ws = torch.empty(R.lib().router_expert_maps_workspace_bytes(T, E), dtype=torch.uint8,
+                         device=dev)
+        q, amap, _ = R.router_aux_scores_fwd(x, K, "softmax")
+        lws = torch.empty(R.lib().router_aux_loss_workspace_bytes(T, E), dtype=torch.uint8,
+                          device=dev)
+        loss = torch.empty(1, device=dev)
+        tok = torch.empty(E, dtype=torch.int32, device=dev)
+        gl = torch.ones(1, device=dev)
+        gq = torch.empty(T, E, device=dev)
+        ops = [lambda: R.router_topk_fwd_compact(x, K, "softmax", topk_weights=w,
+                                                 topk_indices=idx, token_expert_indices=tei),
+               lambda: R.router_expert_maps(idx, E, workspace=ws),
+               lambda: R.router_aux_loss_fwd(q, amap, K, 0.01, loss=loss,
+                                             tokens_per_expert=tok, workspace=lws),
+               lambda: R.router_aux_loss_bwd(gl, tok, T, K, 0.01, grad_aux_scores=gq)]
     for _ in range(a.warmup + a.steps):
-        for _, fn in st.ops():
+        for fn in ops:
             fn()
     torch.cuda.synchronize()
-    print(f"profile run done: {a.profile} {a.profile_score}, {a.warmup + a.steps} steps")
+    print(f"profile run done: {a.profile} {a.profile_ops} {a.profile_score}, "
+          f"{a.warmup + a.steps} steps")
 
 
 def main(argv=None):
@@ -706,6 +733,9 @@ def main(argv=None):
                     help="run W + K untimed steps of the four ops on a named workload "
                          "(softmax; for ncu captures) and print nothing else")
     ap.add_argument("--profile-score", default="softmax", choices=("softmax", "sigmoid"))
+    ap.add_argument("--profile-ops", default="step", choices=("step", "next"),
+                    help="with --profile: the four router ops, or the compact forward, "
+                         "expert maps and aux loss")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
