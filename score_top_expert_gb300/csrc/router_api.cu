@@ -109,7 +109,7 @@ void staged_shape(int E, int /*K*/, int* seg, int* nc) {
   *nc = E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18));
 }
 
-StagedLayout staged_layout(int seg, int nc, int dt, int km) {
+StagedLayout staged_layout(int seg, int nc, int dt, int km, int op) {
   StagedLayout L{};
   const int d = dt == MR_F32 ? 4 : 2;
   L.head_bytes = km == 1 ? round_up(4 * seg * nc * 4, 128) : 0;  // the bias row
@@ -125,6 +125,10 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km) {
   off += kCandPerLane * seg * 8;
   L.mask_off = off;
   off += round_up(seg * nc / 2, 16);  // one bit per padded expert
+  if (op >= 2) {  // compact outputs: the K selected words by rank
+    L.sorted_off = off;
+    off += MR_MAX_TOPK * 8;
+  }
   L.bar_off = round_up(off, 16);
   off = L.bar_off + 32;
   L.seg_bytes = round_up(off, 128);
@@ -180,7 +184,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
   StagedPlan p{};
   staged_shape(E, K, &p.seg, &p.nc);
   p.full = E == 4 * p.seg * p.nc;
-  p.layout = staged_layout(p.seg, p.nc, dt, km);
+  p.layout = staged_layout(p.seg, p.nc, dt, km, op);
   p.op = op;
   p.km = km;
   p.tail_bytes = op == 3 ? (2 * E + 16) * 4 : 0;  // the block's expert maps
@@ -273,6 +277,21 @@ int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStre
                      : launch_staged_sigmoid_bf16(a, p, di.status, st);
   }
   return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+}
+
+// Candidate rank whose key becomes the staged forward's next speculative
+// threshold: K - 1 plus a margin (max(K / 2, 4) unless the tuning variable
+// MOE_ROUTER_SPEC_MARGIN gives one).  A larger margin makes the next row's
+// speculation fail less often (fewer than K candidates) but ranks more
+// candidates per row.
+int spec_target(int K) {
+  static const int env_margin = [] {
+    const char* env = std::getenv("MOE_ROUTER_SPEC_MARGIN");
+    const int v = env != nullptr ? std::atoi(env) : -1;
+    return v >= 0 ? v : -1;
+  }();
+  const int margin = env_margin >= 0 ? env_margin : (K / 2 > 4 ? K / 2 : 4);
+  return K - 1 + margin;
 }
 
 int check_shape(int dtype, int T, int E, int K, int sf) {
@@ -441,6 +460,7 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
     a.maps_pexp = maps->pexp;
   }
   a.T = T; a.E = E; a.K = K;
+  a.spec_target = spec_target(K);
   a.scaling = scaling_factor;
   a.num_groups = grouped ? num_groups : 0;
   a.group_topk = grouped ? group_topk : 0;
@@ -591,6 +611,7 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.scores = scores;
   a.intermediate = intermediate;
   a.T = T; a.E = E; a.K = K;
+  a.spec_target = spec_target(K);
   a.scaling = 1.0f;
   if (use_staged(E, dtype, vec, T))
     return launch_staged_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));

@@ -68,6 +68,8 @@ struct FwdArgs {
                           // a power of two <= 32) when groups align with chunks
                           // and per_group <= 4; else 0 (shared-memory scan)
   float inv_group_size;   // 1 / group_size (exact enough for idx < 4096)
+  int spec_target;        // staged path: the candidate rank whose key becomes the
+                          // next row's speculative threshold (>= K - 1)
   float scaling;
 };
 

@@ -66,6 +66,7 @@ struct StagedLayout {
   int grp_off;      // KM 1: group scores and kept flags (32 + 32 words)
   int stage_bytes;  // SEG * NC chunks of 4 logits
   int cand_off;     // kCandPerLane * SEG packed candidate words
+  int sorted_off;   // OP 2, 3: the K selected words by rank (MR_MAX_TOPK words)
   int mask_off;     // selection words, one bit per expert of the padded row
   int bar_off;      // two mbarriers and one 32-bit slot
   int seg_bytes;    // slice size, multiple of 128
@@ -167,18 +168,20 @@ __device__ __forceinline__ void compact_marked(const unsigned char* stage, const
 }
 
 // Rank of each owned candidate among all `total` candidates (NOWN per lane):
-// the K best set their selection bits; the one ranked `target` publishes its
-// key as the next row's threshold; sigmoid rows sum their selected scores.
+// the K best set their selection bits (and, with SORTED, take their place in
+// sorted[rank]); the one ranked `target` publishes its key as the next row's
+// threshold; sigmoid rows sum their selected scores.
 // With TRY32 (fp32 rows, where equal logits are rare) the rank first counts
 // the candidates with a larger 32-bit key (one compare per pair); when keys
 // repeat, the ranks of the tied candidates coincide and no longer sum to
 // 0 + 1 + ... + (total - 1), and the rank is recounted on the full
 // (key, ~index) words, which is what bf16 rows do directly.
-template <int SEG, int NOWN, bool SIG, bool TRY32, class ScoreOf>
+template <int SEG, int NOWN, bool SIG, bool TRY32, bool SORTED, class ScoreOf>
 __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, int total,
                                                 int li, int K, int target, uint32_t* selmask,
                                                 uint32_t* next_key, float& part,
-                                                const ScoreOf& score_of) {
+                                                const ScoreOf& score_of,
+                                                unsigned long long* sorted) {
   const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(cand) + 1;  // keys
   unsigned long long own[NOWN];
   int rank[NOWN];
@@ -214,6 +217,7 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
       if (rank[r] < K) {
         const uint32_t idx = ~static_cast<uint32_t>(own[r]);
         atomicOr(&selmask[idx >> 5], 1u << (idx & 31));
+        if constexpr (SORTED) sorted[rank[r]] = own[r];
         if constexpr (SIG) part += score_of(static_cast<int>(idx), static_cast<uint32_t>(own[r] >> 32));
       }
       if (rank[r] == target) *next_key = static_cast<uint32_t>(own[r] >> 32);
@@ -253,13 +257,15 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   uint32_t* next_key = reinterpret_cast<uint32_t*>(bars + 2);
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(base + L.cand_off);
   uint32_t* selmask = reinterpret_cast<uint32_t*>(base + L.mask_off);
+  unsigned long long* sorted_sel =
+      reinterpret_cast<unsigned long long*>(base + L.sorted_off);  // OP 2, 3
 
   const int E = a.E, K = a.K, T = a.T;
   const int nchunks = E >> 2;
   const uint32_t row_bytes = static_cast<uint32_t>(E) * D;
   const int nsegs = gridDim.x * spb;
   const unsigned char* src = static_cast<const unsigned char*>(a.logits);
-  const int target = K - 1 + (K / 2 > 4 ? K / 2 : 4);  // rank giving the next threshold
+  const int target = a.spec_target;  // rank giving the next row's threshold
 
   // logits (KM 0) or keys (KM 1) of chunk j; padding chunks of a partial
   // row read as -inf
@@ -541,6 +547,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     // ---- 3: exact selection ----------------------------------------------------------
     float part = 0.0f;  // sum of the selected scores (sigmoid top-K)
     bool tie_row = false;
+    bool sorted_row = false;  // OP 2, 3: the K selected words sit in sorted_sel by rank
     float v = row_max;    // tied rows: the K-th largest logit
     int above = 0;        // tied rows: logits > v
     if (!cand_ok) {
@@ -618,16 +625,17 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       const int nown = (total + SEG - 1) / SEG;
       const int tgt = target < total - 1 ? target : total - 1;
       if (nown <= 1)
-        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
+        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
       else if (nown == 2)
-        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
+        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
       else if (nown == 3)
-        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
+        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
       else
-        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32>(cand, total, li, K, tgt, selmask, next_key, part, score_of);
+        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
       __syncwarp(smask);
       spec_t = key_to_float(*next_key);
       have_spec = true;
+      sorted_row = true;
     } else if (tie_row) {
       // need-th lowest index among the logits equal to v: chunks in index
       // order (chunk c covers experts 4c..4c+3), prefix counts across lanes
@@ -704,6 +712,24 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
 
     bool dense = true;  // OP 2, 3: dense outputs requested
     if constexpr (OP >= 2) {
+      if (sorted_row) {
+        // ---- compact outputs, ranks known: the K selected words by rank ----
+        constexpr int kPerLane = (MR_MAX_TOPK + SEG - 1) / SEG;
+        const size_t t = static_cast<size_t>(row);
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+          const int k = r * SEG + li;
+          if (k < K) {
+            const unsigned long long w = sorted_sel[k];
+            const int idx = static_cast<int>(~static_cast<uint32_t>(w));
+            const float x = stage_x1<DT>(stage, idx);
+            const float wt = (SF != SF_SIGMOID) ? exp_shifted(x, max_l2e) : sigmoid_f32(x);
+            a.topk_w[t * a.ld_w + k] = wt * pf;
+            a.topk_i[t * a.ld_i + k] = idx;
+            if (a.tei != nullptr) a.tei[t * K + k] = k * T + row;
+          }
+        }
+      } else {
       // ---- compact outputs: gather the K selected words (lane order), rank ----
       CandMask<NC> sel;  // the lane's selected experts, bit 4 j + u
       sel.clear();
@@ -733,6 +759,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       }
       __syncwarp(smask);
       write_compact_row<SEG>(a, row, li, cand, cand_p);
+      }
       dense = a.map != nullptr || a.probs != nullptr || a.scores != nullptr;
     }
 

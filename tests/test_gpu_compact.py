@@ -60,9 +60,17 @@ def check_compact(R, case, K, sf, c=1.0, ng=0, gk=0, bias=None, strided=False):
         topk_indices=None if i_buf is None else i_buf[:, :K])
     if strided:
         assert (w_buf[:, K:] == -7.0).all() and (i_buf[:, K:] == -9).all()
-    # the dense outputs are those of router_topk_fwd on the same input
+    # the dense outputs are those of router_topk_fwd on the same input: the
+    # map and the scores bit for bit; the renormalised probs up to the order
+    # in which the K selected scores are summed (it follows the candidate
+    # order, which depends on each launch's rows-per-warp plan)
     p0, m0, s0 = R.router_topk_fwd(x, K, sf, ng, gk, c, b)
-    assert torch.equal(probs, p0) and torch.equal(rmap, m0) and torch.equal(scores, s0)
+    assert torch.equal(rmap, m0) and torch.equal(scores, s0)
+    dp = (probs.double() - p0.double()).abs()
+    if dt == "f32":
+        assert dp.max().item() <= F32_ABS
+    else:
+        assert (dp <= 2.0 ** -7 * p0.double().abs()).all()
     # compact and dense agree: the indices are the map's support, the
     # weights its probs (bf16 probs are the weights rounded)
     idx_l = idx.long()
