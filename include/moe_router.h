@@ -314,8 +314,9 @@ MR_API int router_aux_scores_bwd(const float* grad_scores, const float* saved,
  *                    aligned, owned by the caller; its contents need no
  *                    initialisation and are overwritten
  *
- * Two kernels on `stream`; the reduction order is fixed (no atomics), so
- * repeated calls give identical bits.  T == 0 is a no-op (nothing written).
+ * A memset of the workspace's counters and one kernel on `stream`; the
+ * reduction order is fixed (compensated fp32 sums, no floating-point
+ * atomics), so repeated calls give identical bits.  T == 0 is a no-op (nothing written).
  * MR_ERR_INVALID: T < 0, E < 1, K outside [1, E], T*E > INT_MAX, a NULL
  * pointer when T > 0, a workspace too small or misaligned.
  * MR_ERR_UNSUPPORTED: E > MR_MAX_EXPERTS.
@@ -358,8 +359,8 @@ MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per
  *
  * Arguments, layouts, results and errors are those of router_aux_loss_fwd
  * without workspace/workspace_bytes; E beyond what the array holds returns
- * MR_ERR_UNSUPPORTED.  The loss and tokens equal router_aux_loss_fwd's up to
- * the order of fp32 partial sums (fewer, longer partial rows); repeated
+ * MR_ERR_UNSUPPORTED.  The loss and tokens equal router_aux_loss_fwd's bit
+ * for bit (the same kernel, partial rows and summation order); repeated
  * calls on the same inputs give the same bits.
  *
  * Set-up: the first call on a device (that device current) looks up the
@@ -367,7 +368,7 @@ MR_API int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per
  * stream capture begins.  Sharing: every call on a device uses the same
  * array, which keeps the last call's contents (nothing needs clearing: each
  * call writes every partial it reads before reading it and zeroes its own
- * completion counter).  Calls whose work
+ * completion counters).  Calls whose work
  * overlaps on the GPU — on two streams, or from two host threads — race on
  * the array and give wrong results; order them on one stream or with
  * events.

@@ -1,19 +1,17 @@
 // Load-balancing aux loss over the aux-score forward's outputs, and its
 // backward.  Declarations and contracts: moe_router.h.
 //
-// Forward, two launches, deterministic (no floating-point atomics):
-//   1  B blocks split the T rows; each thread owns four consecutive experts
-//      (one float4 of q, four map bytes per row; unaligned rows: experts
-//      e = t, t + 256, ...) and sums q[t, e] and map[t, e] over its block's
-//      rows (coalesced row reads); the block writes its column partials to
-//      the workspace.
-//   2  E / 32 blocks, a lane per expert: the block's 8 warps add the B
-//      partials of its 32 experts (warp w takes partial rows w, w + 8, ...,
-//      coalesced; compensated fp32 sums), combine them in a fixed order,
-//      write tokens_per_expert and the block's share (in double) of
-//        loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e;
-//      the last block to finish (a counter in the workspace, zeroed by
-//      launch 1) adds the shares in block order and writes the loss.
+// Forward: one launch, deterministic (fixed summation orders, compensated
+// fp32 sums, no floating-point atomics).  The grid is B row ranges x G
+// column groups of 128 experts (32 with scalar rows):
+//   1  block (b, g): lane l owns the four experts of chunk 32 g + l, warp w
+//      the rows w, w + 8, ... of range b (eight rows' loads in flight); the
+//      8 warps combine in order and the block writes its partial row;
+//   2  the last block of group g to finish (a counter per group) adds the B
+//      partial rows of its experts, writes tokens_per_expert and the group's
+//      share of  loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e;
+//   3  the last group to finish adds the shares in group order.
+// The counters are zeroed by a memset on the stream before the launch.
 // Backward: grad[t, e] = grad_loss * coeff E / (K T^2) * tokens_e, a pure
 // streaming write (blocks stride over rows, threads over 16-byte chunks).
 #include <atomic>
@@ -28,17 +26,16 @@
 namespace moe_router {
 
 constexpr int kAuxThreads = 256;
-constexpr int kAuxMaxBlocks = 256;
-constexpr int kAuxCols = (MR_MAX_EXPERTS + kAuxThreads - 1) / kAuxThreads;  // per thread
+constexpr int kAuxWarps = kAuxThreads / 32;
+constexpr int kAuxMaxBlocks = 64;  // row ranges (partial rows)
 
 __host__ __device__ inline int aux_blocks(int T) { return T < kAuxMaxBlocks ? T : kAuxMaxBlocks; }
 
 // workspace: B rows of E float partial score sums, then B rows of E int
-// counts, then the final blocks' shares (doubles) and the completion counter
-constexpr int kAuxFinalExperts = 32;  // experts per final block (a lane each)
-constexpr int kAuxShareSlots = 128;   // >= MR_MAX_EXPERTS / kAuxFinalExperts
-constexpr size_t kAuxTailBytes = kAuxShareSlots * sizeof(double) + 16;
-static_assert(kAuxShareSlots * kAuxFinalExperts >= MR_MAX_EXPERTS, "share slots");
+// counts, then the column groups' shares (fp32) and the completion counters
+constexpr int kAuxSlots = 128;  // >= MR_MAX_EXPERTS / 32 + 1
+constexpr size_t kAuxTailBytes = kAuxSlots * sizeof(float) + kAuxSlots * sizeof(int) + 16;
+static_assert(kAuxSlots >= MR_MAX_EXPERTS / 32 + 1, "share and counter slots");
 
 __host__ __device__ inline size_t aux_workspace_bytes(int T, int E) {
   return static_cast<size_t>(aux_blocks(T)) * static_cast<size_t>(E) * 8u + kAuxTailBytes;
@@ -47,87 +44,20 @@ __host__ __device__ inline size_t aux_workspace_bytes(int T, int E) {
 struct AuxScratch {
   float* part_q;
   int* part_n;
-  double* shares;
-  unsigned int* counter;
+  float* shares;            // one per column group
+  unsigned int* counters;   // one per column group, then one for the groups
 };
 
 __host__ __device__ inline AuxScratch aux_scratch(void* base, int nb, int E) {
   AuxScratch s;
   s.part_q = static_cast<float*>(base);
   s.part_n = reinterpret_cast<int*>(s.part_q + static_cast<size_t>(nb) * E);
-  s.shares = reinterpret_cast<double*>(s.part_n + static_cast<size_t>(nb) * E);
-  s.counter = reinterpret_cast<unsigned int*>(s.shares + kAuxShareSlots);
+  s.shares = reinterpret_cast<float*>(s.part_n + static_cast<size_t>(nb) * E);
+  s.counters = reinterpret_cast<unsigned int*>(s.shares + kAuxSlots);
   return s;
 }
 
-__global__ void __launch_bounds__(kAuxThreads)
-aux_loss_partial_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, int T,
-                        int E, int rows_per_block, AuxScratch ws) {
-  const int b = blockIdx.x;
-  if (b == 0 && threadIdx.x == 0) *ws.counter = 0u;
-  const int r0 = b * rows_per_block;
-  const int r1 = min(T, r0 + rows_per_block);
-  float acc_q[kAuxCols];
-  int acc_n[kAuxCols];
-#pragma unroll
-  for (int i = 0; i < kAuxCols; ++i) { acc_q[i] = 0.0f; acc_n[i] = 0; }
-#pragma unroll 2
-  for (int r = r0; r < r1; ++r) {
-    const size_t off = static_cast<size_t>(r) * static_cast<size_t>(E);
-#pragma unroll
-    for (int i = 0; i < kAuxCols; ++i) {
-      const int e = threadIdx.x + kAuxThreads * i;
-      if (e < E) {
-        acc_q[i] += __ldcs(q + off + e);
-        acc_n[i] += __ldcs(map + off + e) != 0;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kAuxCols; ++i) {
-    const int e = threadIdx.x + kAuxThreads * i;
-    if (e < E) {
-      ws.part_q[static_cast<size_t>(b) * E + e] = acc_q[i];
-      ws.part_n[static_cast<size_t>(b) * E + e] = acc_n[i];
-    }
-  }
-}
-
-// Vector form of the partial sums (E % 4 == 0, 16-byte aligned q): thread
-// (blockIdx.y, threadIdx.x) owns the four experts of chunk
-// blockIdx.y * 256 + threadIdx.x and reads one float4 of q and four map
-// bytes per row, eight rows in flight.
-__global__ void __launch_bounds__(kAuxThreads)
-aux_loss_partial_vec_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, int T,
-                            int E, int rows_per_block, AuxScratch ws) {
-  const int b = blockIdx.x;
-  if (b == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ws.counter = 0u;
-  const int c = blockIdx.y * kAuxThreads + threadIdx.x;
-  if (4 * c >= E) return;
-  const int r0 = b * rows_per_block;
-  const int r1 = min(T, r0 + rows_per_block);
-  float4 aq = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
-  const float4* q4 = reinterpret_cast<const float4*>(q);
-  const uint32_t* m4 = reinterpret_cast<const uint32_t*>(map);
-  const size_t stride = static_cast<size_t>(E) >> 2;
-#pragma unroll 8
-  for (int r = r0; r < r1; ++r) {
-    const size_t i = static_cast<size_t>(r) * stride + c;
-    const float4 v = __ldcs(q4 + i);
-    const uint32_t m = __ldcs(m4 + i);
-    aq.x += v.x; aq.y += v.y; aq.z += v.z; aq.w += v.w;
-    n0 += (m & 0xffu) != 0;
-    n1 += (m & 0xff00u) != 0;
-    n2 += (m & 0xff0000u) != 0;
-    n3 += (m & 0xff000000u) != 0;
-  }
-  const size_t o = static_cast<size_t>(b) * E + 4 * c;
-  *reinterpret_cast<float4*>(ws.part_q + o) = aq;
-  *reinterpret_cast<int4*>(ws.part_n + o) = make_int4(n0, n1, n2, n3);
-}
-
-// Compensated (Kahan) fp32 addition: sum + c carries the running total.
+// Compensated (Kahan) fp32 addition: sum - c carries the running total.
 __device__ __forceinline__ void kahan_add(float& sum, float& c, float v) {
   const float y = v - c;
   const float t = sum + y;
@@ -135,68 +65,174 @@ __device__ __forceinline__ void kahan_add(float& sum, float& c, float v) {
   sum = t;
 }
 
-__global__ void __launch_bounds__(kAuxThreads)
-aux_loss_final_kernel(AuxScratch ws, int nblocks, int T, int E, int K, float coeff,
-                      float* __restrict__ loss, int32_t* __restrict__ tokens) {
-  constexpr int W = kAuxThreads / 32;
-  __shared__ float sq[W][32];
-  __shared__ float sc[W][32];
-  __shared__ int sn[W][32];
+// Experts a lane owns: four consecutive ones (VEC: one float4 of q and four
+// map bytes per row) or one.
+template <bool VEC>
+struct AuxLane {
+  static constexpr int N = VEC ? 4 : 1;
+  float q[N], c[N];
+  int n[N];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < N; ++i) { q[i] = 0.0f; c[i] = 0.0f; n[i] = 0; }
+  }
+};
+
+template <bool VEC>
+__device__ __forceinline__ void aux_load(const float* __restrict__ q, const uint8_t* __restrict__ map,
+                                         size_t off, float (&v)[AuxLane<VEC>::N], uint32_t& m) {
+  if constexpr (VEC) {
+    const float4 t = __ldcs(reinterpret_cast<const float4*>(q + off));
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    m = __ldcs(reinterpret_cast<const unsigned int*>(map + off));
+  } else {
+    v[0] = __ldcs(q + off);
+    m = __ldcs(map + off);
+  }
+}
+
+// Four blocks per SM (at most 64 registers a thread): the row phase needs
+// many warps in flight.
+template <bool VEC>
+__global__ void __launch_bounds__(kAuxThreads, 4)
+aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, int T, int E,
+                int rows_per_block, float scale, AuxScratch ws, float* __restrict__ loss,
+                int32_t* __restrict__ tokens) {
+  constexpr int N = AuxLane<VEC>::N;
+  constexpr int kBatch = 8;   // rows whose loads precede any use
+  constexpr int kBatch2 = 4;  // partial rows whose loads precede any use
+  __shared__ float sq[kAuxWarps][32][N];  // per warp: sums (compensation folded in)
+  __shared__ int sn[kAuxWarps][32][N];
   __shared__ bool last;
-  __shared__ double sh[kAuxShareSlots];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int e = blockIdx.x * kAuxFinalExperts + lane;
-  // per expert: the partials of rows w, w + 8, ... (fp32, compensated; the
-  // fp64 pipe of this part is far too narrow for a per-partial double add)
-  float cq = 0.0f, cc = 0.0f;
-  int cn = 0;
-  if (e < E) {
-#pragma unroll 8
-    for (int b = w; b < nblocks; b += W) {
-      kahan_add(cq, cc, ws.part_q[static_cast<size_t>(b) * E + e]);
-      cn += ws.part_n[static_cast<size_t>(b) * E + e];
+  const int b = blockIdx.x, g = blockIdx.y;
+  const int e0 = (g * 32 + lane) * N;  // first expert of the lane
+  const bool mine = e0 < E;
+  const int nb = gridDim.x;
+
+  // ---- 1: this block's rows -------------------------------------------------
+  const int r0 = b * rows_per_block;
+  const int r1 = min(T, r0 + rows_per_block);
+  AuxLane<VEC> acc;
+  acc.zero();
+  if (mine) {
+    for (int r = r0 + w; r < r1; r += kAuxWarps * kBatch) {
+      float v[kBatch][N];
+      uint32_t m[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int rj = r + j * kAuxWarps;
+        if (rj < r1) {
+          aux_load<VEC>(q, map, static_cast<size_t>(rj) * E + e0, v[j], m[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < N; ++i) v[j][i] = 0.0f;
+          m[j] = 0u;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          acc.q[i] += v[j][i];
+          acc.n[i] += ((m[j] >> (8 * i)) & 0xffu) != 0;
+        }
     }
   }
-  sq[w][lane] = cq;
-  sc[w][lane] = cc;
-  sn[w][lane] = cn;
+#pragma unroll
+  for (int i = 0; i < N; ++i) { sq[w][lane][i] = acc.q[i]; sn[w][lane][i] = acc.n[i]; }
+  __syncthreads();
+  if (w == 0 && mine) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      float s = 0.0f, c = 0.0f;
+      int n = 0;
+#pragma unroll
+      for (int v = 0; v < kAuxWarps; ++v) {
+        kahan_add(s, c, sq[v][lane][i]);
+        n += sn[v][lane][i];
+      }
+      const int e = e0 + i;
+      if (e < E) {
+        ws.part_q[static_cast<size_t>(b) * E + e] = s - c;
+        ws.part_n[static_cast<size_t>(b) * E + e] = n;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(&ws.counters[g], 1u) == static_cast<unsigned>(nb) - 1u;
+  }
+  __syncthreads();
+  if (!last) return;
+
+  // ---- 2: the last block of group g adds the partial rows -------------------
+  __threadfence();
+  acc.zero();
+  if (mine) {
+    for (int pb = w; pb < nb; pb += kAuxWarps * kBatch2) {
+      float pq[kBatch2][N];
+      int pn[kBatch2][N];
+#pragma unroll
+      for (int j = 0; j < kBatch2; ++j) {
+        const int bj = pb + j * kAuxWarps;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          const bool ok = bj < nb && e0 + i < E;
+          const size_t o = static_cast<size_t>(bj) * E + e0 + i;
+          pq[j][i] = ok ? __ldcg(ws.part_q + o) : 0.0f;
+          pn[j][i] = ok ? __ldcg(ws.part_n + o) : 0;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch2; ++j)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          kahan_add(acc.q[i], acc.c[i], pq[j][i]);
+          acc.n[i] += pn[j][i];
+        }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    sq[w][lane][i] = acc.q[i] - acc.c[i];
+    sn[w][lane][i] = acc.n[i];
+  }
   __syncthreads();
   if (w == 0) {
-    float colq = 0.0f, colc = 0.0f;
-    int coln = 0;
+    float term = 0.0f;
 #pragma unroll
-    for (int v = 0; v < W; ++v) {
-      kahan_add(colq, colc, sq[v][lane]);
-      kahan_add(colq, colc, -sc[v][lane]);
-      coln += sn[v][lane];
-    }
-    double term = 0.0;
-    if (e < E) {
-      tokens[e] = coln;
-      term = (static_cast<double>(colq) - static_cast<double>(colc)) * static_cast<double>(coln);
+    for (int i = 0; i < N; ++i) {
+      float s = 0.0f, c = 0.0f;
+      int n = 0;
+#pragma unroll
+      for (int v = 0; v < kAuxWarps; ++v) {
+        kahan_add(s, c, sq[v][lane][i]);
+        n += sn[v][lane][i];
+      }
+      const int e = e0 + i;
+      if (e < E) {
+        tokens[e] = n;
+        term += (s - c) * static_cast<float>(n);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
     if (lane == 0) {
-      ws.shares[blockIdx.x] = term;
+      ws.shares[g] = term;
       __threadfence();
-      last = atomicAdd(ws.counter, 1u) == gridDim.x - 1;
+      last = atomicAdd(&ws.counters[gridDim.y], 1u) == gridDim.y - 1u;
     }
   }
   __syncthreads();
-  if (!last) return;
-  // the last block: read every block's share at once, add them in order
-  __threadfence();
-  for (int j = threadIdx.x; j < static_cast<int>(gridDim.x); j += kAuxThreads)
-    sh[j] = __ldcg(ws.shares + j);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double total = 0.0;
-    for (int j = 0; j < static_cast<int>(gridDim.x); ++j) total += sh[j];
-    const double c = static_cast<double>(coeff) * E /
-                     (static_cast<double>(K) * static_cast<double>(T) * static_cast<double>(T));
-    loss[0] = static_cast<float>(c * total);
-    *ws.counter = 0u;
+
+  // ---- 3: the last group adds the shares in order ---------------------------
+  if (last && threadIdx.x == 0) {
+    __threadfence();
+    float total = 0.0f, comp = 0.0f;
+    for (int j = 0; j < static_cast<int>(gridDim.y); ++j) kahan_add(total, comp, __ldcg(ws.shares + j));
+    loss[0] = scale * (total - comp);
   }
 }
 
@@ -231,30 +267,35 @@ int aux_check(int T, int E, int K) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The two forward launches over nb partial rows in the scratch ws.
-int launch_aux_loss(const float* q, const uint8_t* map, int T, int E, int K, float coeff,
-                    float* loss, int32_t* tokens, const AuxScratch& ws, int nb, cudaStream_t st) {
-  const int rows = (T + nb - 1) / nb;
-  // the vector form also needs 16-byte aligned partial rows (E % 4 == 0
-  // keeps every row of the scratch aligned when its base is)
-  if (E % 4 == 0 && aligned16(q) && (reinterpret_cast<uintptr_t>(map) & 3u) == 0 &&
-      aligned16(ws.part_q)) {
-    const dim3 grid(nb, (E / 4 + kAuxThreads - 1) / kAuxThreads);
-    aux_loss_partial_vec_kernel<<<grid, kAuxThreads, 0, st>>>(q, map, T, E, rows, ws);
-  } else {
-    aux_loss_partial_kernel<<<nb, kAuxThreads, 0, st>>>(q, map, T, E, rows, ws);
-  }
-  const int nfinal = (E + kAuxFinalExperts - 1) / kAuxFinalExperts;
-  aux_loss_final_kernel<<<nfinal, kAuxThreads, 0, st>>>(ws, nb, T, E, K, coeff, loss, tokens);
-  return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
-}
-
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
   return n;
+}
+
+// The forward over nb partial rows in the scratch ws: a memset of the
+// completion counters and one launch.
+int launch_aux_loss(const float* q, const uint8_t* map, int T, int E, int K, float coeff,
+                    float* loss, int32_t* tokens, const AuxScratch& ws, int nb, cudaStream_t st) {
+  const int rows = (T + nb - 1) / nb;
+  const bool vec = E % 4 == 0 && aligned16(q) && (reinterpret_cast<uintptr_t>(map) & 3u) == 0;
+  const int per_group = vec ? 128 : 32;
+  const int groups = (E + per_group - 1) / per_group;
+  const float scale = static_cast<float>(static_cast<double>(coeff) * E /
+                                         (static_cast<double>(K) * T * static_cast<double>(T)));
+  if (cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(groups + 1) * sizeof(unsigned int),
+                      st) != cudaSuccess)
+    return MR_ERR_CUDA;
+  const dim3 grid(nb, groups);
+  if (vec)
+    aux_loss_kernel<true><<<grid, kAuxThreads, 0, st>>>(q, map, T, E, rows, scale, ws, loss,
+                                                        tokens);
+  else
+    aux_loss_kernel<false><<<grid, kAuxThreads, 0, st>>>(q, map, T, E, rows, scale, ws, loss,
+                                                         tokens);
+  return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
 }  // namespace
@@ -355,11 +396,11 @@ int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
-// Same two kernels as router_aux_loss_fwd, with at most kNoAllocBlocks
-// partial rows.  Every partial the second kernel reads is written by the
-// first kernel of the same call, which also zeroes the completion counter,
-// so nothing in the scratch has to start at zero and a previous call's
-// contents are never read.
+// The same launch as router_aux_loss_fwd, with at most kNoAllocBlocks
+// partial rows (router_aux_loss_fwd uses the same number).  Every partial the second kernel reads is written by the
+// blocks of the same launch, and the call zeroes the completion counters
+// with a memset first, so nothing in the scratch has to start at zero and a
+// previous call's contents are never read.
 int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T, int E,
                                 int K, float coeff, float* loss, int32_t* tokens_per_expert,
                                 mr_stream_t stream) {

@@ -27,6 +27,20 @@ constexpr int kMapsSlots = kMapsThreads / kMapsTile;    // threads per token
 
 __host__ __device__ inline int maps_blocks(int T) { return (T + kMapsTile - 1) / kMapsTile; }
 
+constexpr int kMapsPerThread = (MR_MAX_TOPK + kMapsSlots - 1) / kMapsSlots;
+
+// The choices k = slot, slot + 4, ... of token t, all loads issued before any
+// use; -1 past K.
+__device__ __forceinline__ void load_choices(const int32_t* __restrict__ idx, long long ld, int t,
+                                             int K, int slot, int (&e)[kMapsPerThread]) {
+  const int32_t* row = idx + static_cast<size_t>(t) * ld;
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j) {
+    const int k = slot + j * kMapsSlots;
+    e[j] = k < K ? row[k] : -1;
+  }
+}
+
 // masks[e] bit l: token blockIdx.x * 64 + l chose expert e.  Entries outside
 // [0, E) are left out.
 __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, long long ld, int T,
@@ -36,11 +50,11 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, lon
   const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
   const int t = blockIdx.x * kMapsTile + tl;
   if (t < T) {
-    const int32_t* row = idx + static_cast<size_t>(t) * ld;
-    for (int k = slot; k < K; k += kMapsSlots) {
-      const int e = row[k];
-      if (e >= 0 && e < E) atomicOr(&masks[e], 1ull << tl);
-    }
+    int e[kMapsPerThread];
+    load_choices(idx, ld, t, K, slot, e);
+#pragma unroll
+    for (int j = 0; j < kMapsPerThread; ++j)
+      if (e[j] >= 0 && e[j] < E) atomicOr(&masks[e[j]], 1ull << tl);
   }
   __syncthreads();
 }
@@ -128,17 +142,27 @@ maps_scatter_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E,
   const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
   const int t = blockIdx.x * kMapsTile + tl;
   if (t >= T) return;
-  const int32_t* row = idx + static_cast<size_t>(t) * ld;
   const int* base = colbase + static_cast<size_t>(blockIdx.x) * E;
   const unsigned long long below = (1ull << tl) - 1ull;
-  for (int k = slot; k < K; k += kMapsSlots) {
-    const int e = row[k];
+  int ch[kMapsPerThread];
+  load_choices(idx, ld, t, K, slot, ch);
+  int pos[kMapsPerThread];
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j) {  // gathers issued before any use
+    const int e = ch[j];
+    pos[j] = (e >= 0 && e < E) ? offsets[e] + base[e] : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j) {
+    const int k = slot + j * kMapsSlots;
+    if (k >= K) break;
+    const int e = ch[j];
     const int u = t + k * T;
-    if (e < 0 || e >= E) {
+    if (pos[j] < 0) {
       u2p[u] = -1;
       continue;
     }
-    const int p = offsets[e] + base[e] + __popcll(masks[e] & below);
+    const int p = pos[j] + __popcll(masks[e] & below);
     p2u[p] = u;
     u2p[u] = p;
     pexp[p] = e;

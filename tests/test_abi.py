@@ -136,7 +136,7 @@ def test_selftest_rejects_out_of_range_timeouts(L):
 
 def test_aux_loss_argument_checks(L):
     L.router_aux_loss_workspace_bytes.restype = ctypes.c_size_t
-    assert L.router_aux_loss_workspace_bytes(8192, 2304) == 256 * 2304 * 8 + 1040
+    assert L.router_aux_loss_workspace_bytes(8192, 2304) == 64 * 2304 * 8 + 1040
     assert L.router_aux_loss_workspace_bytes(10, 64) == 10 * 64 * 8 + 1040
     assert L.router_aux_loss_workspace_bytes(0, 64) == 0
     f, c = FAKE, ctypes.c_float(0.01)
