@@ -428,8 +428,22 @@ def e2e_arm(torch, R, step, stream, reps, world, dev):
             "ms_per_step": round(ms / reps, 4)}
 
 
+def copy_ceiling(torch, stream, flush, dev, nbytes, peak):
+    """A device-to-device copy moving the same bytes as one launch (half read,
+    half written), timed like the router kernels: what a plain copy reaches
+    at this size with the L2 flushed before it."""
+    half = max(nbytes // 2, 16)
+    src = torch.empty(half, dtype=torch.uint8, device=dev)
+    dst = torch.empty(half, dtype=torch.uint8, device=dev)
+    t = time_ops(torch, stream, flush, [("copy", lambda: dst.copy_(src))], 20, 3)
+    med = statistics.median(t[0])
+    gbs = 2 * half / (med * 1e-3) / 1e9
+    return {"us": round(med * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+
+
 def breakdown(torch, R, stream, flush, dev, peak):
-    """Per-kernel effective GB/s on the other benchmark workloads."""
+    """Per-kernel effective GB/s on the other benchmark workloads, with a
+    plain copy of the top-K forward's bytes beside them (copy_ceiling)."""
     from score_top_expert_gb300.workloads import make_workload
     res = {}
     for name, sfs, dts in (("t8192_e512_k22", ("softmax", "sigmoid"), ("f32",)),
@@ -448,6 +462,8 @@ def breakdown(torch, R, stream, flush, dev, peak):
                     gbs = st.bytes(n) / (med * 1e-3) / 1e9
                     row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
                               "frac": round(gbs / peak, 3)}
+                row["copy_ceiling"] = copy_ceiling(torch, stream, flush, dev,
+                                                   st.bytes("topk_fwd"), peak)
                 res[f"{name}/{sf}/{dt}"] = row
                 del st
     return res
