@@ -567,7 +567,7 @@ def next_rows(torch, R, stream, flush, dev, peak):
             gbs = b / (med * 1e-3) / 1e9
             row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
                       "frac": round(gbs / peak, 3), "bytes": b}
-        row["expert_maps"]["launches"] = 3
+        row["expert_maps"]["launches"] = "one cooperative launch (three beyond one wave)"
         res[f"{name}/softmax/f32"] = row
         del x, q, amap, gq
         torch.cuda.empty_cache()

@@ -179,8 +179,10 @@ MR_API int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, in
  * An index outside [0, E) is skipped: its unpermuted_to_permuted entry is -1
  * and it takes no permuted row.
  * workspace: device memory of router_expert_maps_workspace_bytes(T, E)
- * bytes, 16-byte aligned; its contents need no initialisation.  Three
- * kernel launches on the stream, deterministic.
+ * bytes, 16-byte aligned; its contents need no initialisation.  On the
+ * stream: a memset and one cooperative launch when the batch's 64-token
+ * tiles fit on the GPU at once, else three launches; deterministic either
+ * way (identical results).
  *
  * MR_ERR_INVALID: T < 0, E < 1, K < 1, K > E, ld_indices < K, T*E > INT_MAX,
  *   a NULL pointer when T > 0, a small or misaligned workspace.

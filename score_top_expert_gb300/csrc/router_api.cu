@@ -85,6 +85,15 @@ bool device_info(DeviceInfo* out) {
   return true;
 }
 
+}  // namespace
+
+int* moe_router::device_status_word() {
+  DeviceInfo di{};
+  return device_info(&di) ? di.status : nullptr;
+}
+
+namespace {
+
 // ---- staged forward plans, computed once per (device, shape) ----------------
 struct PlanKey {
   int dev, sf, dt, op, km, E, K;

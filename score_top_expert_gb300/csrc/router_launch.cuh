@@ -280,7 +280,12 @@ MR_DECLARE_MAPS(softmaxpost_f32)
 MR_DECLARE_MAPS(softmaxpost_bf16)
 #undef MR_DECLARE_MAPS
 
-// Stand-alone expert maps (three launches) and their workspace size.
+// Device address of the library's status word on the current device
+// (bounded waits that give up record it there); nullptr if unavailable.
+int* device_status_word();
+
+// Stand-alone expert maps (one cooperative launch, or three) and their
+// workspace size.
 size_t maps_workspace_bytes(int T, int E);
 int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, int32_t* offsets,
                        int32_t* p2u, int32_t* u2p, int32_t* pexp, void* workspace,

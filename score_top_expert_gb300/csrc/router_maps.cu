@@ -12,12 +12,18 @@
 //      scans the totals into the expert offsets.
 //   3  scatter: every block rebuilds its masks and places each choice at
 //        offset[e] + (earlier tiles) + popcount(mask[e] below its token).
+// When every tile's block fits on the GPU at once, the three phases run as
+// one cooperative launch instead, separated by a grid barrier (bounded in
+// time like every wait of this library), and the scatter reuses the masks
+// of phase 1 from shared memory.
 #include <climits>
 #include <cstddef>
 #include <cstdint>
 
 #include "moe_router.h"
+#include "router_launch.cuh"
 #include "router_maps.cuh"
+#include "router_tma.cuh"
 
 namespace moe_router {
 
@@ -169,6 +175,158 @@ maps_scatter_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E,
   }
 }
 
+// Grid-wide barrier of a cooperative launch (every block resident): the
+// blocks add their arrivals to a counter zeroed before the launch; barrier
+// number `gen` (1, 2, ...) is passed when the counter reaches gen blocks per
+// block of the grid.  The wait gives up after kWaitLimitNs and records the
+// timeout in the status word; every thread of the block returns the verdict.
+__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int gen, int* status,
+                                             int* verdict) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(count, 1u);
+    const unsigned int target = gen * gridDim.x;
+    int ok = 1;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+      if (v >= target) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(status, kDeviceWaitTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    *verdict = ok;
+  }
+  __syncthreads();
+  return *verdict != 0;
+}
+
+__global__ void __launch_bounds__(kMapsThreads)
+maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, int K,
+                  int* __restrict__ counts, int* __restrict__ totals,
+                  unsigned int* __restrict__ barrier, int* __restrict__ status,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ p2u,
+                  int32_t* __restrict__ u2p, int32_t* __restrict__ pexp) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
+  int* off = reinterpret_cast<int*>(masks + E);
+  int* verdict = off + E;  // the barrier verdict
+  int* tmp = verdict + 4;  // scan slots / per-warp prefix sums (8 x 32 ints)
+  const int nb = gridDim.x;
+
+  // ---- 1: this tile's masks and counts -------------------------------------
+  build_masks(idx, ld, T, E, K, masks);
+  for (int e = threadIdx.x; e < E; e += kMapsThreads)
+    counts[static_cast<size_t>(blockIdx.x) * E + e] = __popcll(masks[e]);
+  if (!grid_barrier(barrier, 1u, status, verdict)) return;
+
+  // ---- 2: column prefixes: blocks take groups of 32 experts (a lane each),
+  //      the 8 warps split the tiles, then add the sums of the warps before
+  //      them (coalesced 128-byte rows, as the stand-alone prefix kernel) ---
+  {
+    constexpr int W = kMapsThreads / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int* wsum = tmp;  // W x 32 ints, past the scan slots (sized in maps_smem_fused)
+    const int per = (nb + W - 1) / W;
+    const int b0 = min(nb, w * per), b1 = min(nb, b0 + per);
+    for (int grp = blockIdx.x; grp * 32 < E; grp += nb) {
+      const int e = grp * 32 + lane;
+      int run = 0;
+      if (e < E) {
+        for (int b = b0; b < b1; b += 4) {
+          int c[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            c[j] = b + j < b1 ? __ldcg(counts + static_cast<size_t>(b + j) * E + e) : 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (b + j < b1) counts[static_cast<size_t>(b + j) * E + e] = run;
+            run += c[j];
+          }
+        }
+      }
+      wsum[w * 32 + lane] = run;
+      __syncthreads();
+      int base = 0;
+      for (int v = 0; v < w; ++v) base += wsum[v * 32 + lane];
+      if (e < E) {
+        if (base != 0)
+          for (int b = b0; b < b1; ++b) counts[static_cast<size_t>(b) * E + e] += base;
+        if (w == W - 1) totals[e] = base + run;
+      }
+      __syncthreads();
+    }
+  }
+  if (!grid_barrier(barrier, 2u, status, verdict)) return;
+
+  // ---- 3: offsets (every block), then this tile's scatter -------------------
+  for (int e = threadIdx.x; e < E; e += kMapsThreads) off[e] = __ldcg(totals + e);
+  __syncthreads();
+  const int total = block_exclusive_scan(off, E, tmp);
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += kMapsThreads) offsets[e] = e < E ? off[e] : total;
+  const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
+  const int t = blockIdx.x * kMapsTile + tl;
+  if (t >= T) return;
+  const int* base = counts + static_cast<size_t>(blockIdx.x) * E;
+  const unsigned long long below = (1ull << tl) - 1ull;
+  int ch[kMapsPerThread];
+  load_choices(idx, ld, t, K, slot, ch);
+  int pos[kMapsPerThread];
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j) {
+    const int e = ch[j];
+    pos[j] = (e >= 0 && e < E) ? off[e] + __ldcg(base + e) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j) {
+    const int k = slot + j * kMapsSlots;
+    if (k >= K) break;
+    const int e = ch[j];
+    const int u = t + k * T;
+    if (pos[j] < 0) {
+      u2p[u] = -1;
+      continue;
+    }
+    const int p = pos[j] + __popcll(masks[e] & below);
+    p2u[p] = u;
+    u2p[u] = p;
+    pexp[p] = e;
+  }
+}
+
+size_t maps_smem_fused(int E) {
+  return static_cast<size_t>(E) * 12 + 16 + (kMapsThreads / 32) * 32 * 4;
+}
+
+// Blocks of the fused kernel that fit on the current device at once (0 if
+// cooperative launches are not available); cached per device and E.
+int maps_fused_capacity(int E) {
+  constexpr int kDevs = 64;
+  static int cache_E[kDevs] = {0};
+  static int cache_n[kDevs] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+  if (cache_E[dev] == E) return cache_n[dev];
+  int coop = 0, sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, maps_fused_kernel, kMapsThreads,
+                                                    maps_smem_fused(E)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  const int n = coop ? per_sm * sms : 0;
+  cache_n[dev] = n;
+  cache_E[dev] = E;
+  return n;
+}
+
 size_t maps_smem_count(int E) { return static_cast<size_t>(E) * 8; }
 size_t maps_smem_colscan(int E) {
   return static_cast<size_t>(E) * 4 + (kMapsThreads / 32 + 1) * 4;
@@ -196,6 +354,17 @@ int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, in
   int* counts = static_cast<int*>(workspace);
   int* totals = counts + static_cast<size_t>(nb) * E;
   unsigned int* counter = reinterpret_cast<unsigned int*>(totals + E);
+  int* status = device_status_word();
+  if (status != nullptr && nb <= maps_fused_capacity(E)) {
+    // one cooperative launch: every tile's block is resident
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), st) != cudaSuccess) return MR_ERR_CUDA;
+    void* args[] = {&idx, &ld, &T, &E, &K, &counts, &totals, &counter, &status,
+                    &offsets, &p2u, &u2p, &pexp};
+    const cudaError_t e = cudaLaunchCooperativeKernel(
+        reinterpret_cast<const void*>(maps_fused_kernel), dim3(nb), dim3(kMapsThreads), args,
+        maps_smem_fused(E), st);
+    return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+  }
   // shared memory: at most 18 KB (E <= 2304), no opt-in needed
   maps_count_kernel<<<nb, kMapsThreads, maps_smem_count(E), st>>>(idx, ld, T, E, K, counts,
                                                                   counter);

@@ -59,6 +59,15 @@ def test_expert_maps_of_given_indices(R, T, E, K):
         assert torch.equal(a, b)
 
 
+def test_expert_maps_beyond_one_wave(R):
+    # 131072 tokens are 2048 tiles of 64: more blocks than fit on the GPU at
+    # once, so the maps take the three-launch path instead of the cooperative
+    # one; both must give the oracle's maps
+    T, E, K = 131072, 64, 2
+    idx = random_indices(T, E, K, seed=31)
+    assert_maps_equal(R.router_expert_maps(torch.from_numpy(idx).to(DEV), E), idx, E)
+
+
 def test_expert_maps_strided_and_invalid(R):
     T, E, K = 300, 64, 6
     idx = random_indices(T, E, K, seed=4)
