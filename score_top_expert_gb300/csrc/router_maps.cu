@@ -19,6 +19,7 @@
 #include <climits>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "moe_router.h"
 #include "router_launch.cuh"
@@ -308,10 +309,12 @@ size_t maps_smem_fused(int E) {
 // cooperative launches are not available); cached per device and E.
 int maps_fused_capacity(int E) {
   constexpr int kDevs = 64;
+  static std::mutex mu;
   static int cache_E[kDevs] = {0};
   static int cache_n[kDevs] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+  std::lock_guard<std::mutex> lock(mu);
   if (cache_E[dev] == E) return cache_n[dev];
   int coop = 0, sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
@@ -363,7 +366,8 @@ int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, in
     const cudaError_t e = cudaLaunchCooperativeKernel(
         reinterpret_cast<const void*>(maps_fused_kernel), dim3(nb), dim3(kMapsThreads), args,
         maps_smem_fused(E), st);
-    return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+    if (e == cudaSuccess) return MR_OK;
+    (void)cudaGetLastError();  // not launched: take the three launches below
   }
   // shared memory: at most 18 KB (E <= 2304), no opt-in needed
   maps_count_kernel<<<nb, kMapsThreads, maps_smem_count(E), st>>>(idx, ld, T, E, K, counts,
