@@ -349,7 +349,7 @@ def gpu_arm(a, world, rank, local):
     dom = max(kern, key=lambda n: kern[n]["avg_us"])
 
     # ---- end to end through the public API with host buffers ----------------
-    e2e = e2e_arm(torch, R, step, stream, max(3, min(a.steps, 20)), world, dev)
+    e2e = e2e_arm(torch, R, step, stream, max(3, min(a.steps, 20)), world, dev, case, args)
 
     if rank != 0:
         return None
@@ -388,44 +388,104 @@ def gpu_arm(a, world, rank, local):
     return out
 
 
-def e2e_arm(torch, R, step, stream, reps, world, dev):
-    """Same step through the public API with host buffers: pinned host inputs
-    copied in, the four router calls, every output copied back, per step."""
+def e2e_arm(torch, R, step, stream, reps, world, dev, case, args):
+    """Same step through the public API with host buffers: every step copies
+    its inputs in from pinned host memory, makes the four router calls and
+    copies every output back.  Reported: steps pipelined over two device
+    buffer sets (inputs of step i+1 in flight while step i computes and step
+    i-1's outputs come back, on three streams ordered by events); beside it
+    the same steps one after another on one stream."""
+    steps = [step, Step(R, torch, case, args, dev, "softmax")]
     hx = step.x.cpu().pin_memory()
     hg = step.g.cpu().pin_memory()
     hgs = step.gs.cpu().pin_memory()
-    outs = [step.probs, step.rmap, step.scores, step.gx, step.q, step.amap, step.agx]
-    if step.inter is not None:
-        outs.append(step.inter)
-    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hg, hgs))
-    d2h = sum(t.numel() * t.element_size() for t in hout)
 
-    def one():
-        step.x.copy_(hx, non_blocking=True)
-        step.g.copy_(hg, non_blocking=True)
-        step.gs.copy_(hgs, non_blocking=True)
-        for _, fn in step.ops():
-            fn()
-        for d, h in zip(outs, hout):
+    def outs_of(st):
+        o = [st.probs, st.rmap, st.scores, st.gx, st.q, st.amap, st.agx]
+        return o + ([st.inter] if st.inter is not None else [])
+
+    houts = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs_of(st)]
+             for st in steps]
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hg, hgs))
+    d2h = sum(t.numel() * t.element_size() for t in houts[0])
+    step_bytes = sum(step.bytes(n) for n, _ in step.ops())
+
+    def copy_in(st):
+        st.x.copy_(hx, non_blocking=True)
+        st.g.copy_(hg, non_blocking=True)
+        st.gs.copy_(hgs, non_blocking=True)
+
+    def copy_out(st, hout):
+        for d, h in zip(outs_of(st), hout):
             h.copy_(d, non_blocking=True)
 
+    # one after another on one stream
+    def serial_one():
+        copy_in(step)
+        for _, fn in step.ops():
+            fn()
+        copy_out(step, houts[0])
+
     for _ in range(2):
-        one()
+        serial_one()
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
-        one()
+        serial_one()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    step_bytes = sum(step.bytes(n) for n, _ in step.ops())
+    serial_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    # pipelined over two buffer sets
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def pipelined(n, first=None, last=None):
+        done_cmp, done_out = [None, None], [None, None]
+        for i in range(n):
+            k = i % 2
+            st = steps[k]
+            with torch.cuda.stream(s_in):
+                if i == 0 and first is not None:
+                    first.record(s_in)
+                if done_cmp[k] is not None:
+                    s_in.wait_event(done_cmp[k])  # step i-2 has read this set's inputs
+                copy_in(st)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in)
+                if done_out[k] is not None:
+                    s_cmp.wait_event(done_out[k])  # step i-2's outputs are back on the host
+                for _, fn in st.ops():
+                    fn()
+                done_cmp[k] = torch.cuda.Event()
+                done_cmp[k].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_cmp[k])
+                copy_out(st, houts[k])
+                done_out[k] = torch.cuda.Event()
+                done_out[k].record(s_out)
+        if last is not None:
+            last.record(s_out)
+
+    pipelined(2)
+    torch.cuda.synchronize()
+    barrier(world)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    pipelined(reps, p0, p1)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
     return {"value": round(world * step_bytes * reps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / reps, 4)}
+            "ms_per_step": round(ms / reps, 4),
+            "pipelined": "two device buffer sets; copies in, router calls and copies out on "
+                         "three streams ordered by events",
+            "serial": {"value": round(world * step_bytes * reps / (serial_ms * 1e-3) / 1e9, 1),
+                       "ms_per_step": round(serial_ms / reps, 4)}}
 
 
 def copy_ceiling(torch, stream, flush, dev, nbytes, peak):
