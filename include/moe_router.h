@@ -390,8 +390,9 @@ MR_API const char* moe_router_strerror(int code);
  *   MR_PATH_SEGMENT: the row of logits lives in the registers of 8, 16 or 32
  *     lanes of a warp (every shape, bias and groups included);
  *   MR_PATH_STAGED: each warp streams rows through shared memory with bulk
- *     copies (no bias, no groups; E % 4 == 0 for fp32, E % 8 == 0 for bf16;
- *     16-byte aligned tensors).
+ *     copies (bias and groups included; E % 4 == 0 for fp32, E % 8 == 0 for
+ *     bf16; 16-byte aligned tensors).  router_topk_fwd_maps's one-launch
+ *     decode form always runs on this path.
  * MR_PATH_AUTO takes the staged path where it applies, except for batches of
  * 8192 or more tokens with E < 128 (the segment path is faster there).  A
  * forced path that does not apply to a call falls back to the automatic

@@ -1,8 +1,8 @@
 // Router forward, shared-memory staged path.
 //
-// A segment of SEG lanes (16 or 32; a warp holds 32 / SEG segments) owns one
-// token row at a time and walks the rows of the batch persistently (row,
-// row + all segments, ...).  Rows arrive in shared memory by one bulk copy
+// A segment of SEG lanes (32 in this build; the code also takes 16, a warp
+// then holding 32 / SEG segments) owns one token row at a time and walks the
+// rows of the batch persistently (row, row + all segments, ...).  Rows arrive in shared memory by one bulk copy
 // each, double-buffered: while the segment works on row r from one stage, the
 // copy of its next row fills the other, so every segment keeps a row in
 // flight without holding it in registers.  Segments only synchronise among

@@ -349,7 +349,9 @@ int maps_check(int T, int E, int K, int ld) {
   return MR_OK;
 }
 
-// The three launches; arguments checked by the caller.
+// The maps on the stream: one cooperative launch when every tile's block
+// fits on the GPU at once, else the three launches; arguments checked by the
+// caller.
 int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, int32_t* offsets,
                        int32_t* p2u, int32_t* u2p, int32_t* pexp, void* workspace,
                        cudaStream_t st) {
