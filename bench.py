@@ -77,12 +77,38 @@ def next_row_bytes(op: str, T: int, E: int, K: int, d: int) -> int:
     raise ValueError(op)
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++/CUDA source without comments and whitespace (string literals
+    kept), so that the hash below moves only when code changes."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "score_top_expert_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
