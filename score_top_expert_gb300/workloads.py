@@ -159,3 +159,12 @@ def make_workload(name: str, *, dtype: str | None = None, T: int | None = None,
                 num_groups=w.get("num_groups", 0), group_topk=w.get("group_topk", 0),
                 score_func=w.get("score_func", "softmax"))
     return case, args
+
+
+def make_device_normals(torch, shape, seed: int, device, sigma: float = 1.0):
+    """Seeded N(0, sigma) fp32 tensor drawn on the device (torch's generator):
+    for batches too large to draw on the host.  Tests hand the oracle the rows
+    they check, copied back from this tensor."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * sigma
