@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kAuxThreads, 4)
 aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, int T, int E,
                 int rows_per_block, float scale, AuxScratch ws, float* __restrict__ loss,
                 int32_t* __restrict__ tokens) {
+  pdl_enter();
   constexpr int N = AuxLane<VEC>::N;
   constexpr int kBatch = 8;   // rows whose loads precede any use
   constexpr int kBatch2 = 4;  // partial rows whose loads precede any use
@@ -240,6 +241,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(256)
 aux_loss_bwd_kernel(const float* __restrict__ grad_loss, const int32_t* __restrict__ tokens,
                     int T, int E, float scale, float* __restrict__ grad) {
+  pdl_enter();
   const float gl = grad_loss[0] * scale;
   for (int row = blockIdx.x; row < T; row += gridDim.x) {
     float* out = grad + static_cast<size_t>(row) * E;
@@ -289,13 +291,12 @@ int launch_aux_loss(const float* q, const uint8_t* map, int T, int E, int K, flo
                       st) != cudaSuccess)
     return MR_ERR_CUDA;
   const dim3 grid(nb, groups);
-  if (vec)
-    aux_loss_kernel<true><<<grid, kAuxThreads, 0, st>>>(q, map, T, E, rows, scale, ws, loss,
-                                                        tokens);
-  else
-    aux_loss_kernel<false><<<grid, kAuxThreads, 0, st>>>(q, map, T, E, rows, scale, ws, loss,
-                                                         tokens);
-  return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+  const cudaError_t e =
+      vec ? launch_kernel(aux_loss_kernel<true>, grid, dim3(kAuxThreads), 0, st, q, map, T, E,
+                          rows, scale, ws, loss, tokens)
+          : launch_kernel(aux_loss_kernel<false>, grid, dim3(kAuxThreads), 0, st, q, map, T, E,
+                          rows, scale, ws, loss, tokens);
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
 }  // namespace
@@ -387,18 +388,19 @@ int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert
   long long blocks = T;
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (vec)
-    aux_loss_bwd_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        grad_loss, tokens_per_expert, T, E, scale, grad_aux_scores);
-  else
-    aux_loss_bwd_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        grad_loss, tokens_per_expert, T, E, scale, grad_aux_scores);
+  const dim3 g(static_cast<unsigned>(blocks));
+  const cudaError_t e =
+      vec ? launch_kernel(aux_loss_bwd_kernel<true>, g, dim3(256), 0, st, grad_loss,
+                          tokens_per_expert, T, E, scale, grad_aux_scores)
+          : launch_kernel(aux_loss_bwd_kernel<false>, g, dim3(256), 0, st, grad_loss,
+                          tokens_per_expert, T, E, scale, grad_aux_scores);
+  if (e != cudaSuccess) return MR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
-// The same launch as router_aux_loss_fwd, with at most kNoAllocBlocks
-// partial rows (router_aux_loss_fwd uses the same number).  Every partial the second kernel reads is written by the
-// blocks of the same launch, and the call zeroes the completion counters
+// The same launch as router_aux_loss_fwd (which uses the same number of
+// partial rows, at most kNoAllocBlocks).  Every partial the launch reads is
+// written by its own blocks, and the call zeroes the completion counters
 // with a memset first, so nothing in the scratch has to start at zero and a
 // previous call's contents are never read.
 int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T, int E,

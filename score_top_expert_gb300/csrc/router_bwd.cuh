@@ -41,6 +41,7 @@ struct BwdShape {
 template <int SF, int DT, int SEG, int W, int NC, bool VEC, int OP>
 __global__ void __launch_bounds__(BwdShape<SEG, W>::THREADS)
 router_bwd_kernel(const BwdArgs a) {
+  pdl_enter();
   using S = BwdShape<SEG, W>;
   constexpr int RL = S::RL;
   static_assert(W == 1 || SEG == 32, "multi-warp rows use whole warps");

@@ -7,9 +7,58 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+#include <cstring>
+#include <utility>
+
 #include "moe_router.h"
 
 namespace moe_router {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every router kernel is launched with
+// programmatic stream serialization (unless MOE_ROUTER_PDL=0), so that its
+// blocks may be scheduled while the previous kernel in the stream drains;
+// each kernel waits in pdl_wait(), before its first global memory access,
+// until that kernel has completed and its writes are visible.  No-op for a
+// plain launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Kernel entry: wait for the previous kernel only.  The next kernel is let
+// in as this one's blocks exit (no early trigger: a persistent kernel's
+// dependents would otherwise sit resident beside it).
+__device__ __forceinline__ void pdl_enter() { pdl_wait(); }
+
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* env = std::getenv("MOE_ROUTER_PDL");
+    return env == nullptr || std::strcmp(env, "0") != 0;
+  }();
+  return on;
+}
+
+// Launch `kern` on `st` (with programmatic stream serialization when
+// enabled); returns the launch status.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // SF_SOFTMAX_POST scores like softmax (over all E) and renormalises the
 // selected probabilities like sigmoid (the softmax of the selected logits).

@@ -221,6 +221,7 @@ __device__ __forceinline__ void group_select(const FwdArgs& a, const float* rowk
 template <int SF, int DT, int SEG, int NC, bool VEC, int KM, int OP>
 __global__ void __launch_bounds__(kFwdThreads)
 router_fwd_seg_kernel(const FwdArgs a) {
+  pdl_enter();
   constexpr int SEGS_PER_BLOCK = kFwdThreads / SEG;
   constexpr int CAP = kCandPerLane * SEG;
   extern __shared__ __align__(16) unsigned char smem_raw[];

@@ -233,6 +233,7 @@ constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18 && KM == 0) 
 template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
 __global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC, KM>()))
 router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
+  pdl_enter();
   constexpr int CAP = kCandPerLane * SEG;
   constexpr int RPW = 32 / SEG;                 // rows (segments) per warp
   constexpr int D = DT == DT_F32 ? 4 : 2;

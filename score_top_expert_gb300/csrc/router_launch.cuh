@@ -46,8 +46,7 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>((a.T + kSegsPerBlock - 1) / kSegsPerBlock);
-  kern<<<grid, kFwdThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(kFwdThreads), smem, st, a);
 }
 
 // MODE 0 instantiates the top-K (OP 0) and aux (OP 1) forwards, MODE 2 the
@@ -84,8 +83,8 @@ template <int SF, int DT, int SEG, int W, int NC, bool VEC, int OP>
 cudaError_t launch_bwd_inst(const BwdArgs& a, cudaStream_t st) {
   using S = BwdShape<SEG, W>;
   const unsigned grid = static_cast<unsigned>((a.T + S::RPB - 1) / S::RPB);
-  router_bwd_kernel<SF, DT, SEG, W, NC, VEC, OP><<<grid, S::THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(router_bwd_kernel<SF, DT, SEG, W, NC, VEC, OP>, dim3(grid),
+                       dim3(S::THREADS), 0, st, a);
 }
 
 template <int SF, int DT>
@@ -150,8 +149,8 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
     blocks = (need + rounds - 1) / rounds;
   }
   const unsigned grid = static_cast<unsigned>(blocks);
-  kern<<<grid, p.warps_per_block * 32, smem, st>>>(a, p.layout, status);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(p.warps_per_block * 32), smem, st, a, p.layout,
+                       status);
 }
 
 // Resident blocks per SM of one staged instantiation (occupancy query).

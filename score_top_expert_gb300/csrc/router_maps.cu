@@ -69,6 +69,7 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, lon
 __global__ void __launch_bounds__(kMapsThreads)
 maps_count_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, int K,
                   int* __restrict__ counts, unsigned int* __restrict__ counter) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
   unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
@@ -80,6 +81,7 @@ maps_count_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, i
 __global__ void __launch_bounds__(kMapsThreads)
 maps_colscan_kernel(int* __restrict__ counts, int nb, int E, int* __restrict__ totals,
                     unsigned int* __restrict__ counter, int32_t* __restrict__ offsets) {
+  pdl_enter();
   constexpr int W = kMapsThreads / 32;
   constexpr int kBatch = 8;  // loads issued before the stores that depend on them
   __shared__ int wsum[W][32];
@@ -143,6 +145,7 @@ maps_scatter_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E,
                     const int* __restrict__ colbase, const int32_t* __restrict__ offsets,
                     int32_t* __restrict__ p2u, int32_t* __restrict__ u2p,
                     int32_t* __restrict__ pexp) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
   build_masks(idx, ld, T, E, K, masks);
@@ -213,6 +216,7 @@ maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, i
                   unsigned int* __restrict__ barrier, int* __restrict__ status,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ p2u,
                   int32_t* __restrict__ u2p, int32_t* __restrict__ pexp) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);
   int* off = reinterpret_cast<int*>(masks + E);
@@ -372,12 +376,16 @@ int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, in
     (void)cudaGetLastError();  // not launched: take the three launches below
   }
   // shared memory: at most 18 KB (E <= 2304), no opt-in needed
-  maps_count_kernel<<<nb, kMapsThreads, maps_smem_count(E), st>>>(idx, ld, T, E, K, counts,
-                                                                  counter);
-  maps_colscan_kernel<<<(E + 31) / 32, kMapsThreads, maps_smem_colscan(E), st>>>(
-      counts, nb, E, totals, counter, offsets);
-  maps_scatter_kernel<<<nb, kMapsThreads, maps_smem_scatter(E), st>>>(idx, ld, T, E, K, counts,
-                                                                      offsets, p2u, u2p, pexp);
+  cudaError_t e = launch_kernel(maps_count_kernel, dim3(nb), dim3(kMapsThreads),
+                                maps_smem_count(E), st, idx, ld, T, E, K, counts, counter);
+  if (e == cudaSuccess)
+    e = launch_kernel(maps_colscan_kernel, dim3((E + 31) / 32), dim3(kMapsThreads),
+                      maps_smem_colscan(E), st, counts, nb, E, totals, counter, offsets);
+  if (e == cudaSuccess)
+    e = launch_kernel(maps_scatter_kernel, dim3(nb), dim3(kMapsThreads), maps_smem_scatter(E),
+                      st, idx, ld, T, E, K, static_cast<const int*>(counts),
+                      static_cast<const int32_t*>(offsets), p2u, u2p, pexp);
+  if (e != cudaSuccess) return MR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
