@@ -83,3 +83,40 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
                        timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_next_row_byte_accounting():
+    T, E, K = 8192, 2304, 36
+    assert bench.next_row_bytes("compact_fwd", T, E, K, 4) == T * E * 4 + T * K * 12
+    assert bench.next_row_bytes("expert_maps", T, E, K, 4) == T * K * 16 + (E + 1) * 4
+    assert bench.next_row_bytes("aux_loss_fwd", T, E, K, 4) == T * E * 5 + E * 4 + 4
+    assert bench.next_row_bytes("aux_loss_bwd", T, E, K, 4) == T * E * 4 + E * 4 + 4
+    with pytest.raises(ValueError):
+        bench.next_row_bytes("nope", T, E, K, 4)
+
+
+def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    csrc = tmp_path / "score_top_expert_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = 'int f(int a) { return a / 2; }  // halve\n/* block */ const char* s = "//x /*y*/";\n'
+    (csrc / "k.cu").write_text(src)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (csrc / "k.cu").write_text("// a new comment\n" + src.replace("// halve", "// half of a"))
+    assert bench.kernel_source_hash() == h0
+    (csrc / "k.cu").write_text(src.replace("a / 2", "a / 3"))
+    assert bench.kernel_source_hash() != h0
+    (csrc / "k.cu").write_text(src.replace('"//x /*y*/"', '"//x"'))
+    assert bench.kernel_source_hash() != h0  # string literals are code
+
+
+def test_traffic_needs_a_matching_hash(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.json"
+    f.write_text('{"kernel_source_hash": "0000", "kernels": {"topk_fwd@w": '
+                 '{"dram_bytes_per_launch": 5}}}')
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0000")
+    assert bench.traffic_for("topk_fwd", "w") == 5
+    assert bench.traffic_for("aux_fwd", "w") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "1111")
+    assert bench.traffic_for("topk_fwd", "w") is None
