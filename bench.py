@@ -409,6 +409,7 @@ def gpu_arm(a, world, rank, local):
         out["steady_state"] = steady_state(torch, R, stream, dev, peak, l2)
         out["next_rows"] = next_rows(torch, R, stream, flush, dev, peak)
         out["decode_us"] = decode_latency(torch, R, stream, dev)
+        out["decode_eager_us"] = decode_eager(torch, R, stream, dev)
         out["decode_maps_us"] = decode_latency(torch, R, stream, dev, maps=True)
     out["cpu_baseline"] = cpu_baseline(a.cpu_seconds)
     return out
@@ -657,6 +658,29 @@ def next_rows(torch, R, stream, flush, dev, peak):
         res[f"{name}/softmax/f32"] = row
         del x, q, amap, gq
         torch.cuda.empty_cache()
+    return res
+
+
+def decode_eager(torch, R, stream, dev):
+    """Decode latency per call including launch overhead: 200 calls of the
+    top-K forward through the Python binding, one after another on the
+    stream without a graph (1, 2, 4 rows x 512 experts, K = 8, softmax)."""
+    from score_top_expert_gb300.workloads import make_case
+    res = {}
+    for T in (1, 2, 4):
+        case = make_case(T, 512, 8, seed=77 + T)
+        x = torch.from_numpy(case.logits).to(dev)
+        p = torch.empty(T, 512, device=dev)
+        m = torch.empty(T, 512, dtype=torch.bool, device=dev)
+        s = torch.empty(T, 512, device=dev)
+        for _ in range(20):
+            R.router_topk_fwd(x, 8, "softmax", probs=p, routing_map=m, scores=s)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(200):
+            R.router_topk_fwd(x, 8, "softmax", probs=p, routing_map=m, scores=s)
+        torch.cuda.synchronize()
+        res[f"T{T}_K8"] = round((time.perf_counter() - t0) / 200 * 1e6, 2)
     return res
 
 

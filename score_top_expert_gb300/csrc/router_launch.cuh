@@ -4,11 +4,36 @@
 // instantiations compile in parallel.
 #pragma once
 
+#include <atomic>
+
 #include "router_bwd.cuh"
 #include "router_fwd.cuh"
 #include "router_fwd_staged.cuh"
 
 namespace moe_router {
+
+// Allow `kern` the dynamic shared memory `smem` (above the 48 KB default
+// only), once per device and size: `granted` is the calling launcher's own
+// record (one per kernel instantiation), the largest size set per device.
+constexpr int kSmemDevs = 64;
+template <typename Kern>
+cudaError_t allow_smem(Kern kern, size_t smem, std::atomic<int>* granted) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const bool cached = dev >= 0 && dev < kSmemDevs;
+  if (cached && granted[dev].load(std::memory_order_relaxed) >= static_cast<int>(smem))
+    return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && cached) {
+    int cur = granted[dev].load(std::memory_order_relaxed);
+    while (cur < static_cast<int>(smem) &&
+           !granted[dev].compare_exchange_weak(cur, static_cast<int>(smem))) {
+    }
+  }
+  return e;
+}
 
 // Forward configuration chosen by the C ABI layer.
 struct FwdConfig {
@@ -40,11 +65,9 @@ cudaError_t launch_fwd_inst(const FwdArgs& a, const FwdConfig& c, cudaStream_t s
   auto kern = router_fwd_seg_kernel<SF, DT, SEG, NC, VEC, KM, OP>;
   constexpr int kSegsPerBlock = kFwdThreads / SEG;
   const size_t smem = fwd_smem_bytes_static<SEG>() + c.extra_smem;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  static std::atomic<int> granted[kSmemDevs];  // this kernel's record
+  const cudaError_t se = allow_smem(kern, smem, granted);
+  if (se != cudaSuccess) return se;
   const unsigned grid = static_cast<unsigned>((a.T + kSegsPerBlock - 1) / kSegsPerBlock);
   return launch_kernel(kern, dim3(grid), dim3(kFwdThreads), smem, st, a);
 }
@@ -132,11 +155,9 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
   const size_t smem = p.layout.head_bytes +
                       static_cast<size_t>(p.warps_per_block) * (32 / SEG) * p.layout.seg_bytes +
                       p.tail_bytes;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  static std::atomic<int> granted[kSmemDevs];  // this kernel's record
+  const cudaError_t se = allow_smem(kern, smem, granted);
+  if (se != cudaSuccess) return se;
   // Rows go round-robin over all resident segments.  When they take more
   // than one round, use the fewest blocks that still need the same number of
   // rounds, so that every segment carries the same number of rows (no

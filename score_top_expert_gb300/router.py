@@ -95,6 +95,25 @@ def _stream(device: torch.device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+class _NoSwitch:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoSwitch()
+
+
+def _on(device: torch.device):
+    """Make `device` current for the library call; no switch (and none of its
+    cost) when it already is."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return _NO_SWITCH
+    return torch.cuda.device(device)
+
+
 def _check(fn: str, code: int):
     if code != 0:
         raise RouterError(fn, code)
@@ -143,7 +162,7 @@ def router_topk_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax",
     probs = _out(probs, (T, E), logits.dtype, dev, "probs")
     routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
     scores = _out(scores, (T, E), torch.float32, dev, "scores")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_topk_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
                                    _score(score_func), int(num_groups), int(group_topk),
                                    float(scaling_factor), _ptr(expert_bias), _ptr(probs),
@@ -204,7 +223,7 @@ def router_topk_fwd_compact(logits: torch.Tensor, K: int, score_func: str = "sof
         scores = _out(scores, (T, E), torch.float32, dev, "scores")
     ld_w = topk_weights.stride(0) if T > 0 else K
     ld_i = topk_indices.stride(0) if T > 0 else K
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_topk_fwd_compact(
             _ptr(logits), _DTYPE[logits.dtype], T, E, K, _score(score_func), int(num_groups),
             int(group_topk), float(scaling_factor), _ptr(expert_bias), _ptr(topk_weights),
@@ -247,7 +266,7 @@ def router_expert_maps(topk_indices: torch.Tensor, E: int, *, out=None, workspac
     ld = topk_indices.stride(0) if T > 0 else K
     offsets, p2u, u2p, pexp = _maps_outputs(T, int(E), K, dev, out)
     workspace = _workspace(lib().router_expert_maps_workspace_bytes(T, int(E)), workspace, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_expert_maps(_ptr(topk_indices), ld, T, int(E), K, _ptr(offsets),
                                       _ptr(p2u), _ptr(u2p), _ptr(pexp), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(),
@@ -287,7 +306,7 @@ def router_topk_fwd_maps(logits: torch.Tensor, K: int, score_func: str = "softma
     workspace = _workspace(lib().router_expert_maps_workspace_bytes(T, E), workspace, dev)
     ld_w = topk_weights.stride(0) if T > 0 else K
     ld_i = topk_indices.stride(0) if T > 0 else K
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_topk_fwd_maps(
             _ptr(logits), _DTYPE[logits.dtype], T, E, K, _score(score_func), int(num_groups),
             int(group_topk), float(scaling_factor), _ptr(expert_bias), _ptr(topk_weights), ld_w,
@@ -310,7 +329,7 @@ def router_topk_bwd(grad_probs: torch.Tensor, routing_map: torch.Tensor,
         raise ValueError("grad_probs, routing_map and scores must have the same shape")
     dev = grad_probs.device
     grad_logits = _out(grad_logits, (T, E), grad_probs.dtype, dev, "grad_logits")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_topk_bwd(_ptr(grad_probs), _ptr(routing_map), _ptr(scores),
                                    _DTYPE[grad_probs.dtype], T, E, int(K),
                                    _score(score_func), float(scaling_factor),
@@ -331,7 +350,7 @@ def router_aux_scores_fwd(logits: torch.Tensor, K: int, score_func: str = "softm
     routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
     if score_func == "sigmoid" or intermediate is not None:
         intermediate = _out(intermediate, (T, E), torch.float32, dev, "intermediate")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_aux_scores_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
                                          _score(score_func), _ptr(scores), _ptr(routing_map),
                                          _ptr(intermediate), _stream(dev))
@@ -353,7 +372,7 @@ def router_aux_scores_bwd(grad_scores: torch.Tensor, saved: torch.Tensor, K: int
     T, E = grad_scores.shape
     dev = grad_scores.device
     grad_logits = _out(grad_logits, (T, E), dtype, dev, "grad_logits")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_aux_scores_bwd(_ptr(grad_scores), _ptr(saved), _DTYPE[dtype], T, E,
                                          int(K), _score(score_func), _ptr(grad_logits),
                                          _stream(dev))
@@ -391,7 +410,7 @@ def selftest_bounded_wait(timeout_us: int, device=None) -> None:
     """Enqueue the diagnostic kernel whose bounded wait always runs out (see
     moe_router_selftest_bounded_wait in the header)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("moe_router_selftest_bounded_wait",
                lib().moe_router_selftest_bounded_wait(int(timeout_us), _stream(dev)))
 
@@ -412,7 +431,7 @@ def router_aux_loss_fwd(aux_scores: torch.Tensor, routing_map: torch.Tensor, K: 
     nbytes = lib().router_aux_loss_workspace_bytes(T, E)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_aux_loss_fwd(_ptr(aux_scores), _ptr(routing_map), T, E, int(K),
                                        float(coeff), _ptr(loss), _ptr(tokens_per_expert),
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -442,7 +461,7 @@ def router_aux_loss_fwd_noalloc(aux_scores: torch.Tensor, routing_map: torch.Ten
             or tokens_per_expert.numel() != E or not tokens_per_expert.is_contiguous()):
         raise ValueError("tokens_per_expert must be a contiguous int32 [E] tensor on the "
                          "inputs' device")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_aux_loss_fwd_noalloc(_ptr(aux_scores), _ptr(routing_map), T, E, int(K),
                                                float(coeff), _ptr(loss),
                                                _ptr(tokens_per_expert), _stream(dev))
@@ -462,7 +481,7 @@ def router_aux_loss_bwd(grad_loss: torch.Tensor, tokens_per_expert: torch.Tensor
     grad_loss = grad_loss.contiguous()
     tokens_per_expert = tokens_per_expert.contiguous()
     grad_aux_scores = _out(grad_aux_scores, (T, E), torch.float32, dev, "grad_aux_scores")
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = lib().router_aux_loss_bwd(_ptr(grad_loss), _ptr(tokens_per_expert), int(T), E, int(K),
                                        float(coeff), _ptr(grad_aux_scores), _stream(dev))
     _check("router_aux_loss_bwd", rc)
