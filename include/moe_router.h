@@ -1,17 +1,25 @@
 /*
  * moe_router.h — fused Mixture-of-Experts router for NVIDIA GB300 (sm_103a).
  *
- * C ABI over caller-owned device memory.  The operations are the two fused
- * router ops of NVIDIA TransformerEngine PR #3012 "[Common] Optimize fused
- * router forward/backward kernels" (Summary: fused_topk_with_score_function
- * and fused_score_for_moe_aux_loss, each with a forward and a backward).
+ * C ABI over caller-owned device memory.  The core operations are the two
+ * fused router ops of NVIDIA TransformerEngine PR #3012 "[Common] Optimize
+ * fused router forward/backward kernels" (Summary: fused_topk_with_score_
+ * function and fused_score_for_moe_aux_loss, each with a forward and a
+ * backward).  Around them: the router with compact [T, K] outputs, the
+ * (expert, token)-sorted expert maps and the one-launch decode router with
+ * maps, and the load-balancing aux loss (each documented below with the page
+ * it follows).
  *
  * Conventions shared by every call
  * --------------------------------
  * - Every [T, E] tensor is dense row-major with row stride E elements, in
  *   device memory owned by the caller.  Nothing is allocated, freed or
  *   synchronised here: each call validates its arguments on the host,
- *   enqueues one kernel on `stream` and returns.
+ *   enqueues its work on `stream` (one kernel for the router ops; the calls
+ *   with a workspace say what they enqueue) and returns.  Kernels are
+ *   launched with programmatic dependent launch (each waits for the previous
+ *   kernel in the stream before touching memory; MOE_ROUTER_PDL=0 disables
+ *   it).
  * - `dtype` is the type of the logits and of the tensors that follow it
  *   (probs, grad_probs, grad_logits): MR_F32 (float) or MR_BF16
  *   (__nv_bfloat16).  Scores, intermediates, grad_scores and the expert bias
