@@ -103,12 +103,16 @@ def _strip_comments(src: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments and whitespace ignored)."""
+    """Hash of the code of the CUDA sources and the public header they include
+    (comments and whitespace ignored)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "score_top_expert_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), encoding="utf-8") as f:
-            h.update(name.encode() + _strip_comments(f.read()).encode())
+    for sub in (os.path.join("score_top_expert_gb300", "csrc"), "include"):
+        d = os.path.join(ROOT, sub)
+        if not os.path.isdir(d):
+            continue
+        for name in sorted(os.listdir(d)):
+            with open(os.path.join(d, name), encoding="utf-8") as f:
+                h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
