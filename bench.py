@@ -532,6 +532,19 @@ def copy_ceiling(torch, stream, flush, dev, nbytes, peak):
     return {"us": round(med * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
 
 
+def time_step_ops(torch, stream, flush, st, peak):
+    """The four kernels of one Step, each timed in isolation (L2 flushed
+    before every launch, median of 20): µs, effective GB/s, fraction of peak."""
+    ops = st.ops()
+    t = time_ops(torch, stream, flush, ops, 20, 3)
+    row = {}
+    for i, (n, _) in enumerate(ops):
+        med = statistics.median(t[i])
+        gbs = st.bytes(n) / (med * 1e-3) / 1e9
+        row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+    return row
+
+
 def breakdown(torch, R, stream, flush, dev, peak):
     """Per-kernel effective GB/s on the other benchmark workloads, with a
     plain copy of the top-K forward's bytes beside them (copy_ceiling)."""
@@ -545,19 +558,49 @@ def breakdown(torch, R, stream, flush, dev, peak):
             case, args = make_workload(name, dtype=dt)
             for sf in sfs:
                 st = Step(R, torch, case, args, dev, sf)
-                ops = st.ops()
-                t = time_ops(torch, stream, flush, ops, 20, 3)
-                row = {}
-                for i, (n, _) in enumerate(ops):
-                    med = statistics.median(t[i])
-                    gbs = st.bytes(n) / (med * 1e-3) / 1e9
-                    row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
-                              "frac": round(gbs / peak, 3)}
+                row = time_step_ops(torch, stream, flush, st, peak)
                 row["copy_ceiling"] = copy_ceiling(torch, stream, flush, dev,
                                                    st.bytes("topk_fwd"), peak)
                 res[f"{name}/{sf}/{dt}"] = row
                 del st
     return res
+
+
+# (E, K) pairs of the before/after table on the TransformerEngine page
+# ("[Common] Optimize fused router forward/backward kernels", benchmark
+# results), all at 8192 fp32 tokens; the sweep adds the pairs it leaves out
+SWEEP_E = (512, 2304)
+SWEEP_K = (4, 8, 22, 36)
+
+
+def k_sweep(a):
+    """Every (E, K) of SWEEP_E x SWEEP_K under both score functions, the four
+    kernels timed in isolation like the breakdown; one JSON line."""
+    import torch
+
+    import score_top_expert_gb300.router as R
+    from score_top_expert_gb300 import build
+    from score_top_expert_gb300.workloads import make_workload
+    build.build()
+    R.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    flush = L2Flush(torch, dev)
+    peak, peak_kind = hbm_peak()
+    res = {}
+    for E, name in zip(SWEEP_E, ("t8192_e512_k22", "t8192_e2304_k36")):
+        for K in SWEEP_K:
+            case, args = make_workload(name, K=K)
+            for sf in ("softmax", "sigmoid"):
+                st = Step(R, torch, case, args, dev, sf)
+                res[f"e{E}_k{K}/{sf}"] = time_step_ops(torch, stream, flush, st, peak)
+                del st
+    assert R.device_status() == 0
+    return {"sweep": "router kernels over (E, K), 8192 fp32 tokens, isolated (L2 flushed "
+                     "before each launch), median of 20", "peak_gbs": peak,
+            "peak_kind": peak_kind, "results": res}
 
 
 def steady_state(torch, R, stream, dev, peak, l2):
@@ -904,12 +947,18 @@ def main(argv=None):
     ap.add_argument("--profile-ops", default="step", choices=("step", "next"),
                     help="with --profile: the four router ops, or the compact forward, "
                          "expert maps and aux loss")
+    ap.add_argument("--sweep-k", action="store_true",
+                    help="time the four kernels over E in {512, 2304} x K in {4, 8, 22, 36} "
+                         "(softmax and sigmoid) and print that table instead")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
     if a.profile:
         profile_run(a)
+        return
+    if a.sweep_k:
+        print(json.dumps(k_sweep(a)), flush=True)
         return
     if a.impl == "reference":
         out = reference_arm(a, world, rank)

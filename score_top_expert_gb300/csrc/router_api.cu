@@ -357,7 +357,12 @@ bool choose_fwd(int E, int K, bool vec, FwdConfig* c) {
 
 // Lanes x warps x chunks per row of the two-pass backwards (measured best
 // per row size: more warps per row at large E keep more loads in flight).
-bool choose_bwd(int E, int op, BwdConfig* c) {
+// The softmax top-K backward of a 2304-expert row fits 7 blocks of 9 warps
+// per SM (32 registers a thread); the sigmoid and post-softmax ones need 48
+// and fit only 4 such blocks, so they take the aux shapes, 6 warps of 3
+// chunks at that size (6 blocks per SM): 34.3 us against 40.5 us at
+// 8192 x 2304, where the softmax one takes 32.9 us at 9 x 2 and 35.5 at 6 x 3.
+bool choose_bwd(int E, int op, int sf, BwdConfig* c) {
   const int chunks = (E + 3) / 4;
   struct Opt { int seg, w, nc; };
   static const Opt all[] = {{8, 1, 2}, {16, 1, 4}, {32, 1, 2}, {32, 1, 4}, {32, 2, 1},
@@ -378,7 +383,8 @@ bool choose_bwd(int E, int op, BwdConfig* c) {
   }
   static const Opt opts_topk[] = {{8, 1, 2}, {32, 1, 2}, {32, 1, 4}, {32, 2, 4}, {32, 9, 2}};
   static const Opt opts_aux[] = {{8, 1, 2}, {32, 1, 2}, {32, 1, 4}, {32, 2, 4}, {32, 6, 3}};
-  for (const Opt& o : (op == 0 ? opts_topk : opts_aux)) {
+  const bool topk_shapes = op == 0 && sf == MR_SOFTMAX;
+  for (const Opt& o : (topk_shapes ? opts_topk : opts_aux)) {
     if (o.seg * o.w * o.nc >= chunks) {
       c->seg = o.seg; c->w = o.w; c->nc = o.nc;
       return true;
@@ -584,7 +590,7 @@ int router_topk_bwd(const void* grad_probs, const uint8_t* routing_map,
     return MR_ERR_INVALID;
   if (T == 0) return MR_OK;
   BwdConfig c{};
-  if (!choose_bwd(E, 0, &c)) return MR_ERR_UNSUPPORTED;
+  if (!choose_bwd(E, 0, score_func, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = (E % 4 == 0) && aligned16(grad_probs) && aligned16(routing_map) &&
           aligned16(scores) && aligned16(grad_logits);
   c.op = 0;
@@ -643,7 +649,7 @@ int router_aux_scores_bwd(const float* grad_scores, const float* saved, mr_dtype
     return MR_ERR_INVALID;
   if (T == 0) return MR_OK;
   BwdConfig c{};
-  if (!choose_bwd(E, 1, &c)) return MR_ERR_UNSUPPORTED;
+  if (!choose_bwd(E, 1, score_func, &c)) return MR_ERR_UNSUPPORTED;
   c.vec = (E % 4 == 0) && aligned16(grad_scores) && aligned16(saved) &&
           aligned16(grad_logits);
   c.op = 1;
