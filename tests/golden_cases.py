@@ -30,10 +30,13 @@ def load(path: str) -> dict:
             toks = vals.split()
             if key in ("op", "score_func"):
                 out[key] = toks[0]
-            elif key in ("K", "num_groups", "group_topk"):
+            elif key in ("K", "num_groups", "group_topk", "E"):
                 out[key] = int(toks[0])
-            elif key == "scaling_factor":
+            elif key in ("scaling_factor", "coeff"):
                 out[key] = _value(toks[0])
+            elif "|" in vals:  # rows of a [T, ...] array, separated by "|"
+                out[key] = np.array([[_value(t) for t in row.split()]
+                                     for row in vals.split("|")], dtype=np.float64)
             else:
                 out[key] = np.array([_value(t) for t in toks], dtype=np.float64)
     out.setdefault("num_groups", 0)
