@@ -126,9 +126,39 @@ def selectable_experts(keys: np.ndarray, K: int, num_groups: int,
     return mask, gs
 
 
+# --------------------------------------------------------------------------
+# near ties: the rows whose selection a float32 computation may legitimately
+# decide differently.  Reading of the router's stated accuracy rule: the keys
+# on either side of the top-K boundary (the K-th and (K+1)-th in the ranked
+# order), or the scores on either side of the group boundary (the
+# group_topk-th and (group_topk+1)-th group), are distinct and within 1e-6
+# relative of each other.  Exact ties are not near ties: the lower-index rule
+# decides them.
+# --------------------------------------------------------------------------
 def _near(a: float, b: float) -> bool:
+    """Distinct, and within NEAR_TIE_REL relative of the larger magnitude."""
     d = abs(a - b)
     return 0.0 < d <= NEAR_TIE_REL * max(abs(a), abs(b))
+
+
+def boundary_near_tie(ranked_keys: np.ndarray, K: int) -> bool:
+    """The top-K boundary of one row: ``ranked_keys`` are the selectable keys
+    in selection order (key descending, index ascending); the row is a near
+    tie when its K-th and (K+1)-th keys are.  A row with no (K+1)-th
+    selectable key has no boundary."""
+    if K >= ranked_keys.size:
+        return False
+    return _near(ranked_keys[K - 1], ranked_keys[K])
+
+
+def group_near_tie(gs: np.ndarray, group_topk: int) -> bool:
+    """The group boundary of one grouped row: its group_topk-th and
+    (group_topk+1)-th group scores in group order (score descending, group
+    index ascending).  Keeping every group leaves no boundary."""
+    if group_topk >= gs.size:
+        return False
+    ranked = gs[order_desc(gs)]
+    return _near(ranked[group_topk - 1], ranked[group_topk])
 
 
 # --------------------------------------------------------------------------
@@ -160,12 +190,9 @@ def topk_fwd_row(x, K, score_func, num_groups=0, group_topk=0,
     else:  # sigmoid, softmax_post: renormalised over the selected
         probs = np.where(m, scaling_factor * s / s[sel].sum(), 0.0)
 
-    near = False
-    if K < order.size:
-        near = _near(key[order[K - 1]], key[order[K]])
-    if gs is not None and group_topk < num_groups:
-        go = order_desc(gs)
-        near = near or _near(gs[go[group_topk - 1]], gs[go[group_topk]])
+    near = boundary_near_tie(key[order], K)                       # near ties
+    if gs is not None:
+        near = near or group_near_tie(gs, group_topk)
     if ranked:
         return probs, m, s, near, sel
     return probs, m, s, near
@@ -330,9 +357,7 @@ def aux_scores_fwd(logits, K, score_func=SOFTMAX):
     near = np.zeros(T, dtype=bool)
     for t in range(T):
         q[t], m[t], saved[t] = aux_scores_fwd_row(logits[t], K, score_func)
-        if K < E:
-            o = order_desc(q[t])
-            near[t] = _near(q[t][o[K - 1]], q[t][o[K]])
+        near[t] = boundary_near_tie(q[t][order_desc(q[t])], K)
     return dict(scores=q, routing_map=m, saved=saved, near_tie=near)
 
 

@@ -450,6 +450,110 @@ def test_bf16_rounding():
 
 
 # --------------------------------------------------------------------------
+# near ties: which rows may legitimately select differently.  The rule: a
+# row is a near tie when the keys on either side of its top-K boundary (or the
+# group scores on either side of its group boundary) are distinct and within
+# 1e-6 relative; exact ties are not near ties.  Every row below is built by
+# hand so that its status follows from that rule and the arithmetic of exp:
+# for softmax keys, logits d apart give keys whose relative gap is
+# 1 - exp(-d), i.e. d to within d^2 / 2; for sigmoid keys at x = 0 the relative
+# gap of logits d apart is d / 2 to first order.
+# --------------------------------------------------------------------------
+_TAIL = [-1.0, 0.0, -2.0]   # three experts far below every boundary here
+
+
+def _near_rows():
+    """(name, logits row, K, score function, bias, groups, want near_tie)."""
+    rows = [
+        # K-th and (K+1)-th logits equal: an exact tie, decided by index
+        ("exact tie at the boundary", [3.0, 1.0, 1.0] + _TAIL, 2, "softmax", None, None, False),
+        # 5e-7 apart: relative key gap 4.9999988e-7 <= 1e-6
+        ("5e-7 at the boundary", [3.0, 1.0, 1.0 - 5e-7] + _TAIL, 2, "softmax", None, None, True),
+        # 2e-6 apart: relative key gap 1.999998e-6 > 1e-6
+        ("2e-6 at the boundary", [3.0, 1.0, 1.0 - 2e-6] + _TAIL, 2, "softmax", None, None, False),
+        # the near pair is ranks 1 and 2, both selected; the boundary (rank 2
+        # against rank 3) is 2 logits wide
+        ("near pair inside the top-K", [3.0, 3.0 - 5e-7, 1.0] + _TAIL, 2, "softmax", None,
+         None, False),
+        # the near pair is ranks 3 and 4, both left out
+        ("near pair below the boundary", [3.0, 2.0, 1.0, 1.0 - 5e-7, -2.0, -3.0], 2,
+         "softmax", None, None, False),
+        # keys near 0.1 that differ by about 5e-7 in absolute terms but by
+        # 5e-6 relative: not near (the rule is relative)
+        ("small keys, 5e-6 relative", [3.0, 1.0, 1.0 - 5e-6] + _TAIL, 2, "softmax", None,
+         None, False),
+        # sigmoid keys 0.5 and sigmoid(-1e-6): relative gap 5e-7
+        ("sigmoid, 5e-7 at the boundary", [0.0, -1e-6, -3.0, -4.0], 1, "sigmoid", None,
+         None, True),
+        # equal scores (all logits 0: s = 1/4), keys s + b differ by 3e-7
+        # absolute at 0.75, i.e. 4e-7 relative: the key decides, not the score
+        ("biased keys 4e-7 apart", [0.0, 0.0, 0.0, 0.0], 1, "softmax",
+         [0.0, 0.5, 0.5 - 3e-7, 0.0], None, True),
+    ]
+    # four groups of two, keep two, K = 2: a group scores its largest key.
+    # Kept: groups 0 and 1; the expert boundary (s(3) against s(0)) is wide.
+    rows += [
+        ("group scores 5e-7 apart at the group boundary",
+         [5.0, 0.0, 3.0, -1.0, 3.0 - 5e-7, -1.0, -2.0, -2.0], 2, "softmax", None, (4, 2), True),
+        ("group scores tied exactly at the group boundary",
+         [5.0, 0.0, 3.0, -1.0, 3.0, -1.0, -2.0, -2.0], 2, "softmax", None, (4, 2), False),
+        ("group scores 2e-6 apart at the group boundary",
+         [5.0, 0.0, 3.0, -1.0, 3.0 - 2e-6, -1.0, -2.0, -2.0], 2, "softmax", None, (4, 2), False),
+        # the near groups (0 and 1) are both kept; groups 2 and 3 are far below
+        ("near groups both kept",
+         [3.0, -1.0, 3.0 - 5e-7, -1.0, 1.0, -2.0, -2.0, -3.0], 2, "softmax", None, (4, 2), False),
+        # keeping every group leaves no group boundary; K = 4 puts the
+        # expert boundary between s(0) and s(-1)
+        ("every group kept",
+         [5.0, 0.0, 3.0, -1.0, 3.0 - 5e-7, -1.0, -2.0, -2.0], 4, "softmax", None, (4, 4), False),
+    ]
+    return rows
+
+
+def check_near_tie_classifier():
+    for name, x, K, sf, b, grp, want in _near_rows():
+        logits = np.array([x], dtype=np.float64)
+        bias = None if b is None else np.array(b, dtype=np.float64)
+        ng, gk = grp if grp is not None else (0, 0)
+        got = O.topk_fwd(logits, K, sf, ng, gk, 1.0, bias)["near_tie"][0]
+        assert got == want, (name, got, want)
+        got_c = O.topk_fwd_compact(logits, K, sf, ng, gk, 1.0, bias)["near_tie"][0]
+        assert got_c == want, (name, "compact", got_c, want)
+    # aux scores: the same boundary rule on q (softmax; sigmoid / sum sigmoid,
+    # whose relative gaps are those of the sigmoid)
+    aux = [
+        ([3.0, 1.0, 1.0] + _TAIL, 2, "softmax", False),
+        ([3.0, 1.0, 1.0 - 5e-7] + _TAIL, 2, "softmax", True),
+        ([3.0, 1.0, 1.0 - 2e-6] + _TAIL, 2, "softmax", False),
+        ([3.0, 2.0, 1.0, 1.0 - 5e-7, -2.0, -3.0], 2, "softmax", False),
+        ([0.0, -1e-6, -3.0, -4.0], 1, "sigmoid", True),
+        ([0.0, 0.0, -3.0, -4.0], 1, "sigmoid", False),
+    ]
+    for x, K, sf, want in aux:
+        got = O.aux_scores_fwd(np.array([x]), K, sf)["near_tie"][0]
+        assert got == want, ("aux", x, K, sf, got, want)
+    # K = E: no boundary at all
+    assert not O.topk_fwd(np.array([[1.0, 1.0 - 5e-7]]), 2)["near_tie"][0]
+    # several rows at once: the flags line up with their rows
+    rows = _near_rows()[:3]
+    batch = np.array([r[1] for r in rows])
+    assert list(O.topk_fwd(batch, 2)["near_tie"]) == [r[6] for r in rows]
+
+
+def test_near_tie_classifier():
+    check_near_tie_classifier()
+
+
+def test_near_tie_rows_select_by_the_rule():
+    # the exact-tie row selects the lower index (not exempt); the 5e-7 row
+    # selects the larger key, index 1, like any other row
+    r = O.topk_fwd(np.array([[3.0, 1.0, 1.0] + _TAIL]), 2)
+    assert list(np.nonzero(r["routing_map"][0])[0]) == [0, 1]
+    r = O.topk_fwd(np.array([[3.0, 1.0 - 5e-7, 1.0] + _TAIL]), 2)
+    assert list(np.nonzero(r["routing_map"][0])[0]) == [0, 2]
+
+
+# --------------------------------------------------------------------------
 # the pins catch plausible mistakes planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
 def _wrong_order(keys):  # ties to the HIGHER index
@@ -584,7 +688,38 @@ def _wrong_maps_row_major(idx, E):   # expanded row t K + k instead of t + k T
     return out
 
 
+def _wrong_near_exact_ties(a, b):   # exempts exact ties too
+    d = abs(a - b)
+    return 0.0 <= d <= O.NEAR_TIE_REL * max(abs(a), abs(b))
+
+
+def _wrong_near_absolute(a, b):   # absolute instead of relative
+    d = abs(a - b)
+    return 0.0 < d <= O.NEAR_TIE_REL
+
+
+def _wrong_boundary_one_below(ranked_keys, K):   # (K+1)-th against (K+2)-th
+    if K + 1 >= ranked_keys.size:
+        return False
+    return O._near(ranked_keys[K], ranked_keys[K + 1])
+
+
+def _wrong_boundary_inside(ranked_keys, K):   # (K-1)-th against K-th
+    if K >= ranked_keys.size or K < 2:
+        return False
+    return O._near(ranked_keys[K - 2], ranked_keys[K - 1])
+
+
+def _wrong_group_near_dropped(gs, group_topk):   # the group boundary ignored
+    return False
+
+
 PLANTED = [
+    ("_near", _wrong_near_exact_ties, [check_near_tie_classifier]),
+    ("_near", _wrong_near_absolute, [check_near_tie_classifier]),
+    ("boundary_near_tie", _wrong_boundary_one_below, [check_near_tie_classifier]),
+    ("boundary_near_tie", _wrong_boundary_inside, [check_near_tie_classifier]),
+    ("group_near_tie", _wrong_group_near_dropped, [check_near_tie_classifier]),
     ("expert_maps", _wrong_maps_k_order, [check_expert_maps]),
     ("expert_maps", _wrong_maps_row_major, [check_expert_maps]),
     ("topk_fwd_compact", _wrong_compact_by_weight, [check_compact]),
