@@ -409,6 +409,9 @@ int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_
   const int rc = aux_check(T, E, K);
   if (rc != MR_OK) return rc;
   const int nb = T < kNoAllocBlocks ? T : kNoAllocBlocks;
+  // Cannot fire while aux_check caps E at MR_MAX_EXPERTS (the array is sized
+  // for that E and kNoAllocBlocks rows); kept as a guard should either limit
+  // change.
   if (static_cast<size_t>(nb) * static_cast<size_t>(E) * 8u + kAuxTailBytes >
       sizeof(g_aux_noalloc_scratch))
     return MR_ERR_UNSUPPORTED;

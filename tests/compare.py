@@ -39,6 +39,36 @@ class MapReport:
             f"{what}: {self.mismatched_rows}/{self.rows} rows mismatch"
 
 
+# Near-tie record of the full-size workloads, printed in the test session's
+# terminal summary: label -> [rows, near-tie rows, most mismatched rows over
+# the runs, runs].
+NEAR_TIE_RECORD: dict[str, list[int]] = {}
+
+
+def record_near_ties(label: str, rep: MapReport) -> None:
+    r = NEAR_TIE_RECORD.setdefault(label, [rep.rows, rep.near_tie_rows, 0, 0])
+    r[1] = max(r[1], rep.near_tie_rows)
+    r[2] = max(r[2], rep.mismatched_rows)
+    r[3] += 1
+
+
+def near_tie_summary() -> list[str]:
+    if not NEAR_TIE_RECORD:
+        return []
+    lines = ["near-tie record, full-size workloads (rows, near-tie rows, most mismatched "
+             "rows over the runs, runs):"]
+    worst = 0.0
+    total_mis = 0
+    for label, (rows, near, mis, runs) in sorted(NEAR_TIE_RECORD.items()):
+        lines.append(f"  {label}: {rows} rows, {near} near-tie, {mis} mismatched, {runs} runs")
+        worst = max(worst, mis / max(rows, 1))
+        total_mis += mis
+    lines.append(f"near ties: {len(NEAR_TIE_RECORD)} workloads, mismatched rows {total_mis} "
+                 f"in all, largest mismatched fraction {worst:.2e} (bound {MAX_MISMATCH_FRAC:g}), "
+                 f"near-tie rows {sum(r[1] for r in NEAR_TIE_RECORD.values())} in all")
+    return lines
+
+
 def compare_map(gpu_map: np.ndarray, ref_map: np.ndarray, near: np.ndarray) -> MapReport:
     gpu_map = np.asarray(gpu_map).astype(bool)
     diff = np.any(gpu_map != ref_map, axis=1)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle.router_oracle as O
-from compare import assert_close, compare_map
+from compare import assert_close, compare_map, record_near_ties
 from score_top_expert_gb300.workloads import WORKLOADS, make_case, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -116,6 +116,7 @@ TOPK_CASES = [
     ("t8192_e256_k4", "softmax", "f32"), ("t8192_e256_k4", "sigmoid", "f32"),
     ("t8192_e256_k8", "softmax", "f32"), ("t8192_e256_k8", "sigmoid", "f32"),
     ("t8192_e256_k4", "softmax", "bf16"), ("t8192_e256_k8", "sigmoid", "bf16"),
+    ("t8192_e256_k4", "sigmoid", "bf16"), ("t8192_e256_k8", "softmax", "bf16"),
     ("t8192_e512_k22", "softmax", "f32"), ("t8192_e512_k22", "sigmoid", "f32"),
     ("t8192_e2304_k36", "softmax", "f32"), ("t8192_e2304_k36", "sigmoid", "f32"),
     ("t16384_e256_k8_grouped", "sigmoid", "bf16"),
@@ -129,8 +130,7 @@ def test_topk_workload(R, path, name, sf, dt):
     rep = run_and_check_topk(R, case, args["K"], sf, args["scaling_factor"],
                              args["num_groups"], args["group_topk"], bias,
                              ref_key=("topk", name, sf, dt))
-    print(f"{name} {sf} {dt} {path}: near-tie rows {rep.near_tie_rows}, "
-          f"mismatched rows {rep.mismatched_rows}")
+    record_near_ties(f"topk {name} {sf} {dt}", rep)
 
 
 AUX_CASES = [("t8192_e512_k22", "softmax"), ("t8192_e512_k22", "sigmoid"),
@@ -140,7 +140,8 @@ AUX_CASES = [("t8192_e512_k22", "softmax"), ("t8192_e512_k22", "sigmoid"),
 @pytest.mark.parametrize("name,sf", AUX_CASES, ids=[f"{n}-{s}" for n, s in AUX_CASES])
 def test_aux_workload(R, path, name, sf):
     case, args = make_workload(name)
-    run_and_check_aux(R, case, args["K"], sf, ref_key=("aux", name, sf))
+    rep = run_and_check_aux(R, case, args["K"], sf, ref_key=("aux", name, sf))
+    record_near_ties(f"aux {name} {sf} f32", rep)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
