@@ -5,12 +5,14 @@ forward/backward and the aux-score forward/backward at 8192 tokens.
 
 One step is one pass of the router's hot path over one batch of synthetic
 tokens: top-K forward, aux-score forward, top-K backward, aux-score backward
-(softmax, fp32 logits, 8192 tokens x 2304 experts, K = 36).  L2 is flushed
-before every kernel, outside that kernel's CUDA events: a write of a buffer
-larger than L2, then a read of a second one, so that the written lines are
-back in HBM before the kernel starts (otherwise their write-back would land
-inside the kernel's time).  value = algorithmic bytes of the step / the
-step's kernel time.
+(softmax, fp32 logits, 8192 tokens x 2304 experts, K = 36).  The timed steps
+run back to back, with no flush, over N rotating buffer sets (inputs and
+outputs) whose bytes per kernel launch together exceed 3x L2, so that every
+kernel reads its inputs from HBM and pays the write-back of whatever its
+predecessors left dirty in L2.  value = algorithmic bytes of the K steps / the
+time between CUDA events around them; the per-kernel events inside the region
+give the roofline.  The same kernels timed one at a time with L2 flushed
+before each launch are reported under "isolated".
 
 Algorithmic bytes per token row of E experts (d = bytes per logit):
   top-K fwd  E (d + d + 1 + 4)   logits in; probs, map, scores out (+ bias 4E once)
@@ -20,7 +22,7 @@ Algorithmic bytes per token row of E experts (d = bytes per logit):
 
 Under torchrun (N > 1) every rank routes its own 8192-token batch (token rows
 are independent: no collective on the data path), the timed region is
-bracketed by barriers, the kernel time is the max over ranks and value is the
+bracketed by barriers, the times are the max over ranks and value is the
 bytes of all ranks over that time ("weak" scaling).
 
 --impl reference times the CPU oracle (float64 numpy, one row at a time, the
@@ -231,25 +233,39 @@ def barrier(world: int):
 class Step:
     """Inputs and outputs of one router step on the device."""
 
-    def __init__(self, R, torch, case, args, dev, sf="softmax"):
+    def __init__(self, R, torch, case, args, dev, sf="softmax", packed=False):
+        """packed: the inputs (logits, grad_probs, grad_scores) are views into
+        one device buffer (in_buf) and the outputs into another (out_buf), so
+        that a host round trip takes one copy each way."""
         self.R, self.torch = R, torch
         T, E = case.logits.shape
         dt = torch.float32 if case.dtype == "f32" else torch.bfloat16
         self.dt = dt
         self.K, self.sf = args["K"], sf
         self.c, self.ng, self.gk = args["scaling_factor"], args["num_groups"], args["group_topk"]
-        self.x = torch.from_numpy(case.logits).to(dev).to(dt)
-        self.g = torch.from_numpy(case.grad_probs).to(dev).to(dt)
-        self.gs = torch.from_numpy(case.grad_scores).to(dev)
+        f32, b8 = torch.float32, torch.bool
+        ins = [("x", dt), ("g", dt), ("gs", f32)]
+        outs = [("probs", dt), ("rmap", b8), ("scores", f32), ("gx", dt), ("q", f32),
+                ("amap", b8), ("agx", dt)] + ([("inter", f32)] if sf == "sigmoid" else [])
+        if packed:
+            self.in_buf, views = _carve(torch, dev, (T, E), ins)
+            for (n, _), v in zip(ins, views):
+                setattr(self, n, v)
+            self.out_buf, views = _carve(torch, dev, (T, E), outs)
+            for (n, _), v in zip(outs, views):
+                setattr(self, n, v)
+            self.x.copy_(torch.from_numpy(case.logits).to(dt))
+            self.g.copy_(torch.from_numpy(case.grad_probs).to(dt))
+            self.gs.copy_(torch.from_numpy(case.grad_scores))
+        else:
+            self.x = torch.from_numpy(case.logits).to(dev).to(dt)
+            self.g = torch.from_numpy(case.grad_probs).to(dev).to(dt)
+            self.gs = torch.from_numpy(case.grad_scores).to(dev)
+            for n, t in outs:
+                setattr(self, n, torch.empty(T, E, dtype=t, device=dev))
+        if sf != "sigmoid":
+            self.inter = None
         self.bias = None if case.expert_bias is None else torch.from_numpy(case.expert_bias).to(dev)
-        self.probs = torch.empty(T, E, dtype=dt, device=dev)
-        self.rmap = torch.empty(T, E, dtype=torch.bool, device=dev)
-        self.scores = torch.empty(T, E, dtype=torch.float32, device=dev)
-        self.gx = torch.empty(T, E, dtype=dt, device=dev)
-        self.q = torch.empty(T, E, dtype=torch.float32, device=dev)
-        self.amap = torch.empty(T, E, dtype=torch.bool, device=dev)
-        self.inter = torch.empty(T, E, dtype=torch.float32, device=dev) if sf == "sigmoid" else None
-        self.agx = torch.empty(T, E, dtype=dt, device=dev)
         self.T, self.E, self.d = T, E, (4 if dt == torch.float32 else 2)
 
     def ops(self):
@@ -269,6 +285,21 @@ class Step:
 
     def bytes(self, op):
         return bytes_per_launch(op, self.T, self.E, self.d, self.sf, self.bias is not None)
+
+
+def _carve(torch, dev, shape, specs):
+    """One uint8 device buffer holding a [shape] tensor of each dtype in
+    ``specs`` back to back (each at a 256-byte boundary); returns the buffer
+    and the tensor views."""
+    n = shape[0] * shape[1]
+    sizes = [n * torch.empty(0, dtype=t).element_size() for _, t in specs]
+    offs, off = [], 0
+    for b in sizes:
+        offs.append(off)
+        off += (b + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    views = [buf[o:o + b].view(t).view(shape) for o, b, (_, t) in zip(offs, sizes, specs)]
+    return buf, views
 
 
 class L2Flush:
@@ -311,6 +342,42 @@ def time_ops(torch, stream, flush, ops, reps, warmup):
             for i in range(len(ops))]
 
 
+def rotating_sets(R, torch, case, args, dev, sf, l2, make=None):
+    """Buffer sets (Step objects) for back-to-back timing: enough that the
+    bytes of one kernel launch over all sets exceed 3x L2, so a launch never
+    finds its inputs in L2 from the previous use of its set."""
+    make = make or (lambda: Step(R, torch, case, args, dev, sf))
+    first = make()
+    per_launch = min(first.bytes(n) for n, _ in first.ops())
+    nsets = max(2, -(-3 * l2 // per_launch))
+    return [first] + [make() for _ in range(nsets - 1)]
+
+
+def graph_us(torch, stream, fns, reps_per_fn=3, replays=10):
+    """Device µs per launch: a CUDA graph of the launches ``fns`` repeated
+    ``reps_per_fn`` times back to back, median over ``replays`` replays."""
+    g = torch.cuda.CUDAGraph()
+    for fn in fns:
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fns * reps_per_fn:
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    del g
+    return statistics.median(times) / (len(fns) * reps_per_fn)
+
+
 def gpu_arm(a, world, rank, local):
     import torch
 
@@ -328,33 +395,34 @@ def gpu_arm(a, world, rank, local):
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = L2Flush(torch, dev)
     peak, peak_kind = hbm_peak()
 
     case, args = make_workload(WORKLOAD)
-    step = Step(R, torch, case, args, dev, "softmax")
-    ops = step.ops()
+    sets = rotating_sets(R, torch, case, args, dev, "softmax", l2)
+    nsets = len(sets)
+    step = sets[0]
+    set_ops = [st.ops() for st in sets]
+    names = [n for n, _ in set_ops[0]]
+    step_bytes = sum(step.bytes(n) for n in names)
 
-    # ---- the timed region: K steps ------------------------------------------
-    for _ in range(a.warmup):
-        for _, fn in ops:
-            flush.zero_()
+    # ---- the timed region: K steps back to back over the rotating sets -------
+    for w in range(a.warmup):
+        for _, fn in set_ops[w % nsets]:
             fn()
     torch.cuda.synchronize()
     barrier(world)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in ops] for _ in range(a.steps)]
+           for _ in names] for _ in range(a.steps)]
     t_all0 = torch.cuda.Event(enable_timing=True)
     t_all1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier(world)
         wall0 = time.perf_counter()
-        torch.cuda._sleep(2_000_000)
+        torch.cuda._sleep(2_000_000)  # let the host run ahead of the GPU
         t_all0.record(stream)
         for r in range(a.steps):
-            for i, (_, fn) in enumerate(ops):
-                flush.zero_()
+            for i, (_, fn) in enumerate(set_ops[(a.warmup + r) % nsets]):
                 ev[r][i][0].record(stream)
                 fn()
                 ev[r][i][1].record(stream)
@@ -363,41 +431,47 @@ def gpu_arm(a, world, rank, local):
         barrier(world)
         wall1 = time.perf_counter()
     per_op = [[ev[r][i][0].elapsed_time(ev[r][i][1]) for r in range(a.steps)]
-              for i in range(len(ops))]
-    step_ms = [sum(per_op[i][r] for i in range(len(ops))) for r in range(a.steps)]
-    kernel_ms = max_over_ranks(sum(step_ms), world, dev)
+              for i in range(len(names))]
+    kernel_ms = max_over_ranks(sum(sum(x) for x in per_op), world, dev)
     region_ms = max_over_ranks(t_all0.elapsed_time(t_all1), world, dev)
-    step_bytes = sum(step.bytes(n) for n, _ in ops)
-    value = world * step_bytes * a.steps / (kernel_ms * 1e-3) / 1e9
+    value = world * step_bytes * a.steps / (region_ms * 1e-3) / 1e9
 
     kern = {}
-    for i, (n, _) in enumerate(ops):
-        avg = sum(per_op[i]) / len(per_op[i])
-        kern[n] = dict(avg_us=round(avg * 1e3, 2), gbs=round(step.bytes(n) / (avg * 1e-3) / 1e9, 1),
-                       frac=round(step.bytes(n) / (avg * 1e-3) / 1e9 / peak, 4),
+    for i, n in enumerate(names):
+        avg = max_over_ranks(sum(per_op[i]) / len(per_op[i]), world, dev)
+        gbs = step.bytes(n) / (avg * 1e-3) / 1e9
+        kern[n] = dict(avg_us=round(avg * 1e3, 2), gbs=round(gbs, 1), frac=round(gbs / peak, 4),
                        bytes=step.bytes(n))
     dom = max(kern, key=lambda n: kern[n]["avg_us"])
 
+    # ---- the same kernels one at a time, L2 flushed before each launch --------
+    flush = L2Flush(torch, dev)
+    iso = isolated(torch, stream, flush, step, peak, reps=max(20, min(a.steps, 200)))
+
     # ---- end to end through the public API with host buffers ----------------
-    e2e = e2e_arm(torch, R, step, stream, max(3, min(a.steps, 20)), world, dev, case, args)
+    del sets, set_ops
+    torch.cuda.empty_cache()
+    e2e = e2e_arm(torch, R, stream, max(3, min(a.steps, 20)), world, dev, case, args)
 
     if rank != 0:
         return None
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup,
-        "ms_per_step": round(kernel_ms / a.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(region_ms / a.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} softmax: router_topk_fwd + router_aux_scores_fwd"
                                " + router_topk_bwd + router_aux_scores_bwd",
                    "tokens": 8192, "experts": 2304, "topk": 36, "score_func": "softmax",
                    "logits_dtype": "f32", "tokens_per_gpu": 8192,
                    "parallelism": f"data-parallel x{world} (independent token batches)",
-                   "l2": f"flushed before every kernel (write of {flush.mib} MiB, then a "
-                         f"read of another {flush.mib} MiB), outside the kernel events",
+                   "l2": f"inputs larger than L2: steps rotate over {nsets} buffer sets "
+                         f"({nsets} x {min(step.bytes(n) for n in names) >> 20} MiB and more "
+                         f"per kernel > 3 x {l2 >> 20} MiB L2), kernels back to back, "
+                         "no flush",
                    "peak_hbm_gbs": peak, "peak_kind": peak_kind},
-        "gpu_launches": len(ops) * a.steps,
-        "region_ms_per_step": round(region_ms / a.steps, 4),
+        "gpu_launches": len(names) * a.steps,
+        "kernel_ms_per_step": round(kernel_ms / a.steps, 4),
         "wall_s": round(wall1 - wall0, 3),
         "kernels": kern,
         "roofline": {"bound": "hbm", "kernel": dom,
@@ -405,13 +479,14 @@ def gpu_arm(a, world, rank, local):
                      "frac": kern[dom]["frac"], "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": kern[dom]["bytes"],
                      "traffic": traffic_for(dom, WORKLOAD)},
+        "isolated": iso,
         "e2e": e2e,
         "clocks": clk.summary(),
     }
     if not a.no_extra:
-        out["breakdown"] = breakdown(torch, R, stream, flush, dev, peak)
-        out["steady_state"] = steady_state(torch, R, stream, dev, peak, l2)
-        out["next_rows"] = next_rows(torch, R, stream, flush, dev, peak)
+        out["target_matrix"] = target_matrix(torch, R, stream, dev, peak, l2)
+        out["breakdown"] = breakdown(torch, R, stream, dev, peak, l2)
+        out["next_rows"] = next_rows(torch, R, stream, L2Flush(torch, dev), dev, peak)
         out["decode_us"] = decode_latency(torch, R, stream, dev)
         out["decode_eager_us"] = decode_eager(torch, R, stream, dev)
         out["decode_maps_us"] = decode_latency(torch, R, stream, dev, maps=True)
@@ -419,36 +494,52 @@ def gpu_arm(a, world, rank, local):
     return out
 
 
-def e2e_arm(torch, R, step, stream, reps, world, dev, case, args):
+def isolated(torch, stream, flush, step, peak, reps):
+    """The step's kernels one launch at a time, L2 flushed with clean lines
+    before each (a kernel's own writes may stay dirty in L2 after its end
+    event, so its write-back goes untimed): mean µs per kernel and the step's
+    effective GB/s."""
+    ops = step.ops()
+    t = time_ops(torch, stream, flush, ops, reps, 3)
+    res = {"protocol": f"one launch at a time, L2 flushed before each (write of {flush.mib} "
+                       f"MiB, then a read of another {flush.mib} MiB), mean of {reps}"}
+    total_us, total_b = 0.0, 0
+    for i, (n, _) in enumerate(ops):
+        us = sum(t[i]) / len(t[i]) * 1e3
+        gbs = step.bytes(n) / (us * 1e-6) / 1e9
+        res[n] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        total_us += us
+        total_b += step.bytes(n)
+    gbs = total_b / (total_us * 1e-6) / 1e9
+    res["step"] = {"us": round(total_us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    return res
+
+
+def e2e_arm(torch, R, stream, reps, world, dev, case, args):
     """Same step through the public API with host buffers: every step copies
     its inputs in from pinned host memory, makes the four router calls and
-    copies every output back.  Reported: steps pipelined over two device
-    buffer sets (inputs of step i+1 in flight while step i computes and step
-    i-1's outputs come back, on three streams ordered by events); beside it
-    the same steps one after another on one stream."""
-    steps = [step, Step(R, torch, case, args, dev, "softmax")]
-    hx = step.x.cpu().pin_memory()
-    hg = step.g.cpu().pin_memory()
-    hgs = step.gs.cpu().pin_memory()
-
-    def outs_of(st):
-        o = [st.probs, st.rmap, st.scores, st.gx, st.q, st.amap, st.agx]
-        return o + ([st.inter] if st.inter is not None else [])
-
-    houts = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs_of(st)]
+    copies every output back.  The inputs sit in one device buffer and the
+    outputs in another (the router writes into caller-placed views), so each
+    direction is one copy per step.  Reported: steps pipelined over two
+    device buffer sets (inputs of step i+1 in flight while step i computes and
+    step i-1's outputs come back, on three streams ordered by events); beside
+    it the same steps one after another on one stream, and the host-link copy
+    ceilings measured on the same buffers."""
+    steps = [Step(R, torch, case, args, dev, "softmax", packed=True) for _ in range(2)]
+    step = steps[0]
+    hin = torch.empty(step.in_buf.numel(), dtype=torch.uint8, pin_memory=True)
+    hin.copy_(step.in_buf)
+    houts = [torch.empty(st.out_buf.numel(), dtype=torch.uint8, pin_memory=True)
              for st in steps]
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hg, hgs))
-    d2h = sum(t.numel() * t.element_size() for t in houts[0])
+    h2d = int(hin.numel())
+    d2h = int(houts[0].numel())
     step_bytes = sum(step.bytes(n) for n, _ in step.ops())
 
     def copy_in(st):
-        st.x.copy_(hx, non_blocking=True)
-        st.g.copy_(hg, non_blocking=True)
-        st.gs.copy_(hgs, non_blocking=True)
+        st.in_buf.copy_(hin, non_blocking=True)
 
     def copy_out(st, hout):
-        for d, h in zip(outs_of(st), hout):
-            h.copy_(d, non_blocking=True)
+        hout.copy_(st.out_buf, non_blocking=True)
 
     # one after another on one stream
     def serial_one():
@@ -510,26 +601,73 @@ def e2e_arm(torch, R, step, stream, reps, world, dev, case, args):
     pipelined(reps, p0, p1)
     torch.cuda.synchronize()
     ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
+
+    # host-link ceilings on the same buffers: each direction alone, and both
+    # at once on two streams (what the pipeline overlaps)
+    def copy_gbs(fns_streams, nbytes):
+        for _ in range(2):
+            for fn, st in fns_streams:
+                with torch.cuda.stream(st):
+                    fn()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        uniq = list({id(st): st for _, st in fns_streams}.values())
+        for st in uniq:
+            st.wait_event(c0)
+        for _ in range(reps):
+            for fn, st in fns_streams:
+                with torch.cuda.stream(st):
+                    fn()
+        for st in uniq:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        return nbytes * reps / (c0.elapsed_time(c1) * 1e-3) / 1e9
+
+    d2h_gbs = copy_gbs([(lambda: copy_out(step, houts[0]), s_out)], d2h)
+    h2d_gbs = copy_gbs([(lambda: copy_in(step), s_in)], h2d)
+    both_ms_per = (h2d / h2d_gbs + d2h / d2h_gbs) / 1e9  # if serialised
+    bidir_gbs = copy_gbs([(lambda: copy_in(steps[1]), s_in),
+                          (lambda: copy_out(step, houts[0]), s_out)], h2d + d2h)
+    ms_per = ms / reps
     return {"value": round(world * step_bytes * reps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / reps, 4),
-            "pipelined": "two device buffer sets; copies in, router calls and copies out on "
-                         "three streams ordered by events",
+            "ms_per_step": round(ms_per, 4),
+            "pipelined": "two device buffer sets; one copy in, the four router calls and one "
+                         "copy out per step, on three streams ordered by events",
             "serial": {"value": round(world * step_bytes * reps / (serial_ms * 1e-3) / 1e9, 1),
-                       "ms_per_step": round(serial_ms / reps, 4)}}
+                       "ms_per_step": round(serial_ms / reps, 4)},
+            "copy_ceiling_d2h_gbs": round(d2h_gbs, 1),
+            "copy_ceiling_h2d_gbs": round(h2d_gbs, 1),
+            "copy_ceiling_bidirectional_gbs": round(bidir_gbs, 1),
+            "copies_alone_ms_per_step": round(both_ms_per * 1e3, 4),
+            "d2h_rate_gbs": round(d2h / (ms_per * 1e-3) / 1e9, 1),
+            "d2h_rate_frac_of_ceiling": round(d2h / (ms_per * 1e-3) / 1e9 / d2h_gbs, 3)}
 
 
-def copy_ceiling(torch, stream, flush, dev, nbytes, peak):
+def copy_ceiling(torch, stream, flush, dev, nbytes, peak, l2=None):
     """A device-to-device copy moving the same bytes as one launch (half read,
-    half written), timed like the router kernels: what a plain copy reaches
-    at this size with the L2 flushed before it."""
+    half written), timed like the router kernels: isolated (L2 flushed before
+    each copy, median of 20) or, given l2, back to back over rotating buffer
+    pairs totalling more than 3x L2 (CUDA graph)."""
     half = max(nbytes // 2, 16)
-    src = torch.empty(half, dtype=torch.uint8, device=dev)
-    dst = torch.empty(half, dtype=torch.uint8, device=dev)
-    t = time_ops(torch, stream, flush, [("copy", lambda: dst.copy_(src))], 20, 3)
-    med = statistics.median(t[0])
-    gbs = 2 * half / (med * 1e-3) / 1e9
-    return {"us": round(med * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+    if l2 is None:
+        src = torch.empty(half, dtype=torch.uint8, device=dev)
+        dst = torch.empty(half, dtype=torch.uint8, device=dev)
+        t = time_ops(torch, stream, flush, [("copy", lambda: dst.copy_(src))], 20, 3)
+        us = statistics.median(t[0]) * 1e3
+    else:
+        n = max(2, -(-3 * l2 // (2 * half)))
+        pairs = [(torch.empty(half, dtype=torch.uint8, device=dev),
+                  torch.empty(half, dtype=torch.uint8, device=dev)) for _ in range(n)]
+        us = graph_us(torch, stream, [lambda s=s_, d=d_: d.copy_(s) for s_, d_ in pairs])
+        del pairs
+    gbs = 2 * half / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
 
 
 def time_step_ops(torch, stream, flush, st, peak):
@@ -545,24 +683,43 @@ def time_step_ops(torch, stream, flush, st, peak):
     return row
 
 
-def breakdown(torch, R, stream, flush, dev, peak):
-    """Per-kernel effective GB/s on the other benchmark workloads, with a
-    plain copy of the top-K forward's bytes beside them (copy_ceiling)."""
+def steady_step_ops(torch, stream, sets, peak):
+    """The four kernels of a list of rotating buffer sets, each timed back to
+    back over the sets (CUDA graph of 3 rounds, median of 10 replays)."""
+    row = {}
+    first = sets[0]
+    for i, (n, _) in enumerate(first.ops()):
+        us = graph_us(torch, stream, [st.ops()[i][1] for st in sets])
+        gbs = first.bytes(n) / (us * 1e-6) / 1e9
+        row[n] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+    return row
+
+
+def breakdown(torch, R, stream, dev, peak, l2):
+    """Per-kernel effective GB/s on the other benchmark workloads in both
+    protocols (back to back over rotating buffer sets, and isolated with L2
+    flushed before each launch), with a plain device copy of the top-K
+    forward's bytes beside each (copy_ceiling)."""
     from score_top_expert_gb300.workloads import make_workload
+    flush = L2Flush(torch, dev)
     res = {}
-    for name, sfs, dts in (("t8192_e512_k22", ("softmax", "sigmoid"), ("f32",)),
-                           ("t8192_e2304_k36", ("softmax", "sigmoid"), ("f32",)),
-                           ("t8192_e256_k8", ("softmax", "sigmoid"), ("f32", "bf16")),
-                           ("t16384_e256_k8_grouped", ("sigmoid",), ("bf16",))):
+    for name, sfs, dts in (("t8192_e256_k8", ("softmax", "sigmoid"), ("f32", "bf16")),
+                           ("t16384_e256_k8_grouped", ("sigmoid",), ("bf16",)),
+                           ("t1024_e64_k4", ("softmax",), ("f32",))):
         for dt in dts:
             case, args = make_workload(name, dtype=dt)
             for sf in sfs:
-                st = Step(R, torch, case, args, dev, sf)
-                row = time_step_ops(torch, stream, flush, st, peak)
-                row["copy_ceiling"] = copy_ceiling(torch, stream, flush, dev,
-                                                   st.bytes("topk_fwd"), peak)
-                res[f"{name}/{sf}/{dt}"] = row
-                del st
+                sets = rotating_sets(R, torch, case, args, dev, sf, l2)
+                b = sets[0].bytes("topk_fwd")
+                res[f"{name}/{sf}/{dt}"] = {
+                    "steady": steady_step_ops(torch, stream, sets, peak),
+                    "isolated": time_step_ops(torch, stream, flush, sets[0], peak),
+                    "copy_ceiling": {"steady": copy_ceiling(torch, stream, flush, dev, b, peak,
+                                                            l2),
+                                     "isolated": copy_ceiling(torch, stream, flush, dev, b,
+                                                              peak)}}
+                del sets
+                torch.cuda.empty_cache()
     return res
 
 
@@ -603,59 +760,46 @@ def k_sweep(a):
             "peak_kind": peak_kind, "results": res}
 
 
-def steady_state(torch, R, stream, dev, peak, l2):
-    """Back-to-back launches: a CUDA graph of R launches of one kernel over N
-    rotating buffer sets whose bytes per launch total more than 3x L2 (no
-    flush; each launch also pays the write-backs its predecessors left in
-    L2), median of 10 replays; and the same for whole steps of the four
-    kernels on the headline workload."""
+# the target matrix: E x K x score function at 8192 fp32 tokens (the pairs of
+# the TransformerEngine page's softmax and sigmoid tables, "[Common] Optimize
+# fused router forward/backward kernels", Performance)
+MATRIX_E = ((512, "t8192_e512_k22"), (2304, "t8192_e2304_k36"))
+MATRIX_K = (22, 36)
+MATRIX_TARGET = 0.6
+
+
+def target_matrix(torch, R, stream, dev, peak, l2):
+    """The four kernels at every (E, K, score function) of the target matrix,
+    back to back over rotating buffer sets (more than 3x L2 per kernel), with
+    a device copy of the top-K forward's bytes under the same protocol, and
+    the whole step of four kernels."""
     from score_top_expert_gb300.workloads import make_workload
-    res = {"protocol": "CUDA graph of 3N back-to-back launches over N rotating buffer sets "
-                       "(> 3x L2 of bytes per launch), median of 10 replays, no flush"}
-
-    def graph_us(fns, reps_per_fn):
-        g = torch.cuda.CUDAGraph()
-        for fn in fns:
-            fn()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for fn in fns * reps_per_fn:
-                fn()
-        g.replay()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(10):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1) * 1e3)
-        del g
-        return statistics.median(times) / (len(fns) * reps_per_fn)
-
-    for name in ("t8192_e512_k22", "t8192_e2304_k36"):
-        case, args = make_workload(name)
-        first = Step(R, torch, case, args, dev, "softmax")
-        per_launch = min(first.bytes(n) for n, _ in first.ops())
-        nsets = max(2, -(-3 * l2 // per_launch))
-        steps = [first] + [Step(R, torch, case, args, dev, "softmax") for _ in range(nsets - 1)]
-        row = {"buffer_sets": nsets}
-        for i, (n, _) in enumerate(first.ops()):
-            us = graph_us([st.ops()[i][1] for st in steps], 3)
-            gbs = first.bytes(n) / (us * 1e-6) / 1e9
-            row[n] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
-        if name == WORKLOAD:
-            step_fns = [fn for st in steps for _, fn in st.ops()]
-            us = graph_us(step_fns, 3) * len(first.ops())
-            step_bytes = sum(first.bytes(n) for n, _ in first.ops())
-            res["step"] = {"workload": name, "us": round(us, 2),
-                           "gbs": round(step_bytes / (us * 1e-6) / 1e9, 1),
-                           "frac": round(step_bytes / (us * 1e-6) / 1e9 / peak, 3)}
-        res[name] = row
-        del steps, first
-        torch.cuda.empty_cache()
+    res = {"protocol": "CUDA graph of 3 rounds of back-to-back launches over N rotating "
+                       "buffer sets (> 3x L2 of bytes per launch), median of 10 replays, "
+                       "no flush", "target_frac": MATRIX_TARGET, "cells": {}}
+    below = []
+    for E, name in MATRIX_E:
+        for K in MATRIX_K:
+            case, args = make_workload(name, K=K)
+            for sf in ("softmax", "sigmoid"):
+                sets = rotating_sets(R, torch, case, args, dev, sf, l2)
+                row = steady_step_ops(torch, stream, sets, peak)
+                first = sets[0]
+                step_fns = [fn for st in sets for _, fn in st.ops()]
+                us = graph_us(torch, stream, step_fns) * len(first.ops())
+                sb = sum(first.bytes(n) for n, _ in first.ops())
+                row["step"] = {"us": round(us, 2), "gbs": round(sb / (us * 1e-6) / 1e9, 1),
+                               "frac": round(sb / (us * 1e-6) / 1e9 / peak, 3)}
+                row["copy_ceiling"] = copy_ceiling(torch, stream, None, dev,
+                                                   first.bytes("topk_fwd"), peak, l2)
+                row["buffer_sets"] = len(sets)
+                key = f"e{E}_k{K}/{sf}"
+                res["cells"][key] = row
+                below += [f"{key}/{n}" for n, _ in first.ops()
+                          if row[n]["frac"] < MATRIX_TARGET]
+                del sets, first, step_fns
+                torch.cuda.empty_cache()
+    res["below_target"] = below
     return res
 
 
@@ -808,6 +952,26 @@ def _oracle_rows_worker(arg):
     return done, time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for placing the
+    oracle's timing."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(seconds: float):
     """The oracle on the host: all cores (one process per core, rows split
     between them; the reported value) and one thread."""
@@ -842,10 +1006,11 @@ def cpu_baseline(seconds: float):
     except Exception as exc:  # a host without process pools still gets the one-thread figure
         allc = None
         single["note"] = f"all-cores run unavailable: {type(exc).__name__}"
+    model = cpu_model()
     if allc is None:
-        return dict(single, kind="oracle")
+        return dict(single, kind="oracle", cpu_model=model)
     return {"value": allc["value"], "unit": "GB/s", "cores": allc["cores"], "kind": "oracle",
-            "sample": allc["sample"], "single_thread": single}
+            "cpu_model": model, "sample": allc["sample"], "single_thread": single}
 
 
 def reference_arm(a, world, rank):
@@ -879,7 +1044,7 @@ def reference_arm(a, world, rank):
             "config": {"workload": f"{WORKLOAD} softmax: the four router ops (bounded sample)",
                        "tokens": 8192, "experts": 2304, "topk": 36},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -887,8 +1052,9 @@ def reference_arm(a, world, rank):
 
 def profile_run(a):
     """Untimed steps for an ncu capture, no flush.  --profile-ops step: the
-    four router ops once per step; next: the compact forward, the expert
-    maps (three kernels), the aux-loss forward (two kernels) and backward."""
+    four router ops once per step, steps rotating over the headline's buffer
+    sets; next: the compact forward, the expert maps, the aux-loss forward and
+    backward."""
     import torch
 
     import score_top_expert_gb300.router as R
@@ -898,8 +1064,18 @@ def profile_run(a):
     dev = torch.device("cuda", 0)
     case, args = make_workload(a.profile)
     if a.profile_ops == "step":
-        st = Step(R, torch, case, args, dev, a.profile_score)
-        ops = [fn for _, fn in st.ops()]
+        # the bench's own protocol: back to back over rotating buffer sets
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        sets = rotating_sets(R, torch, case, args, dev, a.profile_score, l2)
+        ops = []
+        for w in range(a.warmup + a.steps):
+            ops += [fn for _, fn in sets[w % len(sets)].ops()]
+        for fn in ops:
+            fn()
+        torch.cuda.synchronize()
+        print(f"profile run done: {a.profile} {a.profile_ops} {a.profile_score}, "
+              f"{a.warmup + a.steps} steps over {len(sets)} buffer sets")
+        return
     else:
         T, E = case.logits.shape
         K = args["K"]

@@ -87,12 +87,28 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+# The per-call path is kept lean for decode-sized calls, where the host cost
+# of a call is most of its latency: pointers go to ctypes as plain integers
+# (the argtypes convert them), the stream as the raw handle of torch's current
+# stream, and devices as indices.
+try:
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+    _cur_dev = torch._C._cuda_getDevice
+except AttributeError:  # pragma: no cover - older torch
+    def _raw_stream(i):
+        return torch.cuda.current_stream(i).cuda_stream
+
+    _cur_dev = torch.cuda.current_device
+
+
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(device: torch.device) -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+def _stream(device) -> int:
+    """Raw handle of torch's current stream on ``device`` (a torch.device or
+    an index)."""
+    return _raw_stream(device if isinstance(device, int) else device.index)
 
 
 class _NoSwitch:
@@ -106,12 +122,13 @@ class _NoSwitch:
 _NO_SWITCH = _NoSwitch()
 
 
-def _on(device: torch.device):
-    """Make `device` current for the library call; no switch (and none of its
-    cost) when it already is."""
-    if device.index is None or device.index == torch.cuda.current_device():
+def _on(device):
+    """Make ``device`` (a torch.device or an index) current for the library
+    call; no switch (and none of its cost) when it already is."""
+    idx = device if isinstance(device, int) else device.index
+    if idx is None or idx == _cur_dev():
         return _NO_SWITCH
-    return torch.cuda.device(device)
+    return torch.cuda.device(idx)
 
 
 def _check(fn: str, code: int):
@@ -126,7 +143,7 @@ def _as_input(t: torch.Tensor, name: str, dtypes) -> torch.Tensor:
         raise ValueError(f"{name} dtype {t.dtype} not in {dtypes}")
     if t.dim() != 2:
         raise ValueError(f"{name} must be [T, E]")
-    return t.contiguous()
+    return t if t.is_contiguous() else t.contiguous()
 
 
 def _score(score_func: str) -> int:
@@ -137,11 +154,14 @@ def _score(score_func: str) -> int:
 
 
 def _out(t, shape, dtype, device, name):
+    """A caller's output tensor, checked (shape, dtype, contiguity, device),
+    or a new one.  ``device``: a torch.device with an index."""
     if t is None:
         return torch.empty(shape, dtype=dtype, device=device)
-    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() \
-            or t.device != device:
-        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
+    if t.shape != shape or t.dtype != dtype or not t.is_contiguous() \
+            or t.get_device() != device.index:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape} on "
+                         f"{device}")
     return t
 
 
@@ -152,21 +172,23 @@ def router_topk_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax",
     """Top-K router forward.  Returns (probs [T,E] logits dtype,
     routing_map [T,E] bool, scores [T,E] float32)."""
     logits = _as_input(logits, "logits", _DTYPE)
-    T, E = logits.shape
+    shape = logits.shape
+    T, E = shape
     dev = logits.device
+    dt = logits.dtype
     if expert_bias is not None:
         if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
-                or expert_bias.device != dev:
+                or expert_bias.get_device() != dev.index:
             raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
         expert_bias = expert_bias.contiguous()
-    probs = _out(probs, (T, E), logits.dtype, dev, "probs")
-    routing_map = _out(routing_map, (T, E), torch.bool, dev, "routing_map")
-    scores = _out(scores, (T, E), torch.float32, dev, "scores")
+    probs = _out(probs, shape, dt, dev, "probs")
+    routing_map = _out(routing_map, shape, torch.bool, dev, "routing_map")
+    scores = _out(scores, shape, torch.float32, dev, "scores")
     with _on(dev):
-        rc = lib().router_topk_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
+        rc = lib().router_topk_fwd(logits.data_ptr(), _DTYPE[dt], T, E, int(K),
                                    _score(score_func), int(num_groups), int(group_topk),
-                                   float(scaling_factor), _ptr(expert_bias), _ptr(probs),
-                                   _ptr(routing_map), _ptr(scores), _stream(dev))
+                                   float(scaling_factor), _ptr(expert_bias), probs.data_ptr(),
+                                   routing_map.data_ptr(), scores.data_ptr(), _stream(dev))
     _check("router_topk_fwd", rc)
     return probs, routing_map, scores
 
@@ -177,7 +199,8 @@ def _rows_out(t, T, K, dtype, device, name):
     if t is None:
         return torch.empty((T, K), dtype=dtype, device=device)
     if t.dim() != 2 or t.shape[0] != T or t.shape[1] < K or t.dtype != dtype \
-            or t.device != device or (T > 1 and t.stride(1) != 1) or t.stride(0) < K:
+            or t.get_device() != device.index or (T > 1 and t.stride(1) != 1) \
+            or t.stride(0) < K:
         raise ValueError(f"{name} must be a {dtype} [T, >= K] tensor with unit column "
                          f"stride and row stride >= K")
     return t
@@ -203,7 +226,7 @@ def router_topk_fwd_compact(logits: torch.Tensor, K: int, score_func: str = "sof
     K = int(K)
     if expert_bias is not None:
         if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
-                or expert_bias.device != dev:
+                or expert_bias.get_device() != dev.index:
             raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
         expert_bias = expert_bias.contiguous()
     topk_weights = _rows_out(topk_weights, T, K, torch.float32, dev, "topk_weights")
@@ -290,7 +313,7 @@ def router_topk_fwd_maps(logits: torch.Tensor, K: int, score_func: str = "softma
     K = int(K)
     if expert_bias is not None:
         if expert_bias.dtype != torch.float32 or expert_bias.numel() != E \
-                or expert_bias.device != dev:
+                or expert_bias.get_device() != dev.index:
             raise ValueError("expert_bias must be a float32 [E] tensor on the logits' device")
         expert_bias = expert_bias.contiguous()
     topk_weights = _rows_out(topk_weights, T, K, torch.float32, dev, "topk_weights")
@@ -455,9 +478,9 @@ def router_aux_loss_fwd_noalloc(aux_scores: torch.Tensor, routing_map: torch.Ten
         raise ValueError("aux_scores and routing_map must have the same shape")
     T, E = aux_scores.shape
     dev = aux_scores.device
-    if loss.device != dev or loss.dtype != torch.float32 or loss.numel() < 1:
+    if loss.get_device() != dev.index or loss.dtype != torch.float32 or loss.numel() < 1:
         raise ValueError("loss must be a float32 tensor on the inputs' device")
-    if (tokens_per_expert.device != dev or tokens_per_expert.dtype != torch.int32
+    if (tokens_per_expert.get_device() != dev.index or tokens_per_expert.dtype != torch.int32
             or tokens_per_expert.numel() != E or not tokens_per_expert.is_contiguous()):
         raise ValueError("tokens_per_expert must be a contiguous int32 [E] tensor on the "
                          "inputs' device")
