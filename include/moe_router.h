@@ -147,7 +147,9 @@ MR_API int router_topk_fwd(const void* logits, mr_dtype dtype, int T, int E, int
  *   token_expert_indices[t * K + k]   k * T + t (int32), when not NULL
  * Columns K .. ld - 1 of the weights and indices are left untouched.
  * probs, routing_map and scores are as in router_topk_fwd, each written only
- * when its pointer is not NULL (the values are identical).
+ * when its pointer is not NULL: the map and the scores identical, the
+ * probabilities of the renormalising score functions (sigmoid, post-softmax)
+ * equal up to the order in which the K selected scores are summed.
  *
  * Errors: as router_topk_fwd, with probs, routing_map and scores optional;
  * MR_ERR_INVALID also for ld_weights < K, ld_indices < K, or NULL
@@ -400,15 +402,26 @@ MR_API const char* moe_router_strerror(int code);
  *   MR_PATH_STAGED: each warp streams rows through shared memory with bulk
  *     copies (bias and groups included; E % 4 == 0 for fp32, E % 8 == 0 for
  *     bf16; 16-byte aligned tensors).  router_topk_fwd_maps's one-launch
- *     decode form always runs on this path.
- * MR_PATH_AUTO takes the staged path where it applies, except for batches of
- * 8192 or more tokens with E < 128 (the segment path is faster there).  A
- * forced path that does not apply to a call falls back to the automatic
- * choice.  Process-wide; meant for tests and benchmarks.  The environment
- * variable MOE_ROUTER_FORCE_PATH (auto|segment|staged) sets the initial
- * value.  Returns the previous value, or MR_ERR_INVALID for an unknown path.
+ *     decode form always runs on this path;
+ *   MR_PATH_REGISTER: rows arrive by bulk copy like the staged path and are
+ *     then held in the registers of one warp, the K-th largest logit found
+ *     by bisection over compacted candidates (router_topk_fwd and
+ *     router_aux_scores_fwd with E <= 512, no bias and no groups, the staged
+ *     path's alignment).
+ * MR_PATH_AUTO takes the register path where it applies and the staged path
+ * elsewhere, except for batches of 8192 or more tokens with E < 128 (the
+ * segment path is faster there).  A forced path that does not apply to a
+ * call falls back to the automatic choice.  Process-wide; meant for tests and
+ * benchmarks.  The environment variable MOE_ROUTER_FORCE_PATH
+ * (auto|segment|staged|register) sets the initial value.  Returns the
+ * previous value, or MR_ERR_INVALID for an unknown path.
  */
-typedef enum { MR_PATH_AUTO = 0, MR_PATH_SEGMENT = 1, MR_PATH_STAGED = 2 } mr_path;
+typedef enum {
+  MR_PATH_AUTO = 0,
+  MR_PATH_SEGMENT = 1,
+  MR_PATH_STAGED = 2,
+  MR_PATH_REGISTER = 3
+} mr_path;
 MR_API int moe_router_force_path(int path);
 
 /*

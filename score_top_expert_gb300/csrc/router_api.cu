@@ -45,6 +45,7 @@ int current_path() {
   if (const char* env = std::getenv("MOE_ROUTER_FORCE_PATH")) {
     if (std::strcmp(env, "segment") == 0) p = MR_PATH_SEGMENT;
     else if (std::strcmp(env, "staged") == 0) p = MR_PATH_STAGED;
+    else if (std::strcmp(env, "register") == 0) p = MR_PATH_REGISTER;
   }
   int expected = -1;
   g_path.compare_exchange_strong(expected, p);
@@ -246,6 +247,103 @@ bool use_staged(int E, int dt, bool aligned, int T) {
   if (path == MR_PATH_SEGMENT) return false;
   if (path == MR_PATH_STAGED) return true;
   return E >= 128 || T < 8192;
+}
+
+// ---- register-resident forward plans, computed once per (device, shape) -----
+struct RegPlanEntry {
+  PlanKey key;
+  RegPlan plan;
+  bool valid;
+};
+RegPlanEntry g_reg_plans[kPlanCache];
+int g_nreg_plans = 0;
+
+RegLayout reg_layout(int nc, int dt) {
+  RegLayout L{};
+  const int d = dt == MR_F32 ? 4 : 2;
+  L.stage_bytes = 4 * 32 * nc * d;  // one padded row
+  L.cand_off = 2 * L.stage_bytes;
+  L.bar_off = round_up(L.cand_off + kRegCap * 4, 16);
+  L.warp_bytes = round_up(L.bar_off + 16, 128);
+  return L;
+}
+
+int occupancy_reg_any(int sf, int dt, const RegPlan& p) {
+  if (sf == MR_SOFTMAX)
+    return dt == MR_F32 ? occupancy_reg_softmax_f32(p) : occupancy_reg_softmax_bf16(p);
+  if (sf == MR_SOFTMAX_POST)
+    return dt == MR_F32 ? occupancy_reg_softmaxpost_f32(p) : occupancy_reg_softmaxpost_bf16(p);
+  return dt == MR_F32 ? occupancy_reg_sigmoid_f32(p) : occupancy_reg_sigmoid_bf16(p);
+}
+
+// Warps per block that keep the most warps resident per SM (fewer per block
+// on a tie: finer grid balance).
+bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int E, RegPlan* out) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < g_nreg_plans; ++i) {
+      const PlanKey& k = g_reg_plans[i].key;
+      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E) {
+        *out = g_reg_plans[i].plan;
+        return g_reg_plans[i].valid;
+      }
+    }
+  }
+  RegPlan p{};
+  p.nc = E <= 256 ? 2 : 4;
+  p.full = E == 128 * p.nc;
+  p.op = op;
+  p.layout = reg_layout(p.nc, dt);
+  int best_warps = 0, best_per_sm = 0;
+  for (int w = 2; w <= kRegMaxWarps; w += 2) {
+    if (static_cast<long long>(w) * p.layout.warp_bytes > di.smem_per_block) break;
+    RegPlan q = p;
+    q.warps_per_block = w;
+    const int per_sm = occupancy_reg_any(sf, dt, q);
+    if (per_sm * w > best_warps) {
+      best_warps = per_sm * w;
+      best_per_sm = per_sm;
+      p.warps_per_block = w;
+    }
+  }
+  const bool valid = best_warps > 0;
+  p.max_blocks = best_per_sm * di.sms;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_nreg_plans < kPlanCache)
+    g_reg_plans[g_nreg_plans++] = RegPlanEntry{{dev, sf, dt, op, 0, E, 0}, p, valid};
+  *out = p;
+  return valid;
+}
+
+// The register-resident forward serves the top-K router (op 0) and the aux
+// scores (op 1) without bias or groups for aligned rows of at most 512
+// experts, wherever the automatic choice would take the staged path.
+bool use_reg(int E, int dt, bool aligned, int T, int km, int op) {
+  if (km != 0 || op > 1 || E > 512 || !aligned || !staged_shape_ok(E, dt)) return false;
+  const int path = current_path();
+  if (path == MR_PATH_SEGMENT || path == MR_PATH_STAGED) return false;
+  if (path == MR_PATH_REGISTER) return true;
+  return E >= 128 || T < 8192;
+}
+
+int launch_reg_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st) {
+  DeviceInfo di{};
+  if (!device_info(&di)) return MR_ERR_CUDA;
+  RegPlan p{};
+  if (!reg_plan(di, sf, dt, op, a.E, &p)) return MR_ERR_CUDA;
+  cudaError_t e;
+  if (sf == MR_SOFTMAX)
+    e = dt == MR_F32 ? launch_reg_softmax_f32(a, p, di.status, st)
+                     : launch_reg_softmax_bf16(a, p, di.status, st);
+  else if (sf == MR_SOFTMAX_POST)
+    e = dt == MR_F32 ? launch_reg_softmaxpost_f32(a, p, di.status, st)
+                     : launch_reg_softmaxpost_bf16(a, p, di.status, st);
+  else
+    e = dt == MR_F32 ? launch_reg_sigmoid_f32(a, p, di.status, st)
+                     : launch_reg_sigmoid_bf16(a, p, di.status, st);
+  return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
 int launch_staged_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStream_t st) {
@@ -495,6 +593,8 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
                               ? gl
                               : 0;
   }
+  if (use_reg(E, dtype, vec, T, km, op))
+    return launch_reg_any(score_func, dtype, a, op, reinterpret_cast<cudaStream_t>(stream));
   if (staged)
     return launch_staged_any(score_func, dtype, a, op, km, reinterpret_cast<cudaStream_t>(stream));
   return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
@@ -628,6 +728,8 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.T = T; a.E = E; a.K = K;
   a.spec_target = spec_target(K);
   a.scaling = 1.0f;
+  if (use_reg(E, dtype, vec, T, 0, 1))
+    return launch_reg_any(score_func, dtype, a, 1, reinterpret_cast<cudaStream_t>(stream));
   if (use_staged(E, dtype, vec, T))
     return launch_staged_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));
   FwdConfig c{};
@@ -676,7 +778,8 @@ const char* moe_router_strerror(int code) {
 }
 
 int moe_router_force_path(int path) {
-  if (path != MR_PATH_AUTO && path != MR_PATH_SEGMENT && path != MR_PATH_STAGED)
+  if (path != MR_PATH_AUTO && path != MR_PATH_SEGMENT && path != MR_PATH_STAGED &&
+      path != MR_PATH_REGISTER)
     return MR_ERR_INVALID;
   const int prev = current_path();
   g_path.store(path, std::memory_order_relaxed);

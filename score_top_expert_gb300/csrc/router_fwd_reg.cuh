@@ -1,0 +1,402 @@
+// Router forward for rows of at most 512 experts, each row held in the
+// registers of one warp (no bias, no groups; top-K router and aux scores).
+//
+// A warp owns one token row at a time and walks the rows of the batch
+// persistently (row, row + all warps, ...).  Rows arrive in shared memory by
+// one bulk copy each into two stages per warp; as soon as a row is in
+// registers its stage is refilled with the row two steps ahead, so every
+// warp keeps two rows in flight.  Lane l holds chunks c = l + 32 j (j < NC)
+// of the row, chunk c being experts 4c .. 4c + 3.
+//
+// Per row:
+//   1  row maximum (a warp max-reduction of ordered keys) and each lane's two
+//      half maxima (64 disjoint group maxima);
+//   2  scores: softmax e = exp(x - max) with the row sum, or sigmoid s,
+//      kept in registers;
+//   3  a threshold t with K <= n <= 128 logits at or above it: the previous
+//      row's estimate when it verifies, else a lower bound from the group
+//      maxima (if K of them reach t, so do K logits) found by bisection on
+//      the value; rows where neither works take step 5 over the whole row;
+//   4  the logits >= t are compacted into shared memory (a prefix count
+//      gives each lane its slots), each lane takes up to four of them back
+//      into registers, and a bisection on the ordered key, counting
+//      candidates with one warp reduction per step, finds the largest key
+//      with exactly K logits at or above it.  A bisection that closes on a
+//      single key with more than K logits at or above it has found a tie:
+//      the logits above that key are taken, and the equal ones in index
+//      order up to K by a prefix count;
+//   5  (no usable t) the same bisection counting over the whole row;
+//   6  outputs straight from registers: probs, map and scores (top-K), or
+//      q, map and the sigmoid (aux scores).
+// The selection keys on the logit, which is exact: softmax and sigmoid are
+// strictly increasing.  Ties go to the lower expert index.
+#pragma once
+
+#include <climits>
+#include <type_traits>
+
+#include "router_common.cuh"
+#include "router_fwd.cuh"
+#include "router_tma.cuh"
+
+namespace moe_router {
+
+// Byte offsets inside one warp's slice of shared memory (set on the host).
+struct RegLayout {
+  int stage_bytes;  // 32 * NC chunks of four logits (one padded row)
+  int cand_off;     // kRegCap candidate logits (fp32)
+  int bar_off;      // two mbarriers
+  int warp_bytes;   // slice size, multiple of 128
+};
+
+constexpr int kRegMaxWarps = 16;
+constexpr int kRegCap = 128;   // candidates one row may carry into the bisection
+constexpr int kRegBoundSlack = 8;  // group maxima above K the bound may leave
+constexpr int kRegBoundSteps = 12;
+
+// Ordered keys restricted to the precision of the logits: bf16 rows bisect
+// on the 16 high bits (every bf16 value is one 16-bit key), fp32 rows on all
+// 32.  to_float(k) is the smallest logit value with key k.
+template <int DT>
+struct RowKey {
+  static constexpr int SH = DT == DT_F32 ? 0 : 16;
+  __device__ __forceinline__ static uint32_t of(float f) { return ordered_key(f) >> SH; }
+  __device__ __forceinline__ static float to_float(uint32_t k) {
+    if constexpr (SH == 0) {
+      return key_to_float(k);
+    } else {
+      return key_to_float((k << 16) | ((k & 0x8000u) ? 0u : 0xffffu));
+    }
+  }
+  // key of the lowest finite logit (-FLT_MAX, or the lowest bf16 value)
+  __device__ __forceinline__ static uint32_t lowest() { return SH == 0 ? 0x00800000u : 0x0080u; }
+};
+
+__device__ __forceinline__ int warp_add(int v) {
+  return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(v)));
+}
+
+// Load one chunk of four logits from a stage.
+template <int DT>
+__device__ __forceinline__ void stage_chunk(const unsigned char* stage, int c, float* x) {
+  if constexpr (DT == DT_F32) {
+    float4 t;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(t.x), "=f"(t.y), "=f"(t.z), "=f"(t.w)
+                 : "r"(smem_addr(stage + 16 * c)));
+    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+  } else {
+    uint32_t lo, hi;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi)
+                 : "r"(smem_addr(stage + 8 * c)));
+    x[0] = __uint_as_float(lo << 16);
+    x[1] = __uint_as_float(lo & 0xffff0000u);
+    x[2] = __uint_as_float(hi << 16);
+    x[3] = __uint_as_float(hi & 0xffff0000u);
+  }
+}
+
+template <int SF, int DT, int NC, int OP, bool FULL>
+__global__ void __launch_bounds__(kRegMaxWarps * 32)
+router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
+  pdl_enter();
+  static_assert(NC == 2 || NC == 4, "rows of up to 256 or 512 experts");
+  constexpr int N = 4 * NC;  // logits per lane
+  constexpr int D = DT == DT_F32 ? 4 : 2;
+  constexpr unsigned kFull = 0xffffffffu;
+  using RK = RowKey<DT>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  unsigned char* base = smem + warp * L.warp_bytes;
+  float* cand = reinterpret_cast<float*>(base + L.cand_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
+
+  const int E = a.E, K = a.K, T = a.T;
+  const int nchunks = E >> 2;
+  const uint32_t row_bytes = static_cast<uint32_t>(E) * D;
+  const int nwarps = gridDim.x * wpb;
+  const unsigned char* src = static_cast<const unsigned char*>(a.logits);
+  const int margin = a.spec_target - (K - 1);  // candidates above K the estimate aims for
+
+  if (lane == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int row0 = blockIdx.x * wpb + warp;
+  if (lane == 0) {
+    if (row0 < T)
+      bulk_load(base, src + static_cast<size_t>(row0) * row_bytes, row_bytes, &bars[0]);
+    if (row0 + nwarps < T)
+      bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nwarps) * row_bytes,
+                row_bytes, &bars[1]);
+  }
+
+  bool have_spec = false;  // an estimate carried over from the previous row
+  float spec_t = 0.0f;
+  uint32_t phase = 0;
+#pragma unroll 1
+  for (int it = 0;; ++it) {
+    const int row = row0 + it * nwarps;
+    if (row >= T) break;  // uniform over the warp
+    const int b = it & 1;
+    if (!__all_sync(kFull, mbar_wait_bounded(&bars[b], (phase >> b) & 1u))) {
+      // record the failure, let the other stage's copy (if any) land, leave
+      if (lane == 0) {
+        atomicExch(status, kDeviceWaitTimeout);
+        if (row + nwarps < T) mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
+      }
+      __syncwarp();
+      return;
+    }
+    phase ^= 1u << b;
+    unsigned char* stage = base + b * L.stage_bytes;
+
+    // ---- 1: the row in registers, maxima; the stage takes the next row ----------
+    float x[N];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int c = lane + 32 * j;
+      stage_chunk<DT>(stage, c, &x[4 * j]);
+      if constexpr (!FULL) {
+        if (c >= nchunks) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[4 * j + u] = -INFINITY;
+        }
+      }
+    }
+    float hm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const float m4 = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
+      hm[j < NC / 2 ? 0 : 1] = fmaxf(hm[j < NC / 2 ? 0 : 1], m4);
+    }
+    // every real row has a finite maximum (padding is -inf, inputs are finite)
+    const float row_max =
+        key_to_float(__reduce_max_sync(kFull, ordered_key(fmaxf(hm[0], hm[1]))));
+    // the maximum consumed every logit read from the stage: refill it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int nr = row + 2 * nwarps;
+      if (nr < T) bulk_load(stage, src + static_cast<size_t>(nr) * row_bytes, row_bytes, &bars[b]);
+    }
+    const size_t off = static_cast<size_t>(row) * static_cast<size_t>(E);
+
+    // ---- 2: scores and their row sum ----------------------------------------------
+    const float max_l2e = row_max * kLog2e;
+    float w[N];  // softmax: e = exp(x - max); sigmoid: s (padding: exactly 0)
+    // summed in the staged forward's order (pairs within a chunk, chunks
+    // alternating between two sums, then the butterfly), so that the scores
+    // are bit for bit those of the other forward paths
+    float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = 4 * j + u;
+        if constexpr (SF != SF_SIGMOID) w[k] = exp_shifted(x[k], max_l2e);
+        else w[k] = sigmoid_f32(x[k]);
+      }
+      const float add = (w[4 * j] + w[4 * j + 1]) + (w[4 * j + 2] + w[4 * j + 3]);
+      if (j & 1) sum1 += add; else sum0 += add;
+    }
+    constexpr bool kNeedSum = SF != SF_SIGMOID || OP == 1;
+    float inv = 1.0f;
+    if constexpr (kNeedSum) inv = 1.0f / seg_sum<32>(sum0 + sum1);
+
+    // ---- 3: a candidate threshold ---------------------------------------------------
+    auto count_ge = [&](float t) {
+      int c = 0;
+#pragma unroll
+      for (int k = 0; k < N; ++k) c += x[k] >= t;
+      return c;
+    };
+    float t = 0.0f;
+    int cnt = 0, n = 0;
+    bool ok = false;
+    if (have_spec) {
+      t = spec_t;
+      cnt = count_ge(t);
+      n = warp_add(cnt);
+      ok = n >= K && n <= kRegCap;
+    }
+    if (!ok) {
+      // bisection on the value between the smallest finite group maximum
+      // (every real group at or above it) and the row maximum; any value
+      // with K group maxima at or above it has K logits at or above it
+      const float g0 = hm[0] == -INFINITY ? INFINITY : hm[0];  // padding groups left out
+      const float g1 = hm[1] == -INFINITY ? INFINITY : hm[1];
+      const float gl = fminf(g0, g1);
+      const float gmin = key_to_float(
+          __reduce_min_sync(kFull, gl == INFINITY ? 0xffffffffu : ordered_key(gl)));
+      int gn = warp_add((hm[0] != -INFINITY) + (hm[1] != -INFINITY));
+      if (gn >= K) {
+        float blo = gmin, bhi = row_max;
+#pragma unroll 1
+        for (int s = 0; s < kRegBoundSteps && gn > K + kRegBoundSlack; ++s) {
+          const float mid = 0.5f * blo + 0.5f * bhi;
+          if (mid == blo || mid == bhi) break;
+          const int c = warp_add((hm[0] >= mid) + (hm[1] >= mid));
+          if (c >= K) {
+            blo = mid;
+            gn = c;
+          } else {
+            bhi = mid;
+          }
+        }
+        t = blo;
+        cnt = count_ge(t);
+        n = warp_add(cnt);
+        ok = n <= kRegCap;  // n >= K holds by construction
+      }
+    }
+
+    // ---- 4 / 5: exact K-th largest key by bisection -------------------------------
+    uint32_t lo, hi = RK::of(row_max) + 1u;
+    int n_lo, n_hi = 0;
+    auto bisect = [&](auto count_at) {
+#pragma unroll 1
+      while (n_lo != K && hi - lo > 1u) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        const int c = warp_add(count_at(RK::to_float(mid)));
+        if (c >= K) {
+          lo = mid;
+          n_lo = c;
+        } else {
+          hi = mid;
+          n_hi = c;
+        }
+      }
+    };
+    if (ok) {
+      // compact the candidates: the lane's logits >= t go to its slots
+      int pos = seg_exclusive_scan<32>(cnt);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        if (x[k] >= t) cand[pos++] = x[k];
+      }
+      __syncwarp();
+      auto slot = [&](int r) { return 32 * r + lane < n ? cand[32 * r + lane] : -INFINITY; };
+      // the smallest key whose value is >= t: the logits at or above it are
+      // exactly the n candidates (t need not lie on the key grid of bf16 rows)
+      lo = RK::of(t);
+      if (RK::to_float(lo) < t) ++lo;
+      n_lo = n;
+      if (n <= 32) {
+        const float o0 = slot(0);
+        __syncwarp();  // the slots are free again (the next row writes them)
+        bisect([&](float m) { return static_cast<int>(o0 >= m); });
+      } else if (n <= 64) {
+        const float o0 = slot(0), o1 = slot(1);
+        __syncwarp();
+        bisect([&](float m) { return (o0 >= m) + (o1 >= m); });
+      } else {
+        const float o0 = slot(0), o1 = slot(1), o2 = slot(2), o3 = slot(3);
+        __syncwarp();
+        bisect([&](float m) { return (o0 >= m) + (o1 >= m) + (o2 >= m) + (o3 >= m); });
+      }
+    } else {
+      lo = RK::lowest();
+      n_lo = E;  // every real logit is finite
+      bisect(count_ge);
+    }
+    const float v = RK::to_float(lo);
+    int ti = INT_MAX;  // selected: x > v, or x == v with index <= ti
+    if (n_lo != K) {
+      // tie at v: n_hi logits above it; the (K - n_hi)-th equal one in index
+      // order (chunk j covers experts 128 j .. 128 j + 127 in lane order)
+      const int need = K - n_hi;
+      int run = 0;
+      ti = -1;
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        int e = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) e += x[4 * j + u] == v;
+        const int excl = seg_exclusive_scan<32>(e);
+        const int tot = __shfl_sync(kFull, excl + e, 31);
+        int mine = -1;
+        if (run + excl < need && run + excl + e >= need) {
+          int left = need - run - excl;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (x[4 * j + u] == v && --left == 0 && mine < 0) mine = 4 * (lane + 32 * j) + u;
+        }
+        const unsigned who = __ballot_sync(kFull, mine >= 0);
+        if (who) {
+          ti = __shfl_sync(kFull, mine, __ffs(who) - 1);
+          break;
+        }
+        run += tot;
+      }
+    }
+
+    // next row's estimate: aim for K + margin candidates, interpolating
+    // between this row's threshold t (n at or above it) and v (K)
+    if (ok) {
+      const float span = n > K ? (v - t) * (static_cast<float>(margin) / static_cast<float>(n - K))
+                               : (row_max - t) * (static_cast<float>(margin) / static_cast<float>(K));
+      spec_t = v - span;
+      have_spec = true;
+    } else {
+      have_spec = false;
+    }
+
+    // ---- 6: outputs -----------------------------------------------------------------
+    auto emit = [&](auto tie_tag) {
+      constexpr bool kTie = decltype(tie_tag)::value;
+      auto sel = [&](int k, int idx) -> bool {
+        if constexpr (kTie) return x[k] > v || (x[k] == v && idx <= ti);
+        else return x[k] >= v;
+      };
+      [[maybe_unused]] float pf = a.scaling;  // probs factor (top-K router only)
+      if constexpr (OP == 0 && SF != SF_SOFTMAX) {
+        // renormalised over the selected: c / sum of their scores
+        float part = 0.0f;
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+          if (sel(k, 4 * (lane + 32 * (k >> 2)) + (k & 3))) part += w[k];
+        pf = a.scaling / seg_sum<32>(part);
+      } else if constexpr (OP == 0) {
+        pf = a.scaling * inv;
+      }
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        const int c = lane + 32 * j;
+        if (FULL || c < nchunks) {
+          bool m[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m[u] = sel(4 * j + u, 4 * c + u);
+          store_map4<true>(a.map, off, 4 * c, E, m);
+          float s[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? w[4 * j + u] * inv : w[4 * j + u];
+          if constexpr (OP == 0) {
+            float p[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[u] = m[u] ? w[4 * j + u] * pf : 0.0f;
+            store4<DT, true>(a.probs, off, 4 * c, E, p);
+            store4_f32<true>(a.scores, off, 4 * c, E, s);
+          } else if constexpr (SF == SF_SOFTMAX) {
+            store4_f32<true>(a.scores, off, 4 * c, E, s);
+            if (a.intermediate != nullptr) store4_f32<true>(a.intermediate, off, 4 * c, E, s);
+          } else {
+            float q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) q[u] = s[u] * inv;
+            store4_f32<true>(a.scores, off, 4 * c, E, q);
+            store4_f32<true>(a.intermediate, off, 4 * c, E, s);
+          }
+        }
+      }
+    };
+    if (ti == INT_MAX) emit(std::false_type{});
+    else emit(std::true_type{});
+  }
+}
+
+}  // namespace moe_router

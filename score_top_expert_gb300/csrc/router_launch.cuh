@@ -8,6 +8,7 @@
 
 #include "router_bwd.cuh"
 #include "router_fwd.cuh"
+#include "router_fwd_reg.cuh"
 #include "router_fwd_staged.cuh"
 
 namespace moe_router {
@@ -249,6 +250,85 @@ int staged_occupancy(const StagedPlan& p) {
 #undef MR_STAGED_OCC
   return 0;
 }
+
+// Register-resident forward (rows of up to 512 experts, no bias or groups,
+// OP 0 and 1): warps per block and the grid cap.
+struct RegPlan {
+  RegLayout layout;
+  int warps_per_block;
+  int max_blocks;  // resident blocks per SM x SMs
+  int nc;          // chunks of 4 experts per lane (2 or 4)
+  int op;          // 0 top-K router, 1 aux scores
+  bool full;       // E == 128 * nc
+};
+
+template <int SF, int DT, int NC, int OP, bool FULL>
+cudaError_t launch_reg_inst(const FwdArgs& a, const RegPlan& p, int* status, cudaStream_t st) {
+  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL>;
+  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
+  static std::atomic<int> granted[kSmemDevs];  // this kernel's record
+  const cudaError_t se = allow_smem(kern, smem, granted);
+  if (se != cudaSuccess) return se;
+  // rows go round-robin over the resident warps; when they take more than one
+  // round, the fewest blocks that still need the same number of rounds
+  const long long need = (static_cast<long long>(a.T) + p.warps_per_block - 1) / p.warps_per_block;
+  long long blocks = need;
+  if (need > p.max_blocks) {
+    const long long rounds = (need + p.max_blocks - 1) / p.max_blocks;
+    blocks = (need + rounds - 1) / rounds;
+  }
+  return launch_kernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(p.warps_per_block * 32),
+                       smem, st, a, p.layout, status);
+}
+
+template <int SF, int DT, int NC, int OP, bool FULL>
+int reg_blocks_per_sm(int warps_per_block, size_t smem) {
+  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, warps_per_block * 32, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+// OCC false: launch; true: resident blocks per SM (returned through *occ).
+template <int SF, int DT, bool OCC>
+cudaError_t reg_dispatch(const FwdArgs& a, const RegPlan& p, int* status, cudaStream_t st,
+                         int* occ) {
+  const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
+#define MR_REG_CASE(N, O, F)                                                         \
+  if (p.nc == N && p.op == O && p.full == F) {                                       \
+    if constexpr (OCC) {                                                             \
+      *occ = reg_blocks_per_sm<SF, DT, N, O, F>(p.warps_per_block, smem);            \
+      return cudaSuccess;                                                            \
+    } else {                                                                         \
+      return launch_reg_inst<SF, DT, N, O, F>(a, p, status, st);                     \
+    }                                                                                \
+  }
+  MR_REG_CASE(2, 0, true) MR_REG_CASE(2, 0, false) MR_REG_CASE(4, 0, true)
+  MR_REG_CASE(4, 0, false)
+  if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
+    MR_REG_CASE(2, 1, true) MR_REG_CASE(2, 1, false) MR_REG_CASE(4, 1, true)
+    MR_REG_CASE(4, 1, false)
+  }
+#undef MR_REG_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
+#define MR_DECLARE_REG(NAME)                                                           \
+  cudaError_t launch_reg_##NAME(const FwdArgs&, const RegPlan&, int*, cudaStream_t);   \
+  int occupancy_reg_##NAME(const RegPlan&);
+MR_DECLARE_REG(softmax_f32)
+MR_DECLARE_REG(softmax_bf16)
+MR_DECLARE_REG(sigmoid_f32)
+MR_DECLARE_REG(sigmoid_bf16)
+MR_DECLARE_REG(softmaxpost_f32)
+MR_DECLARE_REG(softmaxpost_bf16)
+#undef MR_DECLARE_REG
 
 // One (score function, dtype) pair per translation unit.
 cudaError_t launch_staged_softmax_f32(const FwdArgs&, const StagedPlan&, int*, cudaStream_t);

@@ -1,0 +1,14 @@
+// Instantiations of the register-resident router forward: softmax score, bf16 logits.
+#include "router_launch.cuh"
+
+namespace moe_router {
+cudaError_t launch_reg_softmax_bf16(const FwdArgs& a, const RegPlan& p, int* status,
+                                    cudaStream_t st) {
+  return reg_dispatch<SF_SOFTMAX, DT_BF16, false>(a, p, status, st, nullptr);
+}
+int occupancy_reg_softmax_bf16(const RegPlan& p) {
+  int n = 0;
+  reg_dispatch<SF_SOFTMAX, DT_BF16, true>(FwdArgs{}, p, nullptr, nullptr, &n);
+  return n;
+}
+}  // namespace moe_router

@@ -17,7 +17,7 @@ from . import build as _build
 
 MR_SOFTMAX, MR_SIGMOID, MR_SOFTMAX_POST = 0, 1, 2
 MR_F32, MR_BF16 = 0, 1
-MR_PATH_AUTO, MR_PATH_SEGMENT, MR_PATH_STAGED = 0, 1, 2
+MR_PATH_AUTO, MR_PATH_SEGMENT, MR_PATH_STAGED, MR_PATH_REGISTER = 0, 1, 2, 3
 STATUS = {0: "MR_OK", -1: "MR_ERR_INVALID", -2: "MR_ERR_UNSUPPORTED", -3: "MR_ERR_CUDA"}
 
 _SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID, "softmax_post": MR_SOFTMAX_POST}
@@ -404,9 +404,10 @@ def router_aux_scores_bwd(grad_scores: torch.Tensor, saved: torch.Tensor, K: int
 
 
 def force_path(path: str) -> str:
-    """Force the forward kernel path: 'auto', 'segment' or 'staged'; returns the
-    previous one."""
-    names = {"auto": MR_PATH_AUTO, "segment": MR_PATH_SEGMENT, "staged": MR_PATH_STAGED}
+    """Force the forward kernel path: 'auto', 'segment', 'staged' or 'register';
+    returns the previous one."""
+    names = {"auto": MR_PATH_AUTO, "segment": MR_PATH_SEGMENT, "staged": MR_PATH_STAGED,
+             "register": MR_PATH_REGISTER}
     prev = lib().moe_router_force_path(names[path])
     if prev < 0:
         raise RouterError("moe_router_force_path", prev)

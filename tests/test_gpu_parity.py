@@ -28,7 +28,7 @@ def R():
 
 
 DEV = "cuda:0"
-PATHS = ["auto", "segment", "staged"]
+PATHS = ["auto", "segment", "staged", "register"]
 
 
 @pytest.fixture(params=PATHS)
@@ -142,6 +142,26 @@ def test_aux_workload(R, path, name, sf):
     case, args = make_workload(name)
     rep = run_and_check_aux(R, case, args["K"], sf, ref_key=("aux", name, sf))
     record_near_ties(f"aux {name} {sf} f32", rep)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 3, 129, 1100])
+@pytest.mark.parametrize("E", [8, 16, 64, 120, 128, 136, 200, 256, 264, 384, 504, 512])
+def test_register_shapes(R, E, T, dt):
+    # the register-resident forward on every row shape it serves (E <= 512,
+    # E % 8 == 0): padded and full rows, both chunk counts, one to many rows
+    # per warp, K from 1 to 36 and K = E
+    prev = R.force_path("register")
+    try:
+        for K in sorted({1, min(E, 4), min(E, 22), min(E, 36), E if E <= 36 else 1}):
+            case = make_case(T, E, K, dtype=dt, sigma=1.5, seed=E * 13 + K + T)
+            for sf in ("softmax", "sigmoid", "softmax_post"):
+                run_and_check_topk(R, case, K, sf, c=2.5, check_bwd=False)
+                if sf != "softmax_post":
+                    run_and_check_aux(R, case, K, sf)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -390,6 +410,44 @@ def test_adversarial_rows(R, path, E, K):
             run_and_check_topk(R, case, K, sf, c=2.0)
             if dt == "f32" and sf != "softmax_post":
                 run_and_check_aux(R, case, K, sf)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E,K", [(256, 8), (512, 22), (512, 36), (384, 30)])
+def test_register_rows_in_sequence(R, E, K, dt):
+    # many rows per warp, so that each row starts from the previous row's
+    # threshold estimate: a mix of row kinds in a fixed cycle (normal, wide,
+    # integer-valued with heavy ties, adversarial, shifted and sorted rows), so the
+    # estimate fails and recovers over and over
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    rng = np.random.default_rng(E * 31 + K)
+    T = 12000
+    adv = adversarial_rows(E, K, rng)
+    x = np.empty((T, E), dtype=np.float32)
+    for i in range(T):
+        kind = i % 6
+        if kind == 0:
+            x[i] = rng.normal(0, 1, E)
+        elif kind == 1:
+            x[i] = rng.normal(0, 3, E)
+        elif kind == 2:
+            x[i] = rng.integers(-3, 4, E)
+        elif kind == 3:
+            x[i] = adv[(i // 6) % adv.shape[0]][rng.permutation(E)]
+        elif kind == 4:
+            x[i] = rng.normal(0, 1, E) + 10.0  # shifted (sigmoid keys stay distinct in f64)
+        else:
+            x[i] = np.sort(rng.normal(0, 1, E))
+    prev = R.force_path("register")
+    try:
+        case = make_case(T, E, K, dtype=dt, seed=5)
+        case.logits = x if dt == "f32" else round_to_bf16_values(x)
+        for sf in ("softmax", "sigmoid"):
+            run_and_check_topk(R, case, K, sf, c=2.5, check_bwd=False)
+            run_and_check_aux(R, case, K, sf)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
 
 
 def test_bounded_wait_reports_a_timeout(R):

@@ -44,7 +44,7 @@ def draw(rng):
         if opts:
             ng, gk = opts[int(rng.integers(len(opts)))]
     bias = rng.uniform(-0.1, 0.1, E).astype(np.float32) if rng.random() < 0.3 else None
-    path = str(rng.choice(["auto", "segment", "staged"]))
+    path = str(rng.choice(["auto", "segment", "staged", "register"]))
     lanes = int(rng.choice([0, 0, 8, 16, 32]))
     sigma = float(rng.choice([0.5, 1.0, 2.0]))
     return dict(E=E, K=K, T=T, sf=sf, dt=dt, c=c, ng=ng, gk=gk, bias=bias, path=path,
