@@ -14,7 +14,7 @@
 //   2  scores: softmax e = exp(x - max) with the row sum, or sigmoid s,
 //      kept in registers;
 //   3  a threshold t with K <= n <= 128 logits at or above it: the previous
-//      row's estimate when it verifies, else a lower bound from the group
+//      row's threshold when it verifies, else a lower bound from the group
 //      maxima (if K of them reach t, so do K logits) found by bisection on
 //      the value; rows where neither works take step 5 over the whole row;
 //   4  the logits >= t are compacted into shared memory (a prefix count
@@ -118,7 +118,6 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
   const uint32_t row_bytes = static_cast<uint32_t>(E) * D;
   const int nwarps = gridDim.x * wpb;
   const unsigned char* src = static_cast<const unsigned char*>(a.logits);
-  const int margin = a.spec_target - (K - 1);  // candidates above K the estimate aims for
 
   if (lane == 0) {
     mbar_init(&bars[0], 1);
@@ -257,7 +256,7 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
 
     // ---- 4 / 5: exact K-th largest key by bisection -------------------------------
     uint32_t lo, hi = RK::of(row_max) + 1u;
-    int n_lo, n_hi = 0;
+    int n_lo;
     auto bisect = [&](auto count_at) {
 #pragma unroll 1
       while (n_lo != K && hi - lo > 1u) {
@@ -268,10 +267,10 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
           n_lo = c;
         } else {
           hi = mid;
-          n_hi = c;
         }
       }
     };
+    float o[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's candidates
     if (ok) {
       // compact the candidates: the lane's logits >= t go to its slots
       int pos = seg_exclusive_scan<32>(cnt);
@@ -287,17 +286,19 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
       if (RK::to_float(lo) < t) ++lo;
       n_lo = n;
       if (n <= 32) {
-        const float o0 = slot(0);
+        o[0] = slot(0);
         __syncwarp();  // the slots are free again (the next row writes them)
-        bisect([&](float m) { return static_cast<int>(o0 >= m); });
+        bisect([&](float m) { return static_cast<int>(o[0] >= m); });
       } else if (n <= 64) {
-        const float o0 = slot(0), o1 = slot(1);
+        o[0] = slot(0);
+        o[1] = slot(1);
         __syncwarp();
-        bisect([&](float m) { return (o0 >= m) + (o1 >= m); });
+        bisect([&](float m) { return (o[0] >= m) + (o[1] >= m); });
       } else {
-        const float o0 = slot(0), o1 = slot(1), o2 = slot(2), o3 = slot(3);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o[r] = slot(r);
         __syncwarp();
-        bisect([&](float m) { return (o0 >= m) + (o1 >= m) + (o2 >= m) + (o3 >= m); });
+        bisect([&](float m) { return (o[0] >= m) + (o[1] >= m) + (o[2] >= m) + (o[3] >= m); });
       }
     } else {
       lo = RK::lowest();
@@ -307,8 +308,13 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     const float v = RK::to_float(lo);
     int ti = INT_MAX;  // selected: x > v, or x == v with index <= ti
     if (n_lo != K) {
-      // tie at v: n_hi logits above it; the (K - n_hi)-th equal one in index
-      // order (chunk j covers experts 128 j .. 128 j + 127 in lane order)
+      // tie at v: n_hi logits above it (those at or above the next key); the
+      // (K - n_hi)-th equal one in index order (chunk j covers experts
+      // 128 j .. 128 j + 127 in lane order)
+      const float above = RK::to_float(hi);
+      const int n_hi = ok ? warp_add((o[0] >= above) + (o[1] >= above) + (o[2] >= above) +
+                                     (o[3] >= above))
+                          : warp_add(count_ge(above));
       const int need = K - n_hi;
       int run = 0;
       ti = -1;
@@ -335,16 +341,9 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
       }
     }
 
-    // next row's estimate: aim for K + margin candidates, interpolating
-    // between this row's threshold t (n at or above it) and v (K)
-    if (ok) {
-      const float span = n > K ? (v - t) * (static_cast<float>(margin) / static_cast<float>(n - K))
-                               : (row_max - t) * (static_cast<float>(margin) / static_cast<float>(K));
-      spec_t = v - span;
-      have_spec = true;
-    } else {
-      have_spec = false;
-    }
+    // the next row starts from this row's candidate threshold
+    spec_t = t;
+    have_spec = ok;
 
     // ---- 6: outputs -----------------------------------------------------------------
     auto emit = [&](auto tie_tag) {
