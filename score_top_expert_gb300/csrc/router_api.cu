@@ -263,7 +263,8 @@ RegLayout reg_layout(int nc, int dt) {
   const int d = dt == MR_F32 ? 4 : 2;
   L.stage_bytes = 4 * 32 * nc * d;  // one padded row
   L.cand_off = 2 * L.stage_bytes;
-  L.bar_off = round_up(L.cand_off + kRegCap * 4, 16);
+  L.grp_off = round_up(L.cand_off + kRegCap * 4, 16);
+  L.bar_off = L.grp_off + kMaxGroups * 8;
   L.warp_bytes = round_up(L.bar_off + 16, 128);
   return L;
 }
@@ -278,14 +279,14 @@ int occupancy_reg_any(int sf, int dt, const RegPlan& p) {
 
 // Warps per block that keep the most warps resident per SM (fewer per block
 // on a tie: finer grid balance).
-bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int E, RegPlan* out) {
+bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, RegPlan* out) {
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < g_nreg_plans; ++i) {
       const PlanKey& k = g_reg_plans[i].key;
-      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.E == E) {
+      if (k.dev == dev && k.sf == sf && k.dt == dt && k.op == op && k.km == km && k.E == E) {
         *out = g_reg_plans[i].plan;
         return g_reg_plans[i].valid;
       }
@@ -295,6 +296,7 @@ bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int E, RegPlan* out)
   p.nc = E <= 256 ? 2 : 4;
   p.full = E == 128 * p.nc;
   p.op = op;
+  p.km = km;
   p.layout = reg_layout(p.nc, dt);
   int best_warps = 0, best_per_sm = 0;
   for (int w = 2; w <= kRegMaxWarps; w += 2) {
@@ -312,27 +314,30 @@ bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int E, RegPlan* out)
   p.max_blocks = best_per_sm * di.sms;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_nreg_plans < kPlanCache)
-    g_reg_plans[g_nreg_plans++] = RegPlanEntry{{dev, sf, dt, op, 0, E, 0}, p, valid};
+    g_reg_plans[g_nreg_plans++] = RegPlanEntry{{dev, sf, dt, op, km, E, 0}, p, valid};
   *out = p;
   return valid;
 }
 
-// The register-resident forward serves the top-K router (op 0) and the aux
-// scores (op 1) without bias or groups for aligned rows of at most 512
-// experts, wherever the automatic choice would take the staged path.
-bool use_reg(int E, int dt, bool aligned, int T, int km, int op) {
-  if (km != 0 || op > 1 || E > 512 || !aligned || !staged_shape_ok(E, dt)) return false;
+// The register-resident forward serves the top-K router (op 0, with or
+// without bias; groups only when they align with 4-expert chunks and sum at
+// most kTopMRegs keys) and the aux scores (op 1) for aligned rows of at most
+// 512 experts, wherever the automatic choice would take the staged path.
+bool use_reg(int E, int dt, bool aligned, int T, int km, int op, bool groups_ok = true) {
+  if (op > 1 || (km == 1 && (op != 0 || !groups_ok)) || E > 512 || !aligned ||
+      !staged_shape_ok(E, dt))
+    return false;
   const int path = current_path();
   if (path == MR_PATH_SEGMENT || path == MR_PATH_STAGED) return false;
   if (path == MR_PATH_REGISTER) return true;
   return E >= 128 || T < 8192;
 }
 
-int launch_reg_any(int sf, int dt, const FwdArgs& a, int op, cudaStream_t st) {
+int launch_reg_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStream_t st) {
   DeviceInfo di{};
   if (!device_info(&di)) return MR_ERR_CUDA;
   RegPlan p{};
-  if (!reg_plan(di, sf, dt, op, a.E, &p)) return MR_ERR_CUDA;
+  if (!reg_plan(di, sf, dt, op, km, a.E, &p)) return MR_ERR_CUDA;
   cudaError_t e;
   if (sf == MR_SOFTMAX)
     e = dt == MR_F32 ? launch_reg_softmax_f32(a, p, di.status, st)
@@ -577,24 +582,29 @@ int topk_fwd_launch(int op, const void* logits, int dtype, int T, int E, int K, 
   a.scaling = scaling_factor;
   a.num_groups = grouped ? num_groups : 0;
   a.group_topk = grouped ? group_topk : 0;
+  // groups of a power-of-two number of 4-expert chunks (at most a warp) with
+  // at most kTopMRegs keys summed are scored in registers on the staged and
+  // register paths; the register path takes no other groups
+  bool chunk_groups = false;
   if (grouped) {
     a.group_size = E / num_groups;
     a.per_group = K / group_topk;
     a.inv_group_size = 1.0f / static_cast<float>(a.group_size);
-    const int lanes = staged ? 32 : c.seg;
+    const int gl = a.group_size / 4;
+    chunk_groups = a.group_size % 4 == 0 && gl >= 1 && gl <= 32 && (gl & (gl - 1)) == 0 &&
+                   a.per_group <= kTopMRegs;
+  }
+  const bool reg = use_reg(E, dtype, vec, T, km, op, !grouped || chunk_groups);
+  if (grouped) {
+    const bool lanes32 = staged || reg;
+    const int lanes = lanes32 ? 32 : c.seg;
     int lpg = 1;
     while (lpg * 2 * num_groups <= lanes) lpg *= 2;
     a.lanes_per_group = lpg;
-    // staged path: groups of a power-of-two number of 4-expert chunks (at
-    // most a warp) with at most 4 keys summed are scored in registers
-    const int gl = a.group_size / 4;
-    a.group_chunk_lanes = (staged && a.group_size % 4 == 0 && gl >= 1 && gl <= 32 &&
-                           (gl & (gl - 1)) == 0 && a.per_group <= kTopMRegs)
-                              ? gl
-                              : 0;
+    a.group_chunk_lanes = (lanes32 && chunk_groups) ? a.group_size / 4 : 0;
   }
-  if (use_reg(E, dtype, vec, T, km, op))
-    return launch_reg_any(score_func, dtype, a, op, reinterpret_cast<cudaStream_t>(stream));
+  if (reg)
+    return launch_reg_any(score_func, dtype, a, op, km, reinterpret_cast<cudaStream_t>(stream));
   if (staged)
     return launch_staged_any(score_func, dtype, a, op, km, reinterpret_cast<cudaStream_t>(stream));
   return launch_fwd_any(score_func, dtype, a, c, reinterpret_cast<cudaStream_t>(stream));
@@ -729,7 +739,7 @@ int router_aux_scores_fwd(const void* logits, mr_dtype dtype, int T, int E, int 
   a.spec_target = spec_target(K);
   a.scaling = 1.0f;
   if (use_reg(E, dtype, vec, T, 0, 1))
-    return launch_reg_any(score_func, dtype, a, 1, reinterpret_cast<cudaStream_t>(stream));
+    return launch_reg_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));
   if (use_staged(E, dtype, vec, T))
     return launch_staged_any(score_func, dtype, a, 1, 0, reinterpret_cast<cudaStream_t>(stream));
   FwdConfig c{};

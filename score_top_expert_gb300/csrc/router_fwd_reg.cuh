@@ -1,5 +1,6 @@
 // Router forward for rows of at most 512 experts, each row held in the
-// registers of one warp (no bias, no groups; top-K router and aux scores).
+// registers of one warp (top-K router and aux scores; the top-K router also
+// with an expert bias and with groups that align with 4-expert chunks).
 //
 // A warp owns one token row at a time and walks the rows of the batch
 // persistently (row, row + all warps, ...).  Rows arrive in shared memory by
@@ -28,8 +29,13 @@
 //   5  (no usable t) the same bisection counting over the whole row;
 //   6  outputs straight from registers: probs, map and scores (top-K), or
 //      q, map and the sigmoid (aux scores).
-// The selection keys on the logit, which is exact: softmax and sigmoid are
-// strictly increasing.  Ties go to the lower expert index.
+// Key mode KM 0 (no bias, no groups) selects on the logit, which is exact:
+// softmax and sigmoid are strictly increasing.  KM 1 selects on the fp32 key
+// s + bias, built in registers after step 2; with groups, a group scores the
+// sum of its per_group largest keys (a butterfly over the lanes holding the
+// group), and the keys of every group outside the group_topk best are set to
+// -inf before step 3.  Ties go to the lower expert index (and, among groups,
+// to the lower group index).
 #pragma once
 
 #include <climits>
@@ -45,6 +51,7 @@ namespace moe_router {
 struct RegLayout {
   int stage_bytes;  // 32 * NC chunks of four logits (one padded row)
   int cand_off;     // kRegCap candidate logits (fp32)
+  int grp_off;      // KM 1 groups: kMaxGroups packed group words (8 bytes each)
   int bar_off;      // two mbarriers
   int warp_bytes;   // slice size, multiple of 128
 };
@@ -96,15 +103,110 @@ __device__ __forceinline__ void stage_chunk(const unsigned char* stage, int c, f
   }
 }
 
-template <int SF, int DT, int NC, int OP, bool FULL>
+// KM 1 groups that align with 4-expert chunks: group g is the
+// a.group_chunk_lanes = Lg consecutive chunks Lg g .. Lg g + Lg - 1 (Lg a
+// power of two <= 32, so one chunk column j holds 32 / Lg whole groups); its
+// score is the sum of its per_group (<= kTopMRegs) largest keys, merged over
+// its Lg lanes by a butterfly.  Ranking: the first lane of each group
+// publishes the packed word (ordered score key << 32 | ~group) in the warp's
+// slots `gw`, each lane of a group counts the larger words among every Lg-th
+// group, and a butterfly over the group's lanes sums the counts (ties between
+// scores go to the lower group index).  The keys of groups ranked group_topk
+// or lower become -inf.
+template <int NC>
+__device__ __forceinline__ void group_mask(const FwdArgs& a, int lane, float (&sk)[4 * NC],
+                                           unsigned long long* gw) {
+  constexpr unsigned kFull = 0xffffffffu;
+  const int Lg = a.group_chunk_lanes;
+  const int M = a.per_group;
+  const int G = a.num_groups;
+  const int gpj = 32 / Lg;  // groups per chunk column
+  float gsum[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const float* k = &sk[4 * j];
+    if (M <= 2) {
+      // top-2 pair (t0 >= t1); M == 1 uses t0 only
+      float t0 = fmaxf(fmaxf(k[0], k[1]), fmaxf(k[2], k[3]));
+      float t1 = fmaxf(fmaxf(fminf(k[0], k[1]), fminf(k[2], k[3])),
+                       fminf(fmaxf(k[0], k[1]), fmaxf(k[2], k[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (o < Lg) {
+          const float p0 = __shfl_xor_sync(kFull, t0, o);
+          const float p1 = __shfl_xor_sync(kFull, t1, o);
+          t1 = fmaxf(fminf(t0, p0), fmaxf(t1, p1));
+          t0 = fmaxf(t0, p0);
+        }
+      }
+      gsum[j] = M == 1 ? t0 : t0 + t1;
+    } else {
+      float top[kTopMRegs];
+#pragma unroll
+      for (int i = 0; i < kTopMRegs; ++i) top[i] = -INFINITY;
+      auto insert = [&](float w) {
+#pragma unroll
+        for (int i = 0; i < kTopMRegs; ++i) {
+          if (i < M) {
+            const float hi = fmaxf(top[i], w);
+            w = fminf(top[i], w);
+            top[i] = hi;
+          }
+        }
+      };
+#pragma unroll
+      for (int u = 0; u < 4; ++u) insert(k[u]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (o < Lg) {
+          float other[kTopMRegs];
+#pragma unroll
+          for (int i = 0; i < kTopMRegs; ++i) other[i] = __shfl_xor_sync(kFull, top[i], o);
+#pragma unroll
+          for (int i = 0; i < kTopMRegs; ++i) insert(other[i]);
+        }
+      }
+      float g = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kTopMRegs; ++i)
+        if (i < M) g += top[i];
+      gsum[j] = g;
+    }
+  }
+  unsigned long long word[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int g = j * gpj + lane / Lg;
+    word[j] = pack_key(ordered_key(gsum[j]), g);
+    if ((lane & (Lg - 1)) == 0 && g < G) gw[g] = word[j];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    int r = 0;
+    for (int h = lane & (Lg - 1); h < G; h += Lg) r += gw[h] > word[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      if (o < Lg) r += __shfl_xor_sync(kFull, r, o);
+    const int g = j * gpj + lane / Lg;
+    if (g < G && r >= a.group_topk) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sk[4 * j + u] = -INFINITY;
+    }
+  }
+  __syncwarp();  // the slots are free again
+}
+
+template <int SF, int DT, int NC, int OP, bool FULL, int KM>
 __global__ void __launch_bounds__(kRegMaxWarps * 32)
 router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
   pdl_enter();
   static_assert(NC == 2 || NC == 4, "rows of up to 256 or 512 experts");
+  static_assert(KM == 0 || OP == 0, "bias and groups: top-K router only");
   constexpr int N = 4 * NC;  // logits per lane
   constexpr int D = DT == DT_F32 ? 4 : 2;
   constexpr unsigned kFull = 0xffffffffu;
-  using RK = RowKey<DT>;
+  using RK = RowKey<KM == 1 ? DT_F32 : DT>;  // keys s + bias are fp32 values
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -132,6 +234,15 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     if (row0 + nwarps < T)
       bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nwarps) * row_bytes,
                 row_bytes, &bars[1]);
+  }
+
+  [[maybe_unused]] float bias[KM == 1 ? N : 1];  // KM 1: this lane's experts' bias
+  if constexpr (KM == 1) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int idx = 4 * (lane + 32 * (k >> 2)) + (k & 3);
+      bias[k] = (a.bias != nullptr && idx < E) ? __ldg(a.bias + idx) : 0.0f;
+    }
   }
 
   bool have_spec = false;  // an estimate carried over from the previous row
@@ -167,14 +278,19 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
         }
       }
     }
-    float hm[2] = {-INFINITY, -INFINITY};
+    // half maxima of the lane (64 group maxima of the row)
+    auto half_maxima = [&](const float (&v)[N], float (&hm)[2]) {
+      hm[0] = hm[1] = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NC; ++j) {
-      const float m4 = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
-      hm[j < NC / 2 ? 0 : 1] = fmaxf(hm[j < NC / 2 ? 0 : 1], m4);
-    }
+      for (int j = 0; j < NC; ++j) {
+        const float m4 = fmaxf(fmaxf(v[4 * j], v[4 * j + 1]), fmaxf(v[4 * j + 2], v[4 * j + 3]));
+        hm[j < NC / 2 ? 0 : 1] = fmaxf(hm[j < NC / 2 ? 0 : 1], m4);
+      }
+    };
+    float hm[2];
+    half_maxima(x, hm);
     // every real row has a finite maximum (padding is -inf, inputs are finite)
-    const float row_max =
+    const float xmax =
         key_to_float(__reduce_max_sync(kFull, ordered_key(fmaxf(hm[0], hm[1]))));
     // the maximum consumed every logit read from the stage: refill it
     fence_proxy_async_smem();
@@ -186,7 +302,7 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     const size_t off = static_cast<size_t>(row) * static_cast<size_t>(E);
 
     // ---- 2: scores and their row sum ----------------------------------------------
-    const float max_l2e = row_max * kLog2e;
+    const float max_l2e = xmax * kLog2e;
     float w[N];  // softmax: e = exp(x - max); sigmoid: s (padding: exactly 0)
     // summed in the staged forward's order (pairs within a chunk, chunks
     // alternating between two sums, then the butterfly), so that the scores
@@ -207,11 +323,27 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     float inv = 1.0f;
     if constexpr (kNeedSum) inv = 1.0f / seg_sum<32>(sum0 + sum1);
 
+    // ---- 2b: selection keys: the logits (KM 0), or s + bias with groups (KM 1) ----
+    float sk[N];
+    float row_max = xmax;  // largest selection key of the row
+    if constexpr (KM == 0) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) sk[k] = x[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < N; ++k)
+        sk[k] = x[k] == -INFINITY ? -INFINITY : ((SF != SF_SIGMOID) ? w[k] * inv : w[k]) + bias[k];
+      if (a.num_groups > 1)
+        group_mask<NC>(a, lane, sk, reinterpret_cast<unsigned long long*>(base + L.grp_off));
+      half_maxima(sk, hm);
+      row_max = key_to_float(__reduce_max_sync(kFull, ordered_key(fmaxf(hm[0], hm[1]))));
+    }
+
     // ---- 3: a candidate threshold ---------------------------------------------------
     auto count_ge = [&](float t) {
       int c = 0;
 #pragma unroll
-      for (int k = 0; k < N; ++k) c += x[k] >= t;
+      for (int k = 0; k < N; ++k) c += sk[k] >= t;
       return c;
     };
     float t = 0.0f;
@@ -276,7 +408,7 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
       int pos = seg_exclusive_scan<32>(cnt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        if (x[k] >= t) cand[pos++] = x[k];
+        if (sk[k] >= t) cand[pos++] = sk[k];
       }
       __syncwarp();
       auto slot = [&](int r) { return 32 * r + lane < n ? cand[32 * r + lane] : -INFINITY; };
@@ -322,7 +454,7 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
       for (int j = 0; j < NC; ++j) {
         int e = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) e += x[4 * j + u] == v;
+        for (int u = 0; u < 4; ++u) e += sk[4 * j + u] == v;
         const int excl = seg_exclusive_scan<32>(e);
         const int tot = __shfl_sync(kFull, excl + e, 31);
         int mine = -1;
@@ -330,7 +462,7 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
           int left = need - run - excl;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            if (x[4 * j + u] == v && --left == 0 && mine < 0) mine = 4 * (lane + 32 * j) + u;
+            if (sk[4 * j + u] == v && --left == 0 && mine < 0) mine = 4 * (lane + 32 * j) + u;
         }
         const unsigned who = __ballot_sync(kFull, mine >= 0);
         if (who) {
@@ -349,8 +481,8 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     auto emit = [&](auto tie_tag) {
       constexpr bool kTie = decltype(tie_tag)::value;
       auto sel = [&](int k, int idx) -> bool {
-        if constexpr (kTie) return x[k] > v || (x[k] == v && idx <= ti);
-        else return x[k] >= v;
+        if constexpr (kTie) return sk[k] > v || (sk[k] == v && idx <= ti);
+        else return sk[k] >= v;
       };
       [[maybe_unused]] float pf = a.scaling;  // probs factor (top-K router only)
       if constexpr (OP == 0 && SF != SF_SOFTMAX) {

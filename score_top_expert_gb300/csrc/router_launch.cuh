@@ -251,20 +251,21 @@ int staged_occupancy(const StagedPlan& p) {
   return 0;
 }
 
-// Register-resident forward (rows of up to 512 experts, no bias or groups,
-// OP 0 and 1): warps per block and the grid cap.
+// Register-resident forward (rows of up to 512 experts; OP 0 with key mode 0
+// or 1, OP 1 with key mode 0): warps per block and the grid cap.
 struct RegPlan {
   RegLayout layout;
   int warps_per_block;
   int max_blocks;  // resident blocks per SM x SMs
   int nc;          // chunks of 4 experts per lane (2 or 4)
   int op;          // 0 top-K router, 1 aux scores
+  int km;          // key mode: 0 logits, 1 s + bias (and aligned groups)
   bool full;       // E == 128 * nc
 };
 
-template <int SF, int DT, int NC, int OP, bool FULL>
+template <int SF, int DT, int NC, int OP, bool FULL, int KM>
 cudaError_t launch_reg_inst(const FwdArgs& a, const RegPlan& p, int* status, cudaStream_t st) {
-  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL>;
+  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL, KM>;
   const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
   static std::atomic<int> granted[kSmemDevs];  // this kernel's record
   const cudaError_t se = allow_smem(kern, smem, granted);
@@ -279,9 +280,9 @@ cudaError_t launch_reg_inst(const FwdArgs& a, const RegPlan& p, int* status, cud
                        smem, st, a, p.layout, status);
 }
 
-template <int SF, int DT, int NC, int OP, bool FULL>
+template <int SF, int DT, int NC, int OP, bool FULL, int KM>
 int reg_blocks_per_sm(int warps_per_block, size_t smem) {
-  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL>;
+  auto kern = router_fwd_reg_kernel<SF, DT, NC, OP, FULL, KM>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -298,20 +299,22 @@ template <int SF, int DT, bool OCC>
 cudaError_t reg_dispatch(const FwdArgs& a, const RegPlan& p, int* status, cudaStream_t st,
                          int* occ) {
   const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
-#define MR_REG_CASE(N, O, F)                                                         \
-  if (p.nc == N && p.op == O && p.full == F) {                                       \
+#define MR_REG_CASE(N, O, F, M)                                                      \
+  if (p.nc == N && p.op == O && p.full == F && p.km == M) {                          \
     if constexpr (OCC) {                                                             \
-      *occ = reg_blocks_per_sm<SF, DT, N, O, F>(p.warps_per_block, smem);            \
+      *occ = reg_blocks_per_sm<SF, DT, N, O, F, M>(p.warps_per_block, smem);         \
       return cudaSuccess;                                                            \
     } else {                                                                         \
-      return launch_reg_inst<SF, DT, N, O, F>(a, p, status, st);                     \
+      return launch_reg_inst<SF, DT, N, O, F, M>(a, p, status, st);                  \
     }                                                                                \
   }
-  MR_REG_CASE(2, 0, true) MR_REG_CASE(2, 0, false) MR_REG_CASE(4, 0, true)
-  MR_REG_CASE(4, 0, false)
+  MR_REG_CASE(2, 0, true, 0) MR_REG_CASE(2, 0, false, 0) MR_REG_CASE(4, 0, true, 0)
+  MR_REG_CASE(4, 0, false, 0)
+  MR_REG_CASE(2, 0, true, 1) MR_REG_CASE(2, 0, false, 1) MR_REG_CASE(4, 0, true, 1)
+  MR_REG_CASE(4, 0, false, 1)
   if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
-    MR_REG_CASE(2, 1, true) MR_REG_CASE(2, 1, false) MR_REG_CASE(4, 1, true)
-    MR_REG_CASE(4, 1, false)
+    MR_REG_CASE(2, 1, true, 0) MR_REG_CASE(2, 1, false, 0) MR_REG_CASE(4, 1, true, 0)
+    MR_REG_CASE(4, 1, false, 0)
   }
 #undef MR_REG_CASE
   return cudaErrorInvalidConfiguration;

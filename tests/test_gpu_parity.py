@@ -305,6 +305,8 @@ GROUPED = [  # (E, num_groups, group_topk, K)
     (2304, 8, 1, 36), (120, 3, 2, 10), (12, 4, 2, 2), (60, 5, 5, 15), (1000, 10, 3, 30),
     # groups that align with 4-expert chunks (scored in registers on the staged path)
     (512, 16, 4, 8), (1024, 32, 4, 16), (384, 12, 4, 8), (2304, 18, 9, 36), (256, 32, 2, 8),
+    # more chunk-aligned groups: sums of 3 and 4 keys, two-lane and quarter-warp groups
+    (256, 8, 4, 12), (512, 32, 4, 12), (128, 4, 2, 8), (512, 16, 8, 32), (136, 17, 1, 2),
 ]
 
 
@@ -445,6 +447,38 @@ def test_register_rows_in_sequence(R, E, K, dt):
         for sf in ("softmax", "sigmoid"):
             run_and_check_topk(R, case, K, sf, c=2.5, check_bwd=False)
             run_and_check_aux(R, case, K, sf)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E,G,gk,K", [(256, 8, 4, 8), (512, 16, 4, 8), (384, 12, 3, 9),
+                                      (256, 0, 0, 8)])
+def test_register_biased_rows_in_sequence(R, E, G, gk, K, dt):
+    # bias (and groups) on the register path with many rows per warp: rows of
+    # normal, wide, integer-valued and adversarial logits in a fixed cycle
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    rng = np.random.default_rng(E * 17 + K + G)
+    T = 12000
+    adv = adversarial_rows(E, K, rng)
+    x = np.empty((T, E), dtype=np.float32)
+    for i in range(T):
+        kind = i % 4
+        if kind == 0:
+            x[i] = rng.normal(0, 1, E)
+        elif kind == 1:
+            x[i] = rng.normal(0, 3, E)
+        elif kind == 2:
+            x[i] = rng.integers(-3, 4, E)
+        else:
+            x[i] = adv[(i // 4) % adv.shape[0]][rng.permutation(E)]
+    prev = R.force_path("register")
+    try:
+        case = make_case(T, E, K, dtype=dt, seed=9, with_bias=True)
+        case.logits = x if dt == "f32" else round_to_bf16_values(x)
+        for sf in ("sigmoid", "softmax", "softmax_post"):
+            run_and_check_topk(R, case, K, sf, 2.5, G, gk, case.expert_bias, check_bwd=False)
     finally:
         R.force_path(prev)
     assert R.device_status() == 0
