@@ -404,13 +404,15 @@ MR_API const char* moe_router_strerror(int code);
  *     bf16; 16-byte aligned tensors).  router_topk_fwd_maps's one-launch
  *     decode form always runs on this path;
  *   MR_PATH_REGISTER: rows arrive by bulk copy like the staged path and are
- *     then held in the registers of one warp, the K-th largest logit found
- *     by bisection over compacted candidates (router_topk_fwd and
- *     router_aux_scores_fwd with E <= 512, no bias and no groups, the staged
- *     path's alignment).
- * MR_PATH_AUTO takes the register path where it applies and the staged path
- * elsewhere, except for batches of 8192 or more tokens with E < 128 (the
- * segment path is faster there).  A forced path that does not apply to a
+ *     then held in the registers of one warp, the K-th largest key found
+ *     by bisection over compacted candidates (router_topk_fwd,
+ *     router_topk_fwd_compact and router_aux_scores_fwd with E <= 512, the
+ *     staged path's alignment; bias allowed, groups when each is a
+ *     power-of-two number of 4-expert chunks and sums at most 4 keys).
+ * MR_PATH_AUTO takes the register path where it applies (for compact
+ * outputs only with bias or groups) and the staged path elsewhere, except
+ * for batches of 8192 or more tokens with E < 128 (the segment path is
+ * faster there).  A forced path that does not apply to a
  * call falls back to the automatic choice.  Process-wide; meant for tests and
  * benchmarks.  The environment variable MOE_ROUTER_FORCE_PATH
  * (auto|segment|staged|register) sets the initial value.  Returns the

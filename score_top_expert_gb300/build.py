@@ -14,6 +14,7 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -22,6 +23,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_router.so")
+# CPython entry points of the hot calls (argument conversion only), built
+# where the interpreter's headers are installed
+PYCALLS_SRC = os.path.join(CSRC, "pycalls.c")
+PYCALLS = os.path.join(LIBDIR, "_pycalls" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -40,15 +45,41 @@ def _sources() -> list[str]:
 
 
 def _inputs() -> list[str]:
-    return (_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
+    return (_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [PYCALLS_SRC] +
             glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
+
+
+def _python_include() -> str | None:
+    inc = sysconfig.get_paths().get("include")
+    return inc if inc and os.path.exists(os.path.join(inc, "Python.h")) else None
 
 
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _inputs())
+    if not all(os.path.getmtime(p) <= t for p in _inputs()):
+        return False
+    if _python_include() is not None:
+        return os.path.exists(PYCALLS) and os.path.getmtime(PYCALLS) >= t
+    return True
+
+
+def _build_pycalls() -> None:
+    """The CPython call shim, linked against the library (found next to it)."""
+    inc = _python_include()
+    if inc is None:
+        return
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        return
+    tmp = PYCALLS + ".tmp"
+    cmd = [cc, "-O2", "-shared", "-fPIC", f"-I{inc}", f"-I{INCLUDE}", PYCALLS_SRC,
+           f"-L{LIBDIR}", "-lmoe_router", "-Wl,-rpath,$ORIGIN", "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the CPython call shim failed:\n{r.stderr}")
+    os.replace(tmp, PYCALLS)
 
 
 def _compile(src: str, verbose: bool) -> tuple[str, str]:
@@ -81,6 +112,7 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    _build_pycalls()
     return LIB
 
 

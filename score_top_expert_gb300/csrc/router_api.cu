@@ -270,6 +270,16 @@ RegLayout reg_layout(int nc, int dt) {
 }
 
 int occupancy_reg_any(int sf, int dt, const RegPlan& p) {
+  if (p.op == 2) {
+    if (sf == MR_SOFTMAX)
+      return dt == MR_F32 ? occupancy_reg_compact_softmax_f32(p)
+                          : occupancy_reg_compact_softmax_bf16(p);
+    if (sf == MR_SOFTMAX_POST)
+      return dt == MR_F32 ? occupancy_reg_compact_softmaxpost_f32(p)
+                          : occupancy_reg_compact_softmaxpost_bf16(p);
+    return dt == MR_F32 ? occupancy_reg_compact_sigmoid_f32(p)
+                        : occupancy_reg_compact_sigmoid_bf16(p);
+  }
   if (sf == MR_SOFTMAX)
     return dt == MR_F32 ? occupancy_reg_softmax_f32(p) : occupancy_reg_softmax_bf16(p);
   if (sf == MR_SOFTMAX_POST)
@@ -319,17 +329,23 @@ bool reg_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, RegPl
   return valid;
 }
 
-// The register-resident forward serves the top-K router (op 0, with or
-// without bias; groups only when they align with 4-expert chunks and sum at
-// most kTopMRegs keys) and the aux scores (op 1) for aligned rows of at most
-// 512 experts, wherever the automatic choice would take the staged path.
+// The register-resident forward serves the top-K router with dense (op 0) or
+// compact (op 2) outputs, with or without bias (groups only when they align
+// with 4-expert chunks and sum at most kTopMRegs keys), and the aux scores
+// (op 1) for aligned rows of at most 512 experts.  The automatic choice
+// takes it wherever it would take the staged path, except for compact
+// outputs without bias or groups: there the staged path's candidate ranking
+// already orders the selection (8192 x 512, K = 22: 11.8 us against 14.0
+// steady state; with bias and groups at 16384 x 256 the register path takes
+// 18.9 us against 25.0).
 bool use_reg(int E, int dt, bool aligned, int T, int km, int op, bool groups_ok = true) {
-  if (op > 1 || (km == 1 && (op != 0 || !groups_ok)) || E > 512 || !aligned ||
+  if (op > 2 || (km == 1 && (op == 1 || !groups_ok)) || E > 512 || !aligned ||
       !staged_shape_ok(E, dt))
     return false;
   const int path = current_path();
   if (path == MR_PATH_SEGMENT || path == MR_PATH_STAGED) return false;
   if (path == MR_PATH_REGISTER) return true;
+  if (op == 2 && km == 0) return false;
   return E >= 128 || T < 8192;
 }
 
@@ -339,6 +355,18 @@ int launch_reg_any(int sf, int dt, const FwdArgs& a, int op, int km, cudaStream_
   RegPlan p{};
   if (!reg_plan(di, sf, dt, op, km, a.E, &p)) return MR_ERR_CUDA;
   cudaError_t e;
+  if (op == 2) {
+    if (sf == MR_SOFTMAX)
+      e = dt == MR_F32 ? launch_reg_compact_softmax_f32(a, p, di.status, st)
+                       : launch_reg_compact_softmax_bf16(a, p, di.status, st);
+    else if (sf == MR_SOFTMAX_POST)
+      e = dt == MR_F32 ? launch_reg_compact_softmaxpost_f32(a, p, di.status, st)
+                       : launch_reg_compact_softmaxpost_bf16(a, p, di.status, st);
+    else
+      e = dt == MR_F32 ? launch_reg_compact_sigmoid_f32(a, p, di.status, st)
+                       : launch_reg_compact_sigmoid_bf16(a, p, di.status, st);
+    return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
+  }
   if (sf == MR_SOFTMAX)
     e = dt == MR_F32 ? launch_reg_softmax_f32(a, p, di.status, st)
                      : launch_reg_softmax_bf16(a, p, di.status, st);

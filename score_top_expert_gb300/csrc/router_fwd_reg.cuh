@@ -28,7 +28,11 @@
 //      order up to K by a prefix count;
 //   5  (no usable t) the same bisection counting over the whole row;
 //   6  outputs straight from registers: probs, map and scores (top-K), or
-//      q, map and the sigmoid (aux scores).
+//      q, map and the sigmoid (aux scores).  Compact outputs (OP 2) gather
+//      the K selected (key, ~index) words into shared memory, rank them
+//      among themselves and write the row's K weights, indices and expanded
+//      rows by rank; the dense outputs follow only where their pointers are
+//      set.
 // Key mode KM 0 (no bias, no groups) selects on the logit, which is exact:
 // softmax and sigmoid are strictly increasing.  KM 1 selects on the fp32 key
 // s + bias, built in registers after step 2; with groups, a group scores the
@@ -197,12 +201,18 @@ __device__ __forceinline__ void group_mask(const FwdArgs& a, int lane, float (&s
   __syncwarp();  // the slots are free again
 }
 
+// Registers per thread: 64 keeps 32 warps per SM; the compact-output kernels
+// at 512 experts get 80 (25 warps), which spills much less.
+template <int NC, int OP, int KM>
+constexpr int reg_max_regs() { return (NC == 4 && OP == 2) ? 80 : 64; }
+
 template <int SF, int DT, int NC, int OP, bool FULL, int KM>
-__global__ void __launch_bounds__(kRegMaxWarps * 32)
+__global__ void __launch_bounds__(kRegMaxWarps * 32) __maxnreg__((reg_max_regs<NC, OP, KM>()))
 router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
   pdl_enter();
   static_assert(NC == 2 || NC == 4, "rows of up to 256 or 512 experts");
-  static_assert(KM == 0 || OP == 0, "bias and groups: top-K router only");
+  static_assert(KM == 0 || OP != 1, "bias and groups: top-K router only");
+  static_assert(OP <= 2, "dense top-K (0), aux scores (1), compact top-K (2)");
   constexpr int N = 4 * NC;  // logits per lane
   constexpr int D = DT == DT_F32 ? 4 : 2;
   constexpr unsigned kFull = 0xffffffffu;
@@ -234,15 +244,6 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     if (row0 + nwarps < T)
       bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nwarps) * row_bytes,
                 row_bytes, &bars[1]);
-  }
-
-  [[maybe_unused]] float bias[KM == 1 ? N : 1];  // KM 1: this lane's experts' bias
-  if constexpr (KM == 1) {
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const int idx = 4 * (lane + 32 * (k >> 2)) + (k & 3);
-      bias[k] = (a.bias != nullptr && idx < E) ? __ldg(a.bias + idx) : 0.0f;
-    }
   }
 
   bool have_spec = false;  // an estimate carried over from the previous row
@@ -330,9 +331,22 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
 #pragma unroll
       for (int k = 0; k < N; ++k) sk[k] = x[k];
     } else {
+      // the bias (16-byte aligned, read through the cache: the same E floats
+      // for every row)
 #pragma unroll
-      for (int k = 0; k < N; ++k)
-        sk[k] = x[k] == -INFINITY ? -INFINITY : ((SF != SF_SIGMOID) ? w[k] * inv : w[k]) + bias[k];
+      for (int j = 0; j < NC; ++j) {
+        const int c = lane + 32 * j;
+        float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (a.bias != nullptr && (FULL || c < nchunks))
+          b4 = __ldg(reinterpret_cast<const float4*>(a.bias) + c);
+        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = 4 * j + u;
+          sk[k] = x[k] == -INFINITY ? -INFINITY
+                                    : ((SF != SF_SIGMOID) ? w[k] * inv : w[k]) + bb[u];
+        }
+      }
       if (a.num_groups > 1)
         group_mask<NC>(a, lane, sk, reinterpret_cast<unsigned long long*>(base + L.grp_off));
       half_maxima(sk, hm);
@@ -485,15 +499,73 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
         else return sk[k] >= v;
       };
       [[maybe_unused]] float pf = a.scaling;  // probs factor (top-K router only)
-      if constexpr (OP == 0 && SF != SF_SOFTMAX) {
+      if constexpr (OP != 1 && SF != SF_SOFTMAX) {
         // renormalised over the selected: c / sum of their scores
         float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < N; ++k)
           if (sel(k, 4 * (lane + 32 * (k >> 2)) + (k & 3))) part += w[k];
         pf = a.scaling / seg_sum<32>(part);
-      } else if constexpr (OP == 0) {
+      } else if constexpr (OP != 1) {
         pf = a.scaling * inv;
+      }
+      if constexpr (OP == 2) {
+        // compact outputs: the K selected (key, ~index) words and their
+        // weights go to the warp's slots by a prefix count, each word's rank
+        // among them is counted (on the 32-bit key first; when keys repeat the
+        // ranks no longer sum to 0 + 1 + ... + K - 1 and they are recounted on
+        // the whole words), and position rank of the row takes the expert
+        unsigned long long* wd = reinterpret_cast<unsigned long long*>(cand);
+        float* wt = reinterpret_cast<float*>(wd + MR_MAX_TOPK);
+        int sc = 0;
+#pragma unroll
+        for (int k = 0; k < N; ++k) sc += sel(k, 4 * (lane + 32 * (k >> 2)) + (k & 3));
+        int pos = seg_exclusive_scan<32>(sc);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          const int idx = 4 * (lane + 32 * (k >> 2)) + (k & 3);
+          if (sel(k, idx)) {
+            wd[pos] = pack_key(ordered_key(sk[k]), idx);
+            wt[pos] = w[k] * pf;
+            ++pos;
+          }
+        }
+        __syncwarp();
+        const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(wd) + 1;  // keys
+        const int i1 = lane + 32;
+        const unsigned long long w0 = lane < K ? wd[lane] : 0ull;
+        const unsigned long long w1 = i1 < K ? wd[i1] : 0ull;
+        const uint32_t k0 = static_cast<uint32_t>(w0 >> 32), k1 = static_cast<uint32_t>(w1 >> 32);
+        int r0 = 0, r1 = 0;
+#pragma unroll 4
+        for (int q = 0; q < K; ++q) {
+          const uint32_t kq = hi_words[2 * q];
+          r0 += kq > k0;
+          r1 += kq > k1;
+        }
+        const int rs = (lane < K ? r0 : 0) + (i1 < K ? r1 : 0);
+        if (warp_add(rs) != K * (K - 1) / 2) {
+          r0 = r1 = 0;
+#pragma unroll 4
+          for (int q = 0; q < K; ++q) {
+            const unsigned long long wq = wd[q];
+            r0 += wq > w0;
+            r1 += wq > w1;
+          }
+        }
+        const size_t t = static_cast<size_t>(row);
+        if (lane < K) {
+          a.topk_w[t * a.ld_w + r0] = wt[lane];
+          a.topk_i[t * a.ld_i + r0] = static_cast<int>(~static_cast<uint32_t>(w0));
+          if (a.tei != nullptr) a.tei[t * K + r0] = r0 * T + row;
+        }
+        if (i1 < K) {
+          a.topk_w[t * a.ld_w + r1] = wt[i1];
+          a.topk_i[t * a.ld_i + r1] = static_cast<int>(~static_cast<uint32_t>(w1));
+          if (a.tei != nullptr) a.tei[t * K + r1] = r1 * T + row;
+        }
+        __syncwarp();  // the slots are free again
+        if (a.map == nullptr && a.probs == nullptr && a.scores == nullptr) return;
       }
 #pragma unroll
       for (int j = 0; j < NC; ++j) {
@@ -502,16 +574,16 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
           bool m[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) m[u] = sel(4 * j + u, 4 * c + u);
-          store_map4<true>(a.map, off, 4 * c, E, m);
+          if (OP != 2 || a.map != nullptr) store_map4<true>(a.map, off, 4 * c, E, m);
           float s[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? w[4 * j + u] * inv : w[4 * j + u];
-          if constexpr (OP == 0) {
+          if constexpr (OP != 1) {
             float p[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) p[u] = m[u] ? w[4 * j + u] * pf : 0.0f;
-            store4<DT, true>(a.probs, off, 4 * c, E, p);
-            store4_f32<true>(a.scores, off, 4 * c, E, s);
+            if (OP == 0 || a.probs != nullptr) store4<DT, true>(a.probs, off, 4 * c, E, p);
+            if (OP == 0 || a.scores != nullptr) store4_f32<true>(a.scores, off, 4 * c, E, s);
           } else if constexpr (SF == SF_SOFTMAX) {
             store4_f32<true>(a.scores, off, 4 * c, E, s);
             if (a.intermediate != nullptr) store4_f32<true>(a.intermediate, off, 4 * c, E, s);

@@ -251,14 +251,14 @@ int staged_occupancy(const StagedPlan& p) {
   return 0;
 }
 
-// Register-resident forward (rows of up to 512 experts; OP 0 with key mode 0
-// or 1, OP 1 with key mode 0): warps per block and the grid cap.
+// Register-resident forward (rows of up to 512 experts; OP 0 and 2 with key
+// mode 0 or 1, OP 1 with key mode 0): warps per block and the grid cap.
 struct RegPlan {
   RegLayout layout;
   int warps_per_block;
   int max_blocks;  // resident blocks per SM x SMs
   int nc;          // chunks of 4 experts per lane (2 or 4)
-  int op;          // 0 top-K router, 1 aux scores
+  int op;          // 0 top-K router, 1 aux scores, 2 compact top-K outputs
   int km;          // key mode: 0 logits, 1 s + bias (and aligned groups)
   bool full;       // E == 128 * nc
 };
@@ -295,7 +295,9 @@ int reg_blocks_per_sm(int warps_per_block, size_t smem) {
 }
 
 // OCC false: launch; true: resident blocks per SM (returned through *occ).
-template <int SF, int DT, bool OCC>
+// MODE 0: top-K (OP 0) and aux (OP 1); MODE 2: compact outputs (OP 2); the
+// modes live in separate translation units.
+template <int SF, int DT, bool OCC, int MODE = 0>
 cudaError_t reg_dispatch(const FwdArgs& a, const RegPlan& p, int* status, cudaStream_t st,
                          int* occ) {
   const size_t smem = static_cast<size_t>(p.warps_per_block) * p.layout.warp_bytes;
@@ -308,13 +310,20 @@ cudaError_t reg_dispatch(const FwdArgs& a, const RegPlan& p, int* status, cudaSt
       return launch_reg_inst<SF, DT, N, O, F, M>(a, p, status, st);                  \
     }                                                                                \
   }
-  MR_REG_CASE(2, 0, true, 0) MR_REG_CASE(2, 0, false, 0) MR_REG_CASE(4, 0, true, 0)
-  MR_REG_CASE(4, 0, false, 0)
-  MR_REG_CASE(2, 0, true, 1) MR_REG_CASE(2, 0, false, 1) MR_REG_CASE(4, 0, true, 1)
-  MR_REG_CASE(4, 0, false, 1)
-  if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
-    MR_REG_CASE(2, 1, true, 0) MR_REG_CASE(2, 1, false, 0) MR_REG_CASE(4, 1, true, 0)
-    MR_REG_CASE(4, 1, false, 0)
+  if constexpr (MODE == 2) {
+    MR_REG_CASE(2, 2, true, 0) MR_REG_CASE(2, 2, false, 0) MR_REG_CASE(4, 2, true, 0)
+    MR_REG_CASE(4, 2, false, 0)
+    MR_REG_CASE(2, 2, true, 1) MR_REG_CASE(2, 2, false, 1) MR_REG_CASE(4, 2, true, 1)
+    MR_REG_CASE(4, 2, false, 1)
+  } else {
+    MR_REG_CASE(2, 0, true, 0) MR_REG_CASE(2, 0, false, 0) MR_REG_CASE(4, 0, true, 0)
+    MR_REG_CASE(4, 0, false, 0)
+    MR_REG_CASE(2, 0, true, 1) MR_REG_CASE(2, 0, false, 1) MR_REG_CASE(4, 0, true, 1)
+    MR_REG_CASE(4, 0, false, 1)
+    if constexpr (SF != SF_SOFTMAX_POST) {  // aux scores take softmax or sigmoid only
+      MR_REG_CASE(2, 1, true, 0) MR_REG_CASE(2, 1, false, 0) MR_REG_CASE(4, 1, true, 0)
+      MR_REG_CASE(4, 1, false, 0)
+    }
   }
 #undef MR_REG_CASE
   return cudaErrorInvalidConfiguration;
@@ -322,7 +331,9 @@ cudaError_t reg_dispatch(const FwdArgs& a, const RegPlan& p, int* status, cudaSt
 
 #define MR_DECLARE_REG(NAME)                                                           \
   cudaError_t launch_reg_##NAME(const FwdArgs&, const RegPlan&, int*, cudaStream_t);   \
-  int occupancy_reg_##NAME(const RegPlan&);
+  int occupancy_reg_##NAME(const RegPlan&);                                            \
+  cudaError_t launch_reg_compact_##NAME(const FwdArgs&, const RegPlan&, int*, cudaStream_t); \
+  int occupancy_reg_compact_##NAME(const RegPlan&);
 MR_DECLARE_REG(softmax_f32)
 MR_DECLARE_REG(softmax_bf16)
 MR_DECLARE_REG(sigmoid_f32)

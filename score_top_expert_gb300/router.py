@@ -24,6 +24,7 @@ _SCORE = {"softmax": MR_SOFTMAX, "sigmoid": MR_SIGMOID, "softmax_post": MR_SOFTM
 _DTYPE = {torch.float32: MR_F32, torch.bfloat16: MR_BF16}
 
 _lib = None
+_fast = None  # the CPython call shim, when built (same C entry points as ctypes)
 
 
 class RouterError(RuntimeError):
@@ -84,7 +85,40 @@ def lib() -> ctypes.CDLL:
         L.moe_router_strerror.argtypes = [i]
         L.moe_router_strerror.restype = ctypes.c_char_p
         _lib = L
+        _load_fast()
     return _lib
+
+
+class _CtypesCalls:
+    """The hot calls through ctypes (pointers as integers, 0 for NULL), for
+    an interpreter without headers to build the CPython shim."""
+
+    def __init__(self, L):
+        self.router_topk_fwd = L.router_topk_fwd
+        self.router_topk_bwd = L.router_topk_bwd
+        self.router_aux_scores_fwd = L.router_aux_scores_fwd
+        self.router_aux_scores_bwd = L.router_aux_scores_bwd
+
+
+def _load_fast():
+    """Bind the hot calls: the CPython shim built next to the library, else
+    ctypes.  Both call the same exported C entry points."""
+    global _fast
+    path = _build.PYCALLS
+    if os.path.exists(path):
+        import importlib.util
+        spec = importlib.util.spec_from_file_location("_pycalls", path)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        _fast = mod
+    else:
+        _fast = _CtypesCalls(_lib)
+
+
+def _calls():
+    if _fast is None:
+        lib()
+    return _fast
 
 
 # The per-call path is kept lean for decode-sized calls, where the host cost
@@ -103,6 +137,10 @@ except AttributeError:  # pragma: no cover - older torch
 
 def _ptr(t: torch.Tensor | None):
     return None if t is None else t.data_ptr()
+
+
+def _ptr0(t: torch.Tensor | None) -> int:
+    return 0 if t is None else t.data_ptr()
 
 
 def _stream(device) -> int:
@@ -185,10 +223,11 @@ def router_topk_fwd(logits: torch.Tensor, K: int, score_func: str = "softmax",
     routing_map = _out(routing_map, shape, torch.bool, dev, "routing_map")
     scores = _out(scores, shape, torch.float32, dev, "scores")
     with _on(dev):
-        rc = lib().router_topk_fwd(logits.data_ptr(), _DTYPE[dt], T, E, int(K),
-                                   _score(score_func), int(num_groups), int(group_topk),
-                                   float(scaling_factor), _ptr(expert_bias), probs.data_ptr(),
-                                   routing_map.data_ptr(), scores.data_ptr(), _stream(dev))
+        rc = _calls().router_topk_fwd(logits.data_ptr(), _DTYPE[dt], T, E, int(K),
+                                      _score(score_func), int(num_groups), int(group_topk),
+                                      float(scaling_factor), _ptr0(expert_bias),
+                                      probs.data_ptr(), routing_map.data_ptr(),
+                                      scores.data_ptr(), _stream(dev))
     _check("router_topk_fwd", rc)
     return probs, routing_map, scores
 
@@ -353,10 +392,10 @@ def router_topk_bwd(grad_probs: torch.Tensor, routing_map: torch.Tensor,
     dev = grad_probs.device
     grad_logits = _out(grad_logits, (T, E), grad_probs.dtype, dev, "grad_logits")
     with _on(dev):
-        rc = lib().router_topk_bwd(_ptr(grad_probs), _ptr(routing_map), _ptr(scores),
-                                   _DTYPE[grad_probs.dtype], T, E, int(K),
-                                   _score(score_func), float(scaling_factor),
-                                   _ptr(grad_logits), _stream(dev))
+        rc = _calls().router_topk_bwd(grad_probs.data_ptr(), routing_map.data_ptr(),
+                                      scores.data_ptr(), _DTYPE[grad_probs.dtype], T, E, int(K),
+                                      _score(score_func), float(scaling_factor),
+                                      grad_logits.data_ptr(), _stream(dev))
     _check("router_topk_bwd", rc)
     return grad_logits
 
@@ -374,9 +413,10 @@ def router_aux_scores_fwd(logits: torch.Tensor, K: int, score_func: str = "softm
     if score_func == "sigmoid" or intermediate is not None:
         intermediate = _out(intermediate, (T, E), torch.float32, dev, "intermediate")
     with _on(dev):
-        rc = lib().router_aux_scores_fwd(_ptr(logits), _DTYPE[logits.dtype], T, E, int(K),
-                                         _score(score_func), _ptr(scores), _ptr(routing_map),
-                                         _ptr(intermediate), _stream(dev))
+        rc = _calls().router_aux_scores_fwd(logits.data_ptr(), _DTYPE[logits.dtype], T, E,
+                                            int(K), _score(score_func), scores.data_ptr(),
+                                            routing_map.data_ptr(), _ptr0(intermediate),
+                                            _stream(dev))
     _check("router_aux_scores_fwd", rc)
     return scores, routing_map, (intermediate if intermediate is not None else scores)
 
@@ -396,9 +436,9 @@ def router_aux_scores_bwd(grad_scores: torch.Tensor, saved: torch.Tensor, K: int
     dev = grad_scores.device
     grad_logits = _out(grad_logits, (T, E), dtype, dev, "grad_logits")
     with _on(dev):
-        rc = lib().router_aux_scores_bwd(_ptr(grad_scores), _ptr(saved), _DTYPE[dtype], T, E,
-                                         int(K), _score(score_func), _ptr(grad_logits),
-                                         _stream(dev))
+        rc = _calls().router_aux_scores_bwd(grad_scores.data_ptr(), saved.data_ptr(),
+                                            _DTYPE[dtype], T, E, int(K), _score(score_func),
+                                            grad_logits.data_ptr(), _stream(dev))
     _check("router_aux_scores_bwd", rc)
     return grad_logits
 

@@ -202,3 +202,36 @@ def test_expert_maps_rejects(L):
              ctypes.c_size_t(0), None) == -1
     assert m(None, 0, 0, 64, 8, 0, 0, 0, 1.0, None, None, 8, None, 8, None, None, None, None,
              None, None, ctypes.c_size_t(0), None) == 0
+
+
+def test_cpython_shim_returns_the_c_status_codes():
+    # the CPython entry points of the hot calls convert their arguments and
+    # return the library's status, exactly as the ctypes entry points do
+    import os
+
+    import score_top_expert_gb300.router as R
+    from score_top_expert_gb300 import build as B
+    if not os.path.exists(B.PYCALLS):
+        pytest.skip("interpreter headers absent: the shim is not built")
+    L = R.lib()
+    fast = R._calls()
+    assert not isinstance(fast, R._CtypesCalls)
+    cases = [
+        ("router_topk_fwd", (0, 0, 0, 64, 4, 0, 0, 0, 1.0, 0, 0, 0, 0, 0)),   # T = 0
+        ("router_topk_fwd", (0, 0, 1, 4, 8, 0, 0, 0, 1.0, 0, 0, 0, 0, 0)),    # K > E
+        ("router_topk_fwd", (8, 0, 1, 4096, 8, 0, 0, 0, 1.0, 0, 8, 8, 8, 0)),  # E > 2304
+        ("router_topk_fwd", (8, 3, 1, 64, 4, 0, 0, 0, 1.0, 0, 8, 8, 8, 0)),   # bad dtype
+        ("router_topk_fwd", (8, 0, 1, 64, 4, 0, 3, 1, 1.0, 0, 8, 8, 8, 0)),   # E % groups
+        ("router_topk_bwd", (0, 0, 0, 0, 0, 64, 4, 0, 1.0, 0, 0)),            # T = 0
+        ("router_topk_bwd", (8, 8, 8, 0, 1, 64, 65, 0, 1.0, 8, 0)),           # K > E
+        ("router_aux_scores_fwd", (8, 0, 1, 64, 4, 2, 8, 8, 0, 0)),           # post-softmax
+        ("router_aux_scores_fwd", (8, 0, 1, 64, 4, 1, 8, 8, 0, 0)),           # sigmoid, no saved
+        ("router_aux_scores_bwd", (0, 0, 0, 0, 64, 4, 0, 0, 0)),              # T = 0
+        ("router_aux_scores_bwd", (8, 8, 0, 1, 3000, 4, 0, 8, 0)),            # E > 2304
+    ]
+    for name, args in cases:
+        assert getattr(fast, name)(*args) == getattr(L, name)(*args), (name, args)
+    with pytest.raises(TypeError):
+        fast.router_topk_fwd(0, 0)
+    with pytest.raises(OverflowError):
+        fast.router_topk_fwd(0, 0, 2 ** 40, 64, 4, 0, 0, 0, 1.0, 0, 0, 0, 0, 0)

@@ -26,7 +26,7 @@ def R():
     return r
 
 
-@pytest.fixture(params=["auto", "segment", "staged"])
+@pytest.fixture(params=["auto", "segment", "staged", "register"])
 def path(R, request):
     prev = R.force_path(request.param)
     yield request.param
@@ -135,6 +135,40 @@ def test_compact_bias_and_groups(R, path):
         bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
         for sf in ("softmax", "sigmoid", "softmax_post"):
             check_compact(R, case, K, sf, c=1.5, ng=ng, gk=gk, bias=bias)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E,K,ng,gk", [(512, 22, 0, 0), (512, 36, 0, 0), (256, 8, 8, 4),
+                                       (384, 12, 12, 4)])
+def test_register_compact_rows_in_sequence(R, E, K, ng, gk, dt):
+    # compact outputs on the register path with many rows per warp (each row
+    # starting from the previous row's threshold): normal, wide and
+    # integer-valued rows in a fixed cycle, with a bias
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    rng = np.random.default_rng(E + K + ng)
+    T = 12000
+    x = np.empty((T, E), dtype=np.float32)
+    for i in range(T):
+        kind = i % 3
+        x[i] = (rng.normal(0, 1, E) if kind == 0 else rng.normal(0, 3, E) if kind == 1
+                else rng.integers(-3, 4, E))
+    case = make_case(T, E, K, dtype=dt, seed=4)
+    case.logits = x if dt == "f32" else round_to_bf16_values(x)
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    prev = R.force_path("register")
+    try:
+        for sf in ("softmax", "sigmoid"):
+            check_compact(R, case, K, sf, c=1.5, ng=ng, gk=gk, bias=bias)
+            # without dense outputs: the same compact rows
+            xd, bd = to_dev(case.logits, dt), to_dev(bias)
+            full = R.router_topk_fwd_compact(xd, K, sf, ng, gk, 1.5, bd, dense=True)
+            only = R.router_topk_fwd_compact(xd, K, sf, ng, gk, 1.5, bd)
+            assert only[3] is None and only[4] is None and only[5] is None
+            for a, b in zip(full[:3], only[:3]):
+                assert torch.equal(a, b)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
 
 
 def test_compact_ties(R, path):
