@@ -753,7 +753,8 @@ SWEEP_K = (4, 8, 22, 36)
 
 def k_sweep(a):
     """Every (E, K) of SWEEP_E x SWEEP_K under both score functions, the four
-    kernels timed in isolation like the breakdown; one JSON line."""
+    kernels timed back to back over rotating buffer sets and in isolation
+    (L2 flushed before each launch); one JSON line."""
     import torch
 
     import score_top_expert_gb300.router as R
@@ -766,19 +767,24 @@ def k_sweep(a):
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     flush = L2Flush(torch, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     peak, peak_kind = hbm_peak()
     res = {}
     for E, name in zip(SWEEP_E, ("t8192_e512_k22", "t8192_e2304_k36")):
         for K in SWEEP_K:
             case, args = make_workload(name, K=K)
             for sf in ("softmax", "sigmoid"):
-                st = Step(R, torch, case, args, dev, sf)
-                res[f"e{E}_k{K}/{sf}"] = time_step_ops(torch, stream, flush, st, peak)
-                del st
+                sets = rotating_sets(R, torch, case, args, dev, sf, l2)
+                res[f"e{E}_k{K}/{sf}"] = {
+                    "steady": steady_step_ops(torch, stream, sets, peak),
+                    "isolated": time_step_ops(torch, stream, flush, sets[0], peak)}
+                del sets
+                torch.cuda.empty_cache()
     assert R.device_status() == 0
-    return {"sweep": "router kernels over (E, K), 8192 fp32 tokens, isolated (L2 flushed "
-                     "before each launch), median of 20", "peak_gbs": peak,
-            "peak_kind": peak_kind, "results": res}
+    return {"sweep": "router kernels over (E, K), 8192 fp32 tokens: steady = back to back "
+                     "over rotating buffer sets (CUDA graph, median of 10 replays); "
+                     "isolated = L2 flushed before each launch, median of 20",
+            "peak_gbs": peak, "peak_kind": peak_kind, "results": res}
 
 
 # the target matrix: E x K x score function at 8192 fp32 tokens (the pairs of
