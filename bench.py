@@ -507,7 +507,7 @@ def gpu_arm(a, world, rank, local):
     if not a.no_extra:
         out["target_matrix"] = target_matrix(torch, R, stream, dev, peak, l2)
         out["breakdown"] = breakdown(torch, R, stream, dev, peak, l2)
-        out["next_rows"] = next_rows(torch, R, stream, L2Flush(torch, dev), dev, peak)
+        out["next_rows"] = next_rows(torch, R, stream, L2Flush(torch, dev), dev, peak, l2)
         out["decode_us"] = decode_latency(torch, R, stream, dev)
         out["decode_eager_us"] = decode_eager(torch, R, stream, dev)
         out["decode_maps_us"] = decode_latency(torch, R, stream, dev, maps=True)
@@ -830,51 +830,78 @@ def target_matrix(torch, R, stream, dev, peak, l2):
     return res
 
 
-def next_rows(torch, R, stream, flush, dev, peak):
+def next_rows(torch, R, stream, flush, dev, peak, l2):
     """The compact forward, the expert maps and the aux loss on the benchmark
-    workloads, timed like the headline kernels (L2 flushed before each
-    launch; median of 20)."""
+    workloads: back to back over rotating copies of each call's buffers (more
+    than 3x L2 of bytes per launch; CUDA graph, median of 10 replays), and in
+    isolation (L2 flushed before each launch; median of 20)."""
     from score_top_expert_gb300.workloads import make_workload
     res = {}
     for name in ("t8192_e512_k22", "t8192_e2304_k36"):
         case, args = make_workload(name)
         T, E, K = case.logits.shape[0], case.logits.shape[1], args["K"]
-        x = torch.from_numpy(case.logits).to(dev)
-        w = torch.empty(T, K, device=dev)
-        idx = torch.empty(T, K, dtype=torch.int32, device=dev)
-        tei = torch.empty(T, K, dtype=torch.int32, device=dev)
-        maps_out = {"expert_first_token_offset": torch.empty(E + 1, dtype=torch.int32, device=dev)}
-        for nm in ("permuted_to_unpermuted", "unpermuted_to_permuted", "permuted_experts"):
-            maps_out[nm] = torch.empty(T * K, dtype=torch.int32, device=dev)
-        ws = torch.empty(R.lib().router_expert_maps_workspace_bytes(T, E), dtype=torch.uint8,
-                         device=dev)
-        q, amap, _ = R.router_aux_scores_fwd(x, K, "softmax")
-        loss = torch.empty(1, device=dev)
-        tok = torch.empty(E, dtype=torch.int32, device=dev)
-        lws = torch.empty(max(16, R.lib().router_aux_loss_workspace_bytes(T, E)),
-                          dtype=torch.uint8, device=dev)
-        gl = torch.ones(1, device=dev)
-        gq = torch.empty(T, E, device=dev)
-        ops = [
-            ("compact_fwd", lambda: R.router_topk_fwd_compact(
-                x, K, "softmax", topk_weights=w, topk_indices=idx, token_expert_indices=tei)),
-            ("expert_maps", lambda: R.router_expert_maps(idx, E, out=maps_out, workspace=ws)),
-            ("aux_loss_fwd", lambda: R.router_aux_loss_fwd(
-                q, amap, K, 0.01, loss=loss, tokens_per_expert=tok, workspace=lws)),
-            ("aux_loss_bwd", lambda: R.router_aux_loss_bwd(gl, tok, T, K, 0.01,
-                                                           grad_aux_scores=gq)),
-        ]
-        t = time_ops(torch, stream, flush, ops, 20, 3)
+        x0 = torch.from_numpy(case.logits).to(dev)
+        i32 = torch.int32
+
+        def compact_set():
+            x = x0.clone()
+            w = torch.empty(T, K, device=dev)
+            idx = torch.empty(T, K, dtype=i32, device=dev)
+            tei = torch.empty(T, K, dtype=i32, device=dev)
+            return lambda: R.router_topk_fwd_compact(
+                x, K, "softmax", topk_weights=w, topk_indices=idx, token_expert_indices=tei)
+
+        _, idx0, *_ = R.router_topk_fwd_compact(x0, K, "softmax")
+
+        def maps_set():
+            idx = idx0.clone()
+            out = {"expert_first_token_offset": torch.empty(E + 1, dtype=i32, device=dev)}
+            for nm in ("permuted_to_unpermuted", "unpermuted_to_permuted", "permuted_experts"):
+                out[nm] = torch.empty(T * K, dtype=i32, device=dev)
+            ws = torch.empty(R.lib().router_expert_maps_workspace_bytes(T, E), dtype=torch.uint8,
+                             device=dev)
+            return lambda: R.router_expert_maps(idx, E, out=out, workspace=ws)
+
+        q0, amap0, _ = R.router_aux_scores_fwd(x0, K, "softmax")
+
+        def loss_fwd_set():
+            q, amap = q0.clone(), amap0.clone()
+            loss = torch.empty(1, device=dev)
+            tok = torch.empty(E, dtype=i32, device=dev)
+            lws = torch.empty(max(16, R.lib().router_aux_loss_workspace_bytes(T, E)),
+                              dtype=torch.uint8, device=dev)
+            return lambda: R.router_aux_loss_fwd(q, amap, K, 0.01, loss=loss,
+                                                 tokens_per_expert=tok, workspace=lws)
+
+        _, tok0 = R.router_aux_loss_fwd(q0, amap0, K, 0.01)
+
+        def loss_bwd_set():
+            gl = torch.ones(1, device=dev)
+            tok = tok0.clone()
+            gq = torch.empty(T, E, device=dev)
+            return lambda: R.router_aux_loss_bwd(gl, tok, T, K, 0.01, grad_aux_scores=gq)
+
         row = {}
-        for i, (n, _) in enumerate(ops):
-            med = statistics.median(t[i])
+        for n, make in (("compact_fwd", compact_set), ("expert_maps", maps_set),
+                        ("aux_loss_fwd", loss_fwd_set), ("aux_loss_bwd", loss_bwd_set)):
             b = next_row_bytes(n, T, E, K, 4)
-            gbs = b / (med * 1e-3) / 1e9
-            row[n] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
-                      "frac": round(gbs / peak, 3), "bytes": b}
-        row["expert_maps"]["launches"] = "one cooperative launch (three beyond one wave)"
+            nsets = min(96, max(2, -(-3 * l2 // b)))
+            fns = [make() for _ in range(nsets)]
+            us = graph_us(torch, stream, fns)
+            t = time_ops(torch, stream, flush, [(n, fns[0])], 20, 3)
+            iso = statistics.median(t[0]) * 1e3
+            row[n] = {"us": round(us, 2), "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                      "frac": round(b / (us * 1e-6) / 1e9 / peak, 3), "bytes": b,
+                      "isolated": {"us": round(iso, 2),
+                                   "frac": round(b / (iso * 1e-6) / 1e9 / peak, 3)}}
+            del fns
+            torch.cuda.empty_cache()
+        row["expert_maps"]["launches"] = ("a one-block kernel zeroing the barrier counter and "
+                                          "one cooperative launch (three launches beyond one "
+                                          "wave)")
+        row["aux_loss_fwd"]["launches"] = "a one-block kernel zeroing the counters and one launch"
         res[f"{name}/softmax/f32"] = row
-        del x, q, amap, gq
+        del x0, q0, amap0
         torch.cuda.empty_cache()
     return res
 

@@ -190,9 +190,9 @@ MR_API int router_topk_fwd_compact(const void* logits, mr_dtype dtype, int T, in
  * and it takes no permuted row.
  * workspace: device memory of router_expert_maps_workspace_bytes(T, E)
  * bytes, 16-byte aligned; its contents need no initialisation.  On the
- * stream: a memset and one cooperative launch when the batch's 64-token
- * tiles fit on the GPU at once, else three launches; deterministic either
- * way (identical results).
+ * stream: a one-block kernel that zeroes a counter and one cooperative
+ * launch when the batch's 64-token tiles fit on the GPU at once, else three
+ * launches; deterministic either way (identical results).
  *
  * MR_ERR_INVALID: T < 0, E < 1, K < 1, K > E, ld_indices < K, T*E > INT_MAX,
  *   a NULL pointer when T > 0, a small or misaligned workspace.
@@ -326,9 +326,10 @@ MR_API int router_aux_scores_bwd(const float* grad_scores, const float* saved,
  *                    aligned, owned by the caller; its contents need no
  *                    initialisation and are overwritten
  *
- * A memset of the workspace's counters and one kernel on `stream`; the
- * reduction order is fixed (compensated fp32 sums, no floating-point
- * atomics), so repeated calls give identical bits.  T == 0 is a no-op (nothing written).
+ * A one-block kernel that zeroes the workspace's counters, then one kernel,
+ * both on `stream`; the reduction order is fixed (compensated fp32 sums, no
+ * floating-point atomics) and depends on T, E and the row layout only, so
+ * repeated calls give identical bits.  T == 0 is a no-op (nothing written).
  * MR_ERR_INVALID: T < 0, E < 1, K outside [1, E], T*E > INT_MAX, a NULL
  * pointer when T > 0, a workspace too small or misaligned.
  * MR_ERR_UNSUPPORTED: E > MR_MAX_EXPERTS.

@@ -3,15 +3,18 @@
 //
 // Forward: one launch, deterministic (fixed summation orders, compensated
 // fp32 sums, no floating-point atomics).  The grid is B row ranges x G
-// column groups of 128 experts (32 with scalar rows):
+// column groups of 128 experts (32 with scalar rows), B chosen so that the
+// grid is about four blocks on each SM (at most 64 ranges):
 //   1  block (b, g): lane l owns the four experts of chunk 32 g + l, warp w
 //      the rows w, w + 8, ... of range b (eight rows' loads in flight); the
 //      8 warps combine in order and the block writes its partial row;
 //   2  the last block of group g to finish (a counter per group) adds the B
-//      partial rows of its experts, writes tokens_per_expert and the group's
-//      share of  loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e;
+//      partial rows of its experts (all of a warp's rows loaded at once),
+//      writes tokens_per_expert and the group's share of
+//        loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e;
 //   3  the last group to finish adds the shares in group order.
-// The counters are zeroed by a memset on the stream before the launch.
+// The counters are zeroed by a one-block kernel on the stream before the
+// launch.
 // Backward: grad[t, e] = grad_loss * coeff E / (K T^2) * tokens_e, a pure
 // streaming write (blocks stride over rows, threads over 16-byte chunks).
 #include <atomic>
@@ -28,6 +31,11 @@ namespace moe_router {
 constexpr int kAuxThreads = 256;
 constexpr int kAuxWarps = kAuxThreads / 32;
 constexpr int kAuxMaxBlocks = 64;  // row ranges (partial rows)
+// Blocks a forward launch aims for: one wave of three blocks on each of the
+// 152 SMs of a GB300 (fixed, so the summation order does not depend on the
+// GPU).
+constexpr int kAuxBlocksPerSm = 3;
+constexpr int kAuxTargetBlocks = kAuxBlocksPerSm * 152;
 
 __host__ __device__ inline int aux_blocks(int T) { return T < kAuxMaxBlocks ? T : kAuxMaxBlocks; }
 
@@ -91,10 +99,10 @@ __device__ __forceinline__ void aux_load(const float* __restrict__ q, const uint
   }
 }
 
-// Four blocks per SM (at most 64 registers a thread): the row phase needs
-// many warps in flight.
+// Three blocks per SM (at most 80 registers a thread: the partial-row phase
+// holds eight partial rows per lane in flight).
 template <bool VEC>
-__global__ void __launch_bounds__(kAuxThreads, 4)
+__global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm)
 aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, int T, int E,
                 int rows_per_block, float scale, AuxScratch ws, float* __restrict__ loss,
                 int32_t* __restrict__ tokens) {
@@ -153,11 +161,18 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
         kahan_add(s, c, sq[v][lane][i]);
         n += sn[v][lane][i];
       }
-      const int e = e0 + i;
-      if (e < E) {
-        ws.part_q[static_cast<size_t>(b) * E + e] = s - c;
-        ws.part_n[static_cast<size_t>(b) * E + e] = n;
-      }
+      acc.q[i] = s - c;
+      acc.n[i] = n;
+    }
+    const size_t o = static_cast<size_t>(b) * E + e0;
+    if constexpr (VEC) {  // E % 4 == 0: the lane's four experts all exist
+      __stcg(reinterpret_cast<float4*>(ws.part_q + o),
+             make_float4(acc.q[0], acc.q[1], acc.q[2], acc.q[3]));
+      __stcg(reinterpret_cast<int4*>(ws.part_n + o),
+             make_int4(acc.n[0], acc.n[1], acc.n[2], acc.n[3]));
+    } else {
+      ws.part_q[o] = acc.q[0];
+      ws.part_n[o] = acc.n[0];
     }
   }
   __syncthreads();
@@ -171,7 +186,37 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
   // ---- 2: the last block of group g adds the partial rows -------------------
   __threadfence();
   acc.zero();
-  if (mine) {
+  if constexpr (VEC) {
+    // a warp's partial rows w, w + 8, ... (nb <= kAuxMaxBlocks: one batch),
+    // added in that order
+    constexpr int R = (kAuxMaxBlocks + kAuxWarps - 1) / kAuxWarps;
+    if (mine) {
+      float4 pq[R];
+      int4 pn[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int bj = w + j * kAuxWarps;
+        const size_t o = static_cast<size_t>(bj) * E + e0;
+        pq[j] = bj < nb ? __ldcg(reinterpret_cast<const float4*>(ws.part_q + o))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        pn[j] = bj < nb ? __ldcg(reinterpret_cast<const int4*>(ws.part_n + o))
+                        : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (w + j * kAuxWarps < nb) {
+          kahan_add(acc.q[0], acc.c[0], pq[j].x);
+          kahan_add(acc.q[1], acc.c[1], pq[j].y);
+          kahan_add(acc.q[2], acc.c[2], pq[j].z);
+          kahan_add(acc.q[3], acc.c[3], pq[j].w);
+          acc.n[0] += pn[j].x;
+          acc.n[1] += pn[j].y;
+          acc.n[2] += pn[j].z;
+          acc.n[3] += pn[j].w;
+        }
+      }
+    }
+  } else if (mine) {
     for (int pb = w; pb < nb; pb += kAuxWarps * kBatch2) {
       float pq[kBatch2][N];
       int pn[kBatch2][N];
@@ -229,11 +274,17 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
   __syncthreads();
 
   // ---- 3: the last group adds the shares in order ---------------------------
-  if (last && threadIdx.x == 0) {
+  // (warp 0 loads them all at once and every lane adds them in group order)
+  if (last && w == 0) {
     __threadfence();
+    const int G = static_cast<int>(gridDim.y);
     float total = 0.0f, comp = 0.0f;
-    for (int j = 0; j < static_cast<int>(gridDim.y); ++j) kahan_add(total, comp, __ldcg(ws.shares + j));
-    loss[0] = scale * (total - comp);
+    for (int c0 = 0; c0 < G; c0 += 32) {
+      const float sh = c0 + lane < G ? __ldcg(ws.shares + c0 + lane) : 0.0f;
+      const int m = G - c0 < 32 ? G - c0 : 32;
+      for (int j = 0; j < m; ++j) kahan_add(total, comp, __shfl_sync(0xffffffffu, sh, j));
+    }
+    if (lane == 0) loss[0] = scale * (total - comp);
   }
 }
 
@@ -277,19 +328,24 @@ int sm_count() {
   return n;
 }
 
-// The forward over nb partial rows in the scratch ws: a memset of the
-// completion counters and one launch.
+// The forward with its partial rows in the scratch at `scratch` (at least
+// aux_workspace_bytes(T, E) bytes, 16-byte aligned): a one-block kernel that
+// zeroes the completion counters, then the forward.  The number of row
+// ranges depends on T, E and the row layout only, so both entry points (and
+// every GPU) sum in the same order.
 int launch_aux_loss(const float* q, const uint8_t* map, int T, int E, int K, float coeff,
-                    float* loss, int32_t* tokens, const AuxScratch& ws, int nb, cudaStream_t st) {
-  const int rows = (T + nb - 1) / nb;
+                    float* loss, int32_t* tokens, void* scratch, cudaStream_t st) {
   const bool vec = E % 4 == 0 && aligned16(q) && (reinterpret_cast<uintptr_t>(map) & 3u) == 0;
   const int per_group = vec ? 128 : 32;
   const int groups = (E + per_group - 1) / per_group;
+  int nb = kAuxTargetBlocks / groups;
+  if (nb < 1) nb = 1;
+  if (nb > aux_blocks(T)) nb = aux_blocks(T);
+  const int rows = (T + nb - 1) / nb;
+  const AuxScratch ws = aux_scratch(scratch, nb, E);
   const float scale = static_cast<float>(static_cast<double>(coeff) * E /
                                          (static_cast<double>(K) * T * static_cast<double>(T)));
-  if (cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(groups + 1) * sizeof(unsigned int),
-                      st) != cudaSuccess)
-    return MR_ERR_CUDA;
+  if (launch_zero_words(ws.counters, groups + 1, st) != cudaSuccess) return MR_ERR_CUDA;
   const dim3 grid(nb, groups);
   const cudaError_t e =
       vec ? launch_kernel(aux_loss_kernel<true>, grid, dim3(kAuxThreads), 0, st, q, map, T, E,
@@ -367,10 +423,8 @@ int router_aux_loss_fwd(const float* aux_scores, const uint8_t* routing_map, int
       tokens_per_expert == nullptr || workspace == nullptr)
     return MR_ERR_INVALID;
   if (workspace_bytes < aux_workspace_bytes(T, E) || !aligned16(workspace)) return MR_ERR_INVALID;
-  const int nb = aux_blocks(T);
   return launch_aux_loss(aux_scores, routing_map, T, E, K, coeff, loss, tokens_per_expert,
-                         aux_scratch(workspace, nb, E), nb,
-                         reinterpret_cast<cudaStream_t>(stream));
+                         workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert, int T, int E,
@@ -398,23 +452,21 @@ int router_aux_loss_bwd(const float* grad_loss, const int32_t* tokens_per_expert
   return cudaGetLastError() == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }
 
-// The same launch as router_aux_loss_fwd (which uses the same number of
-// partial rows, at most kNoAllocBlocks).  Every partial the launch reads is
-// written by its own blocks, and the call zeroes the completion counters
-// with a memset first, so nothing in the scratch has to start at zero and a
+// The same launches as router_aux_loss_fwd (the same number of partial
+// rows, at most aux_blocks(T) <= kNoAllocBlocks).  Every partial the launch
+// reads is written by its own blocks, and the call zeroes the completion
+// counters first, so nothing in the scratch has to start at zero and a
 // previous call's contents are never read.
 int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_map, int T, int E,
                                 int K, float coeff, float* loss, int32_t* tokens_per_expert,
                                 mr_stream_t stream) {
   const int rc = aux_check(T, E, K);
   if (rc != MR_OK) return rc;
-  const int nb = T < kNoAllocBlocks ? T : kNoAllocBlocks;
+  static_assert(kAuxMaxBlocks <= kNoAllocBlocks, "partial rows of the scratch array");
   // Cannot fire while aux_check caps E at MR_MAX_EXPERTS (the array is sized
   // for that E and kNoAllocBlocks rows); kept as a guard should either limit
   // change.
-  if (static_cast<size_t>(nb) * static_cast<size_t>(E) * 8u + kAuxTailBytes >
-      sizeof(g_aux_noalloc_scratch))
-    return MR_ERR_UNSUPPORTED;
+  if (aux_workspace_bytes(T, E) > sizeof(g_aux_noalloc_scratch)) return MR_ERR_UNSUPPORTED;
   if (T == 0) return MR_OK;
   if (aux_scores == nullptr || routing_map == nullptr || loss == nullptr ||
       tokens_per_expert == nullptr)
@@ -423,7 +475,7 @@ int router_aux_loss_fwd_noalloc(const float* aux_scores, const uint8_t* routing_
   const int sc = noalloc_scratch(&scratch);
   if (sc != MR_OK) return sc;
   return launch_aux_loss(aux_scores, routing_map, T, E, K, coeff, loss, tokens_per_expert,
-                         aux_scratch(scratch, nb, E), nb, reinterpret_cast<cudaStream_t>(stream));
+                         scratch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -60,6 +60,24 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Zeroes n words at p (one block of up to 1024 threads, n <= 1024).  Calls
+// that need zeroed counters launch it instead of a memset: in a stream or a
+// CUDA graph a memset costs several times a kernel launch between two
+// kernels, and unlike a memset this launch takes part in the programmatic
+// serialization above.
+template <typename Word>
+__global__ void zero_words_kernel(Word* __restrict__ p, int n) {
+  pdl_enter();
+  if (static_cast<int>(threadIdx.x) < n) p[threadIdx.x] = Word(0);
+}
+
+template <typename Word>
+cudaError_t launch_zero_words(Word* p, int n, cudaStream_t st) {
+  if (n < 1 || n > 1024) return cudaErrorInvalidValue;
+  const unsigned threads = static_cast<unsigned>((n + 31) / 32 * 32);
+  return launch_kernel(zero_words_kernel<Word>, dim3(1), dim3(threads), 0, st, p, n);
+}
+
 // SF_SOFTMAX_POST scores like softmax (over all E) and renormalises the
 // selected probabilities like sigmoid (the softmax of the selected logits).
 enum { SF_SOFTMAX = 0, SF_SIGMOID = 1, SF_SOFTMAX_POST = 2 };

@@ -13,9 +13,10 @@
 //   3  scatter: every block rebuilds its masks and places each choice at
 //        offset[e] + (earlier tiles) + popcount(mask[e] below its token).
 // When every tile's block fits on the GPU at once, the three phases run as
-// one cooperative launch instead, separated by a grid barrier (bounded in
-// time like every wait of this library), and the scatter reuses the masks
-// of phase 1 from shared memory.
+// one cooperative launch instead (after a one-block kernel that zeroes the
+// barrier's counter), separated by a grid barrier (bounded in time like
+// every wait of this library), and the scatter reuses the masks of phase 1
+// from shared memory.
 #include <climits>
 #include <cstddef>
 #include <cstdint>
@@ -231,38 +232,46 @@ maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, i
   if (!grid_barrier(barrier, 1u, status, verdict)) return;
 
   // ---- 2: column prefixes: blocks take groups of 32 experts (a lane each),
-  //      the 8 warps split the tiles, then add the sums of the warps before
-  //      them (coalesced 128-byte rows, as the stand-alone prefix kernel) ---
+  //      the 8 warps split the tiles (coalesced 128-byte rows); a warp sums
+  //      its tiles' counts, then, after the sums of the warps before it,
+  //      writes their exclusive prefixes (each pass loads 16 tiles at once) -
   {
     constexpr int W = kMapsThreads / 32;
+    constexpr int B = 16;  // loads in flight per lane
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int* wsum = tmp;  // W x 32 ints, past the scan slots (sized in maps_smem_fused)
     const int per = (nb + W - 1) / W;
     const int b0 = min(nb, w * per), b1 = min(nb, b0 + per);
     for (int grp = blockIdx.x; grp * 32 < E; grp += nb) {
       const int e = grp * 32 + lane;
-      int run = 0;
+      int sum = 0;
       if (e < E) {
-        for (int b = b0; b < b1; b += 4) {
-          int c[4];
+        for (int b = b0; b < b1; b += B) {
+          int c[B];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < B; ++j)
             c[j] = b + j < b1 ? __ldcg(counts + static_cast<size_t>(b + j) * E + e) : 0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (b + j < b1) counts[static_cast<size_t>(b + j) * E + e] = run;
+          for (int j = 0; j < B; ++j) sum += c[j];
+        }
+      }
+      wsum[w * 32 + lane] = sum;
+      __syncthreads();
+      int run = 0;
+      for (int v = 0; v < w; ++v) run += wsum[v * 32 + lane];
+      if (e < E) {
+        if (w == W - 1) totals[e] = run + sum;
+        for (int b = b0; b < b1; b += B) {
+          int c[B];
+#pragma unroll
+          for (int j = 0; j < B; ++j)
+            c[j] = b + j < b1 ? __ldcg(counts + static_cast<size_t>(b + j) * E + e) : 0;
+#pragma unroll
+          for (int j = 0; j < B; ++j) {
+            if (b + j < b1) __stcg(counts + static_cast<size_t>(b + j) * E + e, run);
             run += c[j];
           }
         }
-      }
-      wsum[w * 32 + lane] = run;
-      __syncthreads();
-      int base = 0;
-      for (int v = 0; v < w; ++v) base += wsum[v * 32 + lane];
-      if (e < E) {
-        if (base != 0)
-          for (int b = b0; b < b1; ++b) counts[static_cast<size_t>(b) * E + e] += base;
-        if (w == W - 1) totals[e] = base + run;
       }
       __syncthreads();
     }
@@ -366,7 +375,7 @@ int launch_expert_maps(const int32_t* idx, long long ld, int T, int E, int K, in
   int* status = device_status_word();
   if (status != nullptr && nb <= maps_fused_capacity(E)) {
     // one cooperative launch: every tile's block is resident
-    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), st) != cudaSuccess) return MR_ERR_CUDA;
+    if (launch_zero_words(counter, 1, st) != cudaSuccess) return MR_ERR_CUDA;
     void* args[] = {&idx, &ld, &T, &E, &K, &counts, &totals, &counter, &status,
                     &offsets, &p2u, &u2p, &pexp};
     const cudaError_t e = cudaLaunchCooperativeKernel(
