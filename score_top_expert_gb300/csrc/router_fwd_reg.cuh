@@ -403,11 +403,12 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     // ---- 4 / 5: exact K-th largest key by bisection -------------------------------
     uint32_t lo, hi = RK::of(row_max) + 1u;
     int n_lo;
+    // count_at(m): this lane's keys at or above key m
     auto bisect = [&](auto count_at) {
 #pragma unroll 1
       while (n_lo != K && hi - lo > 1u) {
         const uint32_t mid = lo + ((hi - lo) >> 1);
-        const int c = warp_add(count_at(RK::to_float(mid)));
+        const int c = warp_add(count_at(mid));
         if (c >= K) {
           lo = mid;
           n_lo = c;
@@ -431,25 +432,32 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
       lo = RK::of(t);
       if (RK::to_float(lo) < t) ++lo;
       n_lo = n;
+      // the bisection compares keys (x >= to_float(m) exactly when
+      // RK::of(x) >= m; an empty slot's -inf keys below every finite one)
       if (n <= 32) {
         o[0] = slot(0);
         __syncwarp();  // the slots are free again (the next row writes them)
-        bisect([&](float m) { return static_cast<int>(o[0] >= m); });
+        const uint32_t k0 = RK::of(o[0]);
+        bisect([&](uint32_t m) { return static_cast<int>(k0 >= m); });
       } else if (n <= 64) {
         o[0] = slot(0);
         o[1] = slot(1);
         __syncwarp();
-        bisect([&](float m) { return (o[0] >= m) + (o[1] >= m); });
+        const uint32_t k0 = RK::of(o[0]), k1 = RK::of(o[1]);
+        bisect([&](uint32_t m) { return (k0 >= m) + (k1 >= m); });
       } else {
 #pragma unroll
         for (int r = 0; r < 4; ++r) o[r] = slot(r);
         __syncwarp();
-        bisect([&](float m) { return (o[0] >= m) + (o[1] >= m) + (o[2] >= m) + (o[3] >= m); });
+        uint32_t k[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) k[r] = RK::of(o[r]);
+        bisect([&](uint32_t m) { return (k[0] >= m) + (k[1] >= m) + (k[2] >= m) + (k[3] >= m); });
       }
     } else {
       lo = RK::lowest();
       n_lo = E;  // every real logit is finite
-      bisect(count_ge);
+      bisect([&](uint32_t m) { return count_ge(RK::to_float(m)); });
     }
     const float v = RK::to_float(lo);
     int ti = INT_MAX;  // selected: x > v, or x == v with index <= ti
