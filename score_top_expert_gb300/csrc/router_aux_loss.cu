@@ -65,6 +65,18 @@ __host__ __device__ inline AuxScratch aux_scratch(void* base, int nb, int E) {
   return s;
 }
 
+// Arrival on a completion counter: one acquire-release atomic add at GPU
+// scope.  The release publishes the block's earlier writes (ordered before
+// it by the block barrier that precedes the call); the acquire lets the
+// block that arrives last read every other block's writes (the rest of its
+// threads after the next block barrier).  Returns the previous count.
+__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* counter) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+               : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
 // Compensated (Kahan) fp32 addition: sum - c carries the running total.
 __device__ __forceinline__ void kahan_add(float& sum, float& c, float v) {
   const float y = v - c;
@@ -177,14 +189,12 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(&ws.counters[g], 1u) == static_cast<unsigned>(nb) - 1u;
+    last = arrive_acq_rel(&ws.counters[g]) == static_cast<unsigned>(nb) - 1u;
   }
   __syncthreads();
   if (!last) return;
 
   // ---- 2: the last block of group g adds the partial rows -------------------
-  __threadfence();
   acc.zero();
   if constexpr (VEC) {
     // a warp's partial rows w, w + 8, ... (nb <= kAuxMaxBlocks: one batch),
@@ -267,8 +277,7 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
     for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
     if (lane == 0) {
       ws.shares[g] = term;
-      __threadfence();
-      last = atomicAdd(&ws.counters[gridDim.y], 1u) == gridDim.y - 1u;
+      last = arrive_acq_rel(&ws.counters[gridDim.y]) == gridDim.y - 1u;
     }
   }
   __syncthreads();
@@ -276,7 +285,6 @@ aux_loss_kernel(const float* __restrict__ q, const uint8_t* __restrict__ map, in
   // ---- 3: the last group adds the shares in order ---------------------------
   // (warp 0 loads them all at once and every lane adds them in group order)
   if (last && w == 0) {
-    __threadfence();
     const int G = static_cast<int>(gridDim.y);
     float total = 0.0f, comp = 0.0f;
     for (int c0 = 0; c0 < G; c0 += 32) {

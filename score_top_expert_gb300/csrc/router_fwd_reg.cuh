@@ -202,12 +202,15 @@ __device__ __forceinline__ void group_mask(const FwdArgs& a, int lane, float (&s
 }
 
 // Registers per thread: 64 keeps 32 warps per SM; the compact-output kernels
-// at 512 experts get 80 (25 warps), which spills much less.
-template <int NC, int OP, int KM>
-constexpr int reg_max_regs() { return (NC == 4 && OP == 2) ? 80 : 64; }
+// at 512 experts get 80 (25 warps), which spills much less, except fp32 rows
+// of exactly 512 experts without bias or groups, which fit 64.
+template <int NC, int OP, int KM, bool FULL, int DT>
+constexpr int reg_max_regs() {
+  return (NC == 4 && OP == 2 && !(KM == 0 && FULL && DT == DT_F32)) ? 80 : 64;
+}
 
 template <int SF, int DT, int NC, int OP, bool FULL, int KM>
-__global__ void __launch_bounds__(kRegMaxWarps * 32) __maxnreg__((reg_max_regs<NC, OP, KM>()))
+__global__ void __launch_bounds__(kRegMaxWarps * 32) __maxnreg__((reg_max_regs<NC, OP, KM, FULL, DT>()))
 router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
   pdl_enter();
   static_assert(NC == 2 || NC == 4, "rows of up to 256 or 512 experts");
@@ -500,6 +503,20 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
     have_spec = ok;
 
     // ---- 6: outputs -----------------------------------------------------------------
+    // score k: compact outputs without bias or groups (OP 2, KM 0) recompute
+    // it from the logit (the same instructions, so the same bits), which
+    // frees the scores' registers after the row sum (the empty asm keeps the
+    // compiler from reusing the first computation instead)
+    auto wv = [&](int k) -> float {
+      if constexpr (OP == 2 && KM == 0) {
+        float xk = x[k];
+        asm("" : "+f"(xk));
+        if constexpr (SF != SF_SIGMOID) return exp_shifted(xk, max_l2e);
+        else return sigmoid_f32(xk);
+      } else {
+        return w[k];
+      }
+    };
     auto emit = [&](auto tie_tag) {
       constexpr bool kTie = decltype(tie_tag)::value;
       auto sel = [&](int k, int idx) -> bool {
@@ -512,11 +529,43 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
         float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < N; ++k)
-          if (sel(k, 4 * (lane + 32 * (k >> 2)) + (k & 3))) part += w[k];
+          if (sel(k, 4 * (lane + 32 * (k >> 2)) + (k & 3))) part += wv(k);
         pf = a.scaling / seg_sum<32>(part);
       } else if constexpr (OP != 1) {
         pf = a.scaling * inv;
       }
+      // dense outputs straight from registers
+      auto dense_outputs = [&]() {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          const int c = lane + 32 * j;
+          if (FULL || c < nchunks) {
+            bool m[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m[u] = sel(4 * j + u, 4 * c + u);
+            if (OP != 2 || a.map != nullptr) store_map4<true>(a.map, off, 4 * c, E, m);
+            float s[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? wv(4 * j + u) * inv : wv(4 * j + u);
+            if constexpr (OP != 1) {
+              float p[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) p[u] = m[u] ? wv(4 * j + u) * pf : 0.0f;
+              if (OP == 0 || a.probs != nullptr) store4<DT, true>(a.probs, off, 4 * c, E, p);
+              if (OP == 0 || a.scores != nullptr) store4_f32<true>(a.scores, off, 4 * c, E, s);
+            } else if constexpr (SF == SF_SOFTMAX) {
+              store4_f32<true>(a.scores, off, 4 * c, E, s);
+              if (a.intermediate != nullptr) store4_f32<true>(a.intermediate, off, 4 * c, E, s);
+            } else {
+              float q[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) q[u] = s[u] * inv;
+              store4_f32<true>(a.scores, off, 4 * c, E, q);
+              store4_f32<true>(a.intermediate, off, 4 * c, E, s);
+            }
+          }
+        }
+      };
       if constexpr (OP == 2) {
         // compact outputs: the K selected (key, ~index) words and their
         // weights go to the warp's slots by a prefix count, each word's rank
@@ -534,10 +583,13 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
           const int idx = 4 * (lane + 32 * (k >> 2)) + (k & 3);
           if (sel(k, idx)) {
             wd[pos] = pack_key(ordered_key(sk[k]), idx);
-            wt[pos] = w[k] * pf;
+            wt[pos] = wv(k) * pf;
             ++pos;
           }
         }
+        // the dense outputs, when asked for, before the ranking: the row's
+        // registers are then free for it
+        if (a.map != nullptr || a.probs != nullptr || a.scores != nullptr) dense_outputs();
         __syncwarp();
         const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(wd) + 1;  // keys
         const int i1 = lane + 32;
@@ -573,37 +625,8 @@ router_fwd_reg_kernel(const FwdArgs a, const RegLayout L, int* status) {
           if (a.tei != nullptr) a.tei[t * K + r1] = r1 * T + row;
         }
         __syncwarp();  // the slots are free again
-        if (a.map == nullptr && a.probs == nullptr && a.scores == nullptr) return;
       }
-#pragma unroll
-      for (int j = 0; j < NC; ++j) {
-        const int c = lane + 32 * j;
-        if (FULL || c < nchunks) {
-          bool m[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) m[u] = sel(4 * j + u, 4 * c + u);
-          if (OP != 2 || a.map != nullptr) store_map4<true>(a.map, off, 4 * c, E, m);
-          float s[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) s[u] = (SF != SF_SIGMOID) ? w[4 * j + u] * inv : w[4 * j + u];
-          if constexpr (OP != 1) {
-            float p[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) p[u] = m[u] ? w[4 * j + u] * pf : 0.0f;
-            if (OP == 0 || a.probs != nullptr) store4<DT, true>(a.probs, off, 4 * c, E, p);
-            if (OP == 0 || a.scores != nullptr) store4_f32<true>(a.scores, off, 4 * c, E, s);
-          } else if constexpr (SF == SF_SOFTMAX) {
-            store4_f32<true>(a.scores, off, 4 * c, E, s);
-            if (a.intermediate != nullptr) store4_f32<true>(a.intermediate, off, 4 * c, E, s);
-          } else {
-            float q[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) q[u] = s[u] * inv;
-            store4_f32<true>(a.scores, off, 4 * c, E, q);
-            store4_f32<true>(a.intermediate, off, 4 * c, E, s);
-          }
-        }
-      }
+      if constexpr (OP != 2) dense_outputs();
     };
     if (ti == INT_MAX) emit(std::false_type{});
     else emit(std::true_type{});
