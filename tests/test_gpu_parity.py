@@ -502,11 +502,17 @@ def test_bounded_wait_reports_a_timeout(R):
 # ---------------------------------------------------------------------------
 # load-balancing aux loss
 # ---------------------------------------------------------------------------
-AUX_LOSS_REL = 1e-5  # fp32 column partials over <= 32 rows, summed in double
+# fp32 sums: plain over a warp's rows of one block (at most a few hundred at these
+# sizes), compensated across the block's warps and across blocks
+AUX_LOSS_REL = 1e-5
 
 
+# the row ranges per launch follow T and the column groups: one row per range (64 x
+# 512), empty trailing ranges (65 x 2304: 25 ranges of 3 rows), 57 ranges (1024
+# experts), scalar rows (257 experts)
 @pytest.mark.parametrize("T,E,K", [(8192, 512, 22), (8192, 2304, 36), (1000, 257, 5), (77, 64, 4),
-                                   (300, 2304, 36), (1, 8, 1)])
+                                   (300, 2304, 36), (1, 8, 1), (64, 512, 8), (65, 2304, 8),
+                                   (4096, 1024, 8)])
 def test_aux_loss(R, T, E, K):
     case = make_case(T, E, K, seed=T + E)
     for sf in ("softmax", "sigmoid"):
