@@ -140,8 +140,9 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km, int op) {
     off += MR_MAX_TOPK * 8;
   }
   L.bar_off = round_up(off, 16);
-  off = L.bar_off + 32;
+  off = L.bar_off + 48;
   L.seg_bytes = round_up(off, 128);
+  L.steal = 0;
   return L;
 }
 
@@ -224,6 +225,20 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
     if (per_sm * p.warps_per_block > cap_warps) per_sm = cap_warps / p.warps_per_block;
     valid = per_sm > 0;
     p.max_blocks = per_sm * di.sms;
+  }
+  // the stealing launch (one-warp blocks, logit keys, OP 0 to 2): how many
+  // such blocks are resident at once (tuning override MOE_ROUTER_STEAL=0)
+  p.steal_blocks = 0;
+  static const bool steal_on = [] {
+    const char* env = std::getenv("MOE_ROUTER_STEAL");
+    return env == nullptr || std::strcmp(env, "0") != 0;
+  }();
+  if (valid && steal_on && p.seg == 32 && km == 0 && op <= 2) {
+    StagedPlan one = p;
+    one.warps_per_block = 1;
+    int per_sm = occupancy_any(sf, dt, one);
+    if (per_sm > cap_warps) per_sm = cap_warps;
+    p.steal_blocks = per_sm * di.sms;
   }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_nplans < kPlanCache)

@@ -7,6 +7,11 @@
 // copy of its next row fills the other, so every segment keeps a row in
 // flight without holding it in registers.  Segments only synchronise among
 // their own lanes, so the segments of a warp may take different paths.
+// Batches larger than the resident warps (logit keys, OP 0 to 2) launch
+// instead one one-warp block per row; a running warp takes over the rows of
+// blocks that have not started yet (cluster launch control), one request
+// ahead, so the rows go to whichever warps finish first and the batch's
+// tail stays short.
 //
 // Per row (lane l of the segment holds chunks c = l + SEG j, four consecutive
 // experts each):
@@ -68,8 +73,11 @@ struct StagedLayout {
   int cand_off;     // kCandPerLane * SEG packed candidate words
   int sorted_off;   // OP 2, 3: the K selected words by rank (MR_MAX_TOPK words)
   int mask_off;     // selection words, one bit per expert of the padded row
-  int bar_off;      // two mbarriers and one 32-bit slot
+  int bar_off;      // two mbarriers, one 32-bit slot, and for stealing launches
+                    // a third mbarrier (at +24) and a 16-byte response (at +32)
   int seg_bytes;    // slice size, multiple of 128
+  int steal;        // 1: one-warp blocks, one row each, that take over the rows
+                    // of blocks not yet started (cluster launch control)
 };
 
 constexpr int kStagedMaxWarps = 12;
@@ -290,9 +298,18 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       bias_s[i] = (a.bias != nullptr && i < E) ? a.bias[i] : 0.0f;
     __syncthreads();
   }
+  // Stealing launches (one row per one-warp block, whole rows per warp): the
+  // warp's next rows are those of blocks it cancels before they start, one
+  // request in flight, so rows go to whichever warps finish first.
+  constexpr bool kCanSteal = SEG == 32 && KM == 0 && OP <= 2;
+  const bool steal = kCanSteal && L.steal != 0;
+  uint64_t* clc_bar = bars + 3;
+  unsigned char* clc_resp = reinterpret_cast<unsigned char*>(bars) + 32;
+  uint32_t clc_phase = 0;
   if (li == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    if (steal) mbar_init(clc_bar, 1);
     fence_mbar_init();
   }
   __syncwarp(smask);
@@ -304,6 +321,25 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     if (row0 + nsegs < T)
       bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nsegs) * row_bytes,
                 row_bytes, &bars[1]);
+    if (steal && row0 < T) clc_request(clc_resp, clc_bar);
+  }
+  int cur = row0, nxt = -1;  // stealing: this row and the next (-1: none)
+  bool pending = false;      // stealing: a request is in flight
+  if (steal && row0 < T) {
+    const bool got = mbar_wait_bounded(clc_bar, clc_phase);
+    clc_phase ^= 1u;
+    if (got) nxt = clc_cancelled_x(clc_resp);
+    else if (li == 0) atomicExch(status, kDeviceWaitTimeout);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (nxt >= 0) {
+      pending = true;
+      if (li == 0) {
+        bulk_load(base + L.stage_bytes, src + static_cast<size_t>(nxt) * row_bytes, row_bytes,
+                  &bars[1]);
+        clc_request(clc_resp, clc_bar);
+      }
+    }
   }
 
   // The loop is uniform over the warp: the segments of a warp process rows
@@ -314,8 +350,8 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   float spec_t = 0.0f;
   uint32_t phase = 0;
   for (int it = 0;; ++it) {
-    const int row = row0 + it * nsegs;
-    const bool active = row < T;
+    const int row = steal ? cur : row0 + it * nsegs;
+    const bool active = row >= 0 && row < T;
     if (!__any_sync(0xffffffffu, active)) break;
     const int b = it & 1;
     bool ok = true;
@@ -325,7 +361,9 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       // record the failure, let the other stage's copy (if any) land, leave
       if (active && li == 0) {
         atomicExch(status, kDeviceWaitTimeout);
-        if (row + nsegs < T) mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
+        if (steal ? nxt >= 0 : row + nsegs < T)
+          mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
+        if (pending) mbar_wait_bounded(clc_bar, clc_phase);
       }
       __syncwarp();
       if constexpr (OP == 3) {  // the block meets once more below
@@ -809,7 +847,25 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
     fence_proxy_async_smem();
     __syncwarp(0xffffffffu);
-    if (li == 0) {
+    if (steal) {
+      // the row after next: the one the request in flight took, if any
+      int nn = -1;
+      if (pending) {
+        const bool got = mbar_wait_bounded(clc_bar, clc_phase);
+        clc_phase ^= 1u;
+        if (got) nn = clc_cancelled_x(clc_resp);
+        else if (li == 0) atomicExch(status, kDeviceWaitTimeout);
+        fence_proxy_async_smem();  // every lane has read the response
+        __syncwarp();
+        pending = nn >= 0;
+        if (li == 0 && pending) {
+          bulk_load(stage, src + static_cast<size_t>(nn) * row_bytes, row_bytes, &bars[b]);
+          clc_request(clc_resp, clc_bar);
+        }
+      }
+      cur = nxt;
+      nxt = nn;
+    } else if (li == 0) {
       const int nr = row + 2 * nsegs;
       if (nr < T) bulk_load(stage, src + static_cast<size_t>(nr) * row_bytes, row_bytes, &bars[b]);
     }

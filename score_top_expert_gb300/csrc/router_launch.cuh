@@ -144,6 +144,8 @@ struct StagedPlan {
   int km;          // key mode: 0 logits, 1 s + bias (and groups), top-K only
   bool full;       // E == 4 * seg * nc: no padding chunks
   int tail_bytes;  // after the slices: the block's expert maps (op 3)
+  int steal_blocks;  // resident one-warp blocks of the stealing launch (0: none);
+                     // batches of more rows than that launch it
 };
 
 // compiled (SEG, NC) pairs of the staged forward
@@ -159,6 +161,16 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
   static std::atomic<int> granted[kSmemDevs];  // this kernel's record
   const cudaError_t se = allow_smem(kern, smem, granted);
   if (se != cudaSuccess) return se;
+  if constexpr (SEG == 32 && KM == 0 && OP <= 2) {
+    // more rows than resident warps: one one-warp block per row, the warps
+    // taking over the rows of blocks not yet started
+    if (p.steal_blocks > 0 && a.T > p.steal_blocks) {
+      StagedLayout L = p.layout;
+      L.steal = 1;
+      return launch_kernel(kern, dim3(static_cast<unsigned>(a.T)), dim3(32),
+                           static_cast<size_t>(L.head_bytes) + L.seg_bytes, st, a, L, status);
+    }
+  }
   // Rows go round-robin over all resident segments.  When they take more
   // than one round, use the fewest blocks that still need the same number of
   // rounds, so that every segment carries the same number of rows (no

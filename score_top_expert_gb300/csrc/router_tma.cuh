@@ -81,4 +81,36 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster launch control (sm_100 family): a running block asks to cancel the
+// launch of a block of its grid that has not started yet and, when that
+// succeeds, does that block's work itself.  The 16-byte response lands in
+// shared memory (16-byte aligned) and completes `bytes` on an mbarrier, like
+// a bulk copy.  Once a request has failed (no block left to cancel) the block
+// makes no further requests.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void clc_request(void* response, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;"
+               ::"r"(smem_addr(bar)) : "memory");
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_addr(response)), "r"(smem_addr(bar)) : "memory");
+}
+
+// The x index of the block a completed request cancelled, or -1 if it
+// cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(const void* response) {
+  int x = -1, ok = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "+r"(x), "=r"(ok)
+      : "r"(smem_addr(response))
+      : "memory");
+  return ok ? x : -1;
+}
+
 }  // namespace moe_router
