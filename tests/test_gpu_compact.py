@@ -171,6 +171,29 @@ def test_register_compact_rows_in_sequence(R, E, K, ng, gk, dt):
     assert R.device_status() == 0
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_staged_compact_rows_taken_over(R, dt):
+    # compact outputs from the staged forward's one-warp blocks that take over
+    # the rows of blocks not yet started (more rows than resident warps)
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    E, K, T = 2304, 36, 6000
+    rng = np.random.default_rng(23)
+    x = np.empty((T, E), dtype=np.float32)
+    for i in range(T):
+        kind = i % 3
+        x[i] = (rng.normal(0, 1, E) if kind == 0 else rng.normal(0, 3, E) if kind == 1
+                else rng.integers(-3, 4, E))
+    case = make_case(T, E, K, dtype=dt, seed=8)
+    case.logits = x if dt == "f32" else round_to_bf16_values(x)
+    prev = R.force_path("staged")
+    try:
+        for sf in ("softmax", "sigmoid", "softmax_post"):
+            check_compact(R, case, K, sf, c=1.5)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
+
+
 def test_compact_ties(R, path):
     # integer logits: heavy exact ties inside and at the boundary of the top-K
     rng = np.random.default_rng(9)

@@ -414,16 +414,11 @@ def test_adversarial_rows(R, path, E, K):
                 run_and_check_aux(R, case, K, sf)
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("E,K", [(256, 8), (512, 22), (512, 36), (384, 30)])
-def test_register_rows_in_sequence(R, E, K, dt):
-    # many rows per warp, so that each row starts from the previous row's
-    # threshold estimate: a mix of row kinds in a fixed cycle (normal, wide,
-    # integer-valued with heavy ties, adversarial, shifted and sorted rows), so the
-    # estimate fails and recovers over and over
-    from score_top_expert_gb300.workloads import round_to_bf16_values
-    rng = np.random.default_rng(E * 31 + K)
-    T = 12000
+def mixed_rows(T, E, K, seed):
+    # a mix of row kinds in a fixed cycle (normal, wide, integer-valued with heavy
+    # ties, adversarial, shifted and sorted rows), so that a threshold carried over
+    # from a warp's previous row fails and recovers over and over
+    rng = np.random.default_rng(seed)
     adv = adversarial_rows(E, K, rng)
     x = np.empty((T, E), dtype=np.float32)
     for i in range(T):
@@ -440,6 +435,17 @@ def test_register_rows_in_sequence(R, E, K, dt):
             x[i] = rng.normal(0, 1, E) + 10.0  # shifted (sigmoid keys stay distinct in f64)
         else:
             x[i] = np.sort(rng.normal(0, 1, E))
+    return x
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E,K", [(256, 8), (512, 22), (512, 36), (384, 30)])
+def test_register_rows_in_sequence(R, E, K, dt):
+    # many rows per warp, so that each row starts from the previous row's
+    # threshold estimate
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    T = 12000
+    x = mixed_rows(T, E, K, E * 31 + K)
     prev = R.force_path("register")
     try:
         case = make_case(T, E, K, dtype=dt, seed=5)
@@ -447,6 +453,29 @@ def test_register_rows_in_sequence(R, E, K, dt):
         for sf in ("softmax", "sigmoid"):
             run_and_check_topk(R, case, K, sf, c=2.5, check_bwd=False)
             run_and_check_aux(R, case, K, sf)
+    finally:
+        R.force_path(prev)
+    assert R.device_status() == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("E,K", [(1024, 30), (2304, 36)])
+def test_staged_rows_taken_over(R, E, K, dt):
+    # more rows than resident warps: the staged forward launches one one-warp
+    # block per row, and running warps take over the rows of blocks that have
+    # not started, so the rows a warp sees (and the threshold it carries from
+    # one to the next) follow no fixed stride
+    from score_top_expert_gb300.workloads import round_to_bf16_values
+    T = 6000
+    x = mixed_rows(T, E, K, E * 17 + K)
+    prev = R.force_path("staged")
+    try:
+        case = make_case(T, E, K, dtype=dt, seed=6)
+        case.logits = x if dt == "f32" else round_to_bf16_values(x)
+        for sf in ("softmax", "sigmoid", "softmax_post"):
+            run_and_check_topk(R, case, K, sf, c=2.5, check_bwd=False)
+            if sf != "softmax_post":
+                run_and_check_aux(R, case, K, sf)
     finally:
         R.force_path(prev)
     assert R.device_status() == 0
