@@ -19,7 +19,11 @@
  *   with a workspace say what they enqueue) and returns.  Kernels are
  *   launched with programmatic dependent launch (each waits for the previous
  *   kernel in the stream before touching memory; MOE_ROUTER_PDL=0 disables
- *   it).
+ *   it).  Above 512 experts, a forward with more rows than the GPU holds
+ *   warps at once launches one one-warp block per row whose running warps
+ *   take over the rows of blocks not yet started (cluster launch control);
+ *   the results are those of the persistent launch, bit for bit
+ *   (MOE_ROUTER_STEAL=0 keeps the persistent launch).
  * - `dtype` is the type of the logits and of the tensors that follow it
  *   (probs, grad_probs, grad_logits): MR_F32 (float) or MR_BF16
  *   (__nv_bfloat16).  Scores, intermediates, grad_scores and the expert bias
