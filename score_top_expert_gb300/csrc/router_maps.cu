@@ -211,7 +211,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int g
   return *verdict != 0;
 }
 
-__global__ void __launch_bounds__(kMapsThreads)
+__global__ void __launch_bounds__(kMapsThreads, 3)
 maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, int K,
                   int* __restrict__ counts, int* __restrict__ totals,
                   unsigned int* __restrict__ barrier, int* __restrict__ status,
@@ -225,8 +225,23 @@ maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, i
   int* tmp = verdict + 4;  // scan slots / per-warp prefix sums (8 x 32 ints)
   const int nb = gridDim.x;
 
-  // ---- 1: this tile's masks and counts -------------------------------------
-  build_masks(idx, ld, T, E, K, masks);
+  // ---- 1: this tile's choices (kept in registers for the scatter), masks
+  //      and counts (the choice loads overlap the zeroing of the masks) ------
+  const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
+  const int t = blockIdx.x * kMapsTile + tl;
+  int ch[kMapsPerThread];
+  if (t < T) {
+    load_choices(idx, ld, t, K, slot, ch);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMapsPerThread; ++j) ch[j] = -1;
+  }
+  for (int e = threadIdx.x; e < E; e += kMapsThreads) masks[e] = 0ull;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kMapsPerThread; ++j)
+    if (ch[j] >= 0 && ch[j] < E) atomicOr(&masks[ch[j]], 1ull << tl);
+  __syncthreads();
   for (int e = threadIdx.x; e < E; e += kMapsThreads)
     counts[static_cast<size_t>(blockIdx.x) * E + e] = __popcll(masks[e]);
   if (!grid_barrier(barrier, 1u, status, verdict)) return;
@@ -284,30 +299,24 @@ maps_fused_kernel(const int32_t* __restrict__ idx, long long ld, int T, int E, i
   const int total = block_exclusive_scan(off, E, tmp);
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e <= E; e += kMapsThreads) offsets[e] = e < E ? off[e] : total;
-  const int tl = threadIdx.x & (kMapsTile - 1), slot = threadIdx.x / kMapsTile;
-  const int t = blockIdx.x * kMapsTile + tl;
-  if (t >= T) return;
+  // each expert's first row for this tile: its offset plus the earlier tiles'
+  // choices (the same thread reads off[e] above and updates it here)
   const int* base = counts + static_cast<size_t>(blockIdx.x) * E;
+  for (int e = threadIdx.x; e < E; e += kMapsThreads) off[e] += __ldcg(base + e);
+  __syncthreads();
+  if (t >= T) return;
   const unsigned long long below = (1ull << tl) - 1ull;
-  int ch[kMapsPerThread];
-  load_choices(idx, ld, t, K, slot, ch);
-  int pos[kMapsPerThread];
-#pragma unroll
-  for (int j = 0; j < kMapsPerThread; ++j) {
-    const int e = ch[j];
-    pos[j] = (e >= 0 && e < E) ? off[e] + __ldcg(base + e) : -1;
-  }
 #pragma unroll
   for (int j = 0; j < kMapsPerThread; ++j) {
     const int k = slot + j * kMapsSlots;
     if (k >= K) break;
     const int e = ch[j];
     const int u = t + k * T;
-    if (pos[j] < 0) {
+    if (e < 0 || e >= E) {
       u2p[u] = -1;
       continue;
     }
-    const int p = pos[j] + __popcll(masks[e] & below);
+    const int p = off[e] + __popcll(masks[e] & below);
     p2u[p] = u;
     u2p[u] = p;
     pexp[p] = e;
