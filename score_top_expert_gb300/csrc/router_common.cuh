@@ -25,10 +25,6 @@ namespace moe_router {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Kernel entry: wait for the previous kernel only.  The next kernel is let
 // in as this one's blocks exit (no early trigger: a persistent kernel's
 // dependents would otherwise sit resident beside it).
