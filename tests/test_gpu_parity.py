@@ -459,7 +459,7 @@ def test_register_rows_in_sequence(R, E, K, dt):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("E,K", [(1024, 30), (2304, 36)])
+@pytest.mark.parametrize("E,K", [(1024, 30), (2304, 36), (1000, 24), (2000, 36)])
 def test_staged_rows_taken_over(R, E, K, dt):
     # more rows than resident warps: the staged forward launches one one-warp
     # block per row, and running warps take over the rows of blocks that have
