@@ -4,13 +4,14 @@
 // Forward: one launch, deterministic (fixed summation orders, compensated
 // fp32 sums, no floating-point atomics).  The grid is B row ranges x G
 // column groups of 128 experts (32 with scalar rows), B chosen so that the
-// grid is about four blocks on each SM (at most 64 ranges):
+// grid is one wave of three blocks on each SM (at most 64 ranges):
 //   1  block (b, g): lane l owns the four experts of chunk 32 g + l, warp w
 //      the rows w, w + 8, ... of range b (eight rows' loads in flight); the
 //      8 warps combine in order and the block writes its partial row;
-//   2  the last block of group g to finish (a counter per group) adds the B
-//      partial rows of its experts (all of a warp's rows loaded at once),
-//      writes tokens_per_expert and the group's share of
+//   2  the last block of group g to finish (a counter per group, arrived on
+//      with one acquire-release atomic) adds the B partial rows of its
+//      experts (all of a warp's rows loaded at once), writes
+//      tokens_per_expert and the group's share of
 //        loss = coeff E / (K T^2) * sum_e (sum_t q_te) * tokens_e;
 //   3  the last group to finish adds the shares in group order.
 // The counters are zeroed by a one-block kernel on the stream before the
