@@ -15,8 +15,9 @@
 // When every tile's block fits on the GPU at once, the three phases run as
 // one cooperative launch instead (after a one-block kernel that zeroes the
 // barrier's counter), separated by a grid barrier (bounded in time like
-// every wait of this library), and the scatter reuses the masks of phase 1
-// from shared memory.
+// every wait of this library); the scatter reuses the masks of phase 1 from
+// shared memory and each thread's choices from its registers, and adds the
+// tile's column prefixes to the offsets in shared memory once per block.
 #include <climits>
 #include <cstddef>
 #include <cstdint>
