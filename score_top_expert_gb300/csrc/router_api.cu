@@ -139,6 +139,8 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km, int op) {
     L.sorted_off = off;
     off += MR_MAX_TOPK * 8;
   }
+  L.sel_off = off;  // renormalising top-K: the K selected scores by rank
+  off += MR_MAX_TOPK * 4;
   L.bar_off = round_up(off, 16);
   off = L.bar_off + 48;
   L.seg_bytes = round_up(off, 128);

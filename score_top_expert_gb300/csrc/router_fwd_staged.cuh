@@ -72,6 +72,7 @@ struct StagedLayout {
   int stage_bytes;  // SEG * NC chunks of 4 logits
   int cand_off;     // kCandPerLane * SEG packed candidate words
   int sorted_off;   // OP 2, 3: the K selected words by rank (MR_MAX_TOPK words)
+  int sel_off;      // the K selected scores by rank (MR_MAX_TOPK floats)
   int mask_off;     // selection words, one bit per expert of the padded row
   int bar_off;      // two mbarriers, one 32-bit slot, and for stealing launches
                     // a third mbarrier (at +24) and a 16-byte response (at +32)
@@ -178,7 +179,9 @@ __device__ __forceinline__ void compact_marked(const unsigned char* stage, const
 // Rank of each owned candidate among all `total` candidates (NOWN per lane):
 // the K best set their selection bits (and, with SORTED, take their place in
 // sorted[rank]); the one ranked `target` publishes its key as the next row's
-// threshold; sigmoid rows sum their selected scores.
+// threshold.  With SIG (top-K renormalised over the selected), each selected
+// candidate's score goes to sel_scores[rank], so that the row sums them in
+// rank order whatever the candidates' layout.
 // With TRY32 (fp32 rows, where equal logits are rare) the rank first counts
 // the candidates with a larger 32-bit key (one compare per pair); when keys
 // repeat, the ranks of the tied candidates coincide and no longer sum to
@@ -187,7 +190,7 @@ __device__ __forceinline__ void compact_marked(const unsigned char* stage, const
 template <int SEG, int NOWN, bool SIG, bool TRY32, bool SORTED, class ScoreOf>
 __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, int total,
                                                 int li, int K, int target, uint32_t* selmask,
-                                                uint32_t* next_key, float& part,
+                                                uint32_t* next_key, float* sel_scores,
                                                 const ScoreOf& score_of,
                                                 unsigned long long* sorted) {
   const uint32_t* hi_words = reinterpret_cast<const uint32_t*>(cand) + 1;  // keys
@@ -226,7 +229,8 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
         const uint32_t idx = ~static_cast<uint32_t>(own[r]);
         atomicOr(&selmask[idx >> 5], 1u << (idx & 31));
         if constexpr (SORTED) sorted[rank[r]] = own[r];
-        if constexpr (SIG) part += score_of(static_cast<int>(idx), static_cast<uint32_t>(own[r] >> 32));
+        if constexpr (SIG)
+          sel_scores[rank[r]] = score_of(static_cast<int>(idx), static_cast<uint32_t>(own[r] >> 32));
       }
       if (rank[r] == target) *next_key = static_cast<uint32_t>(own[r] >> 32);
     }
@@ -268,6 +272,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   uint32_t* selmask = reinterpret_cast<uint32_t*>(base + L.mask_off);
   unsigned long long* sorted_sel =
       reinterpret_cast<unsigned long long*>(base + L.sorted_off);  // OP 2, 3
+  float* sel_scores = reinterpret_cast<float*>(base + L.sel_off);  // renormalising top-K
 
   const int E = a.E, K = a.K, T = a.T;
   const int nchunks = E >> 2;
@@ -664,14 +669,17 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       const int nown = (total + SEG - 1) / SEG;
       const int tgt = target < total - 1 ? target : total - 1;
       if (nown <= 1)
-        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
+        rank_candidates<SEG, 1, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, sel_scores, score_of, sorted_sel);
       else if (nown == 2)
-        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
+        rank_candidates<SEG, 2, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, sel_scores, score_of, sorted_sel);
       else if (nown == 3)
-        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
+        rank_candidates<SEG, 3, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, sel_scores, score_of, sorted_sel);
       else
-        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, part, score_of, sorted_sel);
+        rank_candidates<SEG, 4, kSigTopk, DT == DT_F32, (OP >= 2)>(cand, total, li, K, tgt, selmask, next_key, sel_scores, score_of, sorted_sel);
       __syncwarp(smask);
+      if constexpr (kSigTopk) {  // the selected scores in rank order
+        for (int r = li; r < K; r += SEG) part += sel_scores[r];
+      }
       spec_t = key_to_float(*next_key);
       have_spec = true;
       sorted_row = true;
