@@ -22,7 +22,9 @@
  *   it).  Above 512 experts, a forward with more rows than the GPU holds
  *   warps at once launches one one-warp block per row whose running warps
  *   take over the rows of blocks not yet started (cluster launch control);
- *   the results are those of the persistent launch, bit for bit
+ *   a compact forward of fp32 rows above 1024 experts with no dense output
+ *   keeps one row buffer per warp instead of two in that launch.  The
+ *   results are those of the persistent launch, bit for bit
  *   (MOE_ROUTER_STEAL=0 keeps the persistent launch).
  * - `dtype` is the type of the logits and of the tensors that follow it
  *   (probs, grad_probs, grad_logits): MR_F32 (float) or MR_BF16

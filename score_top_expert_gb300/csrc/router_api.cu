@@ -119,12 +119,12 @@ void staged_shape(int E, int /*K*/, int* seg, int* nc) {
   *nc = E <= 256 ? 2 : (E <= 512 ? 4 : (E <= 1024 ? 8 : 18));
 }
 
-StagedLayout staged_layout(int seg, int nc, int dt, int km, int op) {
+StagedLayout staged_layout(int seg, int nc, int dt, int km, int op, int stages) {
   StagedLayout L{};
   const int d = dt == MR_F32 ? 4 : 2;
   L.head_bytes = km == 1 ? round_up(4 * seg * nc * 4, 128) : 0;  // the bias row
   L.stage_bytes = 4 * seg * nc * d;  // seg * nc chunks of four logits
-  int off = 2 * L.stage_bytes;
+  int off = stages * L.stage_bytes;
   if (km == 1) {
     L.work_off = off;
     off += 4 * seg * nc * 4;  // keys
@@ -145,6 +145,7 @@ StagedLayout staged_layout(int seg, int nc, int dt, int km, int op) {
   off = L.bar_off + 48;
   L.seg_bytes = round_up(off, 128);
   L.steal = 0;
+  L.one_stage = stages == 1 ? 1 : 0;
   return L;
 }
 
@@ -197,7 +198,7 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
   StagedPlan p{};
   staged_shape(E, K, &p.seg, &p.nc);
   p.full = E == 4 * p.seg * p.nc;
-  p.layout = staged_layout(p.seg, p.nc, dt, km, op);
+  p.layout = staged_layout(p.seg, p.nc, dt, km, op, 2);
   p.op = op;
   p.km = km;
   p.tail_bytes = op == 3 ? (2 * E + 16) * 4 : 0;  // the block's expert maps
@@ -241,6 +242,23 @@ bool staged_plan(const DeviceInfo& di, int sf, int dt, int op, int km, int E, in
     int per_sm = occupancy_any(sf, dt, one);
     if (per_sm > cap_warps) per_sm = cap_warps;
     p.steal_blocks = per_sm * di.sms;
+  }
+  // compact-only outputs of 18-chunk rows take one stage per warp (refilled
+  // once the row's candidates and sum are taken) when that keeps more warps
+  // resident: at 8192x2304, K = 36, fp32, 17 warps per SM instead of 11 and
+  // 22.9 against 27.6 us.  At 512 experts it measured slower (12.9 against
+  // 12.1 us): there the second stage's prefetch is worth more.
+  p.steal_blocks1 = 0;
+  if (p.steal_blocks > 0 && op == 2 && p.nc == 18) {
+    StagedPlan one = p;
+    one.layout = staged_layout(p.seg, p.nc, dt, km, op, 1);
+    one.warps_per_block = 1;
+    int per_sm = occupancy_any(sf, dt, one);
+    if (per_sm > cap_warps) per_sm = cap_warps;
+    if (per_sm * di.sms > p.steal_blocks) {
+      p.layout1 = one.layout;
+      p.steal_blocks1 = per_sm * di.sms;
+    }
   }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_nplans < kPlanCache)

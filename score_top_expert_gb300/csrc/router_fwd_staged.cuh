@@ -11,7 +11,12 @@
 // instead one one-warp block per row; a running warp takes over the rows of
 // blocks that have not started yet (cluster launch control), one request
 // ahead, so the rows go to whichever warps finish first and the batch's
-// tail stays short.
+// tail stays short.  When such a launch writes compact outputs only, a warp
+// may keep one stage instead of two: the row's logits are last needed for
+// its candidates and its row sum, so the stage is refilled with the next
+// row right then, and that copy lands while the candidates are ranked and
+// the K outputs written (each selected logit is read back from its packed
+// key).  Fewer bytes per warp keep more warps resident.
 //
 // Per row (lane l of the segment holds chunks c = l + SEG j, four consecutive
 // experts each):
@@ -79,6 +84,8 @@ struct StagedLayout {
   int seg_bytes;    // slice size, multiple of 128
   int steal;        // 1: one-warp blocks, one row each, that take over the rows
                     // of blocks not yet started (cluster launch control)
+  int one_stage;    // 1 (stealing launches of compact-only outputs): one stage,
+                    // refilled as soon as the row's candidates and sum are taken
 };
 
 constexpr int kStagedMaxWarps = 12;
@@ -237,13 +244,19 @@ __device__ __forceinline__ void rank_candidates(const unsigned long long* cand, 
   }
 }
 
-// Registers of the 18-chunk bf16 logit-keyed kernels are capped so that they keep 16
-// warps per SM (their shared memory would allow 21; uncapped they need 160).
-template <int DT, int NC, int KM>
-constexpr int staged_max_regs() { return (DT == DT_BF16 && NC == 18 && KM == 0) ? 128 : 168; }
+// Registers of the 18-chunk logit-keyed kernels are capped: bf16 at 128, so that they
+// keep 16 warps per SM (their shared memory would allow 21; uncapped they need 160);
+// the fp32 compact kernel at 120, so that its one-stage launch keeps 17 (it uses 114;
+// uncapped, 168).
+template <int DT, int NC, int KM, int OP>
+constexpr int staged_max_regs() {
+  if (NC == 18 && KM == 0 && DT == DT_BF16) return 128;
+  if (NC == 18 && KM == 0 && OP == 2) return 120;
+  return 168;
+}
 
 template <int SF, int DT, int SEG, int NC, int OP, bool FULL, int KM>
-__global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC, KM>()))
+__global__ void __launch_bounds__(kStagedMaxWarps * 32) __maxnreg__((staged_max_regs<DT, NC, KM, OP>()))
 router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   pdl_enter();
   constexpr int CAP = kCandPerLane * SEG;
@@ -308,6 +321,8 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   // request in flight, so rows go to whichever warps finish first.
   constexpr bool kCanSteal = SEG == 32 && KM == 0 && OP <= 2;
   const bool steal = kCanSteal && L.steal != 0;
+  constexpr bool kCanOne = kCanSteal && OP == 2 && NC == 18;  // as the host launches it
+  const bool one = kCanOne && steal && L.one_stage != 0;
   uint64_t* clc_bar = bars + 3;
   unsigned char* clc_resp = reinterpret_cast<unsigned char*>(bars) + 32;
   uint32_t clc_phase = 0;
@@ -323,14 +338,16 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
   if (li == 0) {
     if (row0 < T)
       bulk_load(base, src + static_cast<size_t>(row0) * row_bytes, row_bytes, &bars[0]);
-    if (row0 + nsegs < T)
+    if (!one && row0 + nsegs < T)
       bulk_load(base + L.stage_bytes, src + static_cast<size_t>(row0 + nsegs) * row_bytes,
                 row_bytes, &bars[1]);
     if (steal && row0 < T) clc_request(clc_resp, clc_bar);
   }
   int cur = row0, nxt = -1;  // stealing: this row and the next (-1: none)
   bool pending = false;      // stealing: a request is in flight
-  if (steal && row0 < T) {
+  if (one) {
+    pending = row0 < T;  // answered when the first row releases the stage
+  } else if (steal && row0 < T) {
     const bool got = mbar_wait_bounded(clc_bar, clc_phase);
     clc_phase ^= 1u;
     if (got) nxt = clc_cancelled_x(clc_resp);
@@ -347,6 +364,27 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
   }
 
+  // One-stage launches: the row the request in flight took over (if any) goes
+  // into the stage just released, and the next request is made; returns
+  // that row, or -1.
+  auto refill_one = [&](unsigned char* stage) -> int {
+    int nn = -1;
+    if (pending) {
+      const bool got = mbar_wait_bounded(clc_bar, clc_phase);
+      clc_phase ^= 1u;
+      if (got) nn = clc_cancelled_x(clc_resp);
+      else if (li == 0) atomicExch(status, kDeviceWaitTimeout);
+      pending = nn >= 0;
+    }
+    fence_proxy_async_smem();  // every lane's reads of the stage and the response
+    __syncwarp();
+    if (li == 0 && nn >= 0) {
+      bulk_load(stage, src + static_cast<size_t>(nn) * row_bytes, row_bytes, &bars[0]);
+      clc_request(clc_resp, clc_bar);
+    }
+    return nn;
+  };
+
   // The loop is uniform over the warp: the segments of a warp process rows
   // in step and meet at full-warp barriers after the copy wait and after the
   // selection, so that their paths reconverge.
@@ -358,7 +396,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     const int row = steal ? cur : row0 + it * nsegs;
     const bool active = row >= 0 && row < T;
     if (!__any_sync(0xffffffffu, active)) break;
-    const int b = it & 1;
+    const int b = one ? 0 : (it & 1);
     bool ok = true;
     if (active) ok = mbar_wait_bounded(&bars[b], (phase >> b) & 1u);
     ok = __all_sync(0xffffffffu, ok);
@@ -366,7 +404,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       // record the failure, let the other stage's copy (if any) land, leave
       if (active && li == 0) {
         atomicExch(status, kDeviceWaitTimeout);
-        if (steal ? nxt >= 0 : row + nsegs < T)
+        if (!one && (steal ? nxt >= 0 : row + nsegs < T))
           mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u);
         if (pending) mbar_wait_bounded(clc_bar, clc_phase);
       }
@@ -588,6 +626,34 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       cand_ok = total <= CAP;
     }
 
+    // ---- 4 (as a step): scores e = exp(x - max) or s, their row sum -----------------
+    const float max_l2e = KM == 1 ? xmax_l2e : row_max * kLog2e;
+    float inv = xinv;
+    auto score_pass = [&]() {
+      if constexpr (kNeedSum || kStore) {
+        float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          float x[4], s[4];
+          load_x(stage, j, x);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if constexpr (SF != SF_SIGMOID) s[u] = exp_shifted(x[u], max_l2e);
+            else s[u] = sigmoid_f32(x[u]);
+          }
+          if constexpr (kNeedSum) {
+            const float add = (s[0] + s[1]) + (s[2] + s[3]);
+            if (j & 1) sum1 += add; else sum0 += add;
+          }
+          if constexpr (kStore)
+            sts_f4(stage + 16 * (li + SEG * j), make_float4(s[0], s[1], s[2], s[3]));
+        }
+        if constexpr (kNeedSum) inv = 1.0f / seg_sum<SEG>(sum0 + sum1);
+      }
+    };
+    bool released = false;  // one-stage: the stage holds the next row already
+    int next_one = -1;      // one-stage: that row
+
     // ---- 3: exact selection ----------------------------------------------------------
     float part = 0.0f;  // sum of the selected scores (sigmoid top-K)
     bool tie_row = false;
@@ -666,6 +732,13 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       compact_marked<KDT, SEG, NC>(KM == 1 ? reinterpret_cast<const unsigned char*>(work) : stage,
                                    cm, seg_exclusive_scan<SEG>(cnt), li, cand);
       __syncwarp(smask);
+      if constexpr (kCanOne) {
+        if (one) {  // the stage's last use is the row sum: take it now, refill
+          score_pass();
+          next_one = refill_one(stage);
+          released = true;
+        }
+      }
       const int nown = (total + SEG - 1) / SEG;
       const int tgt = target < total - 1 ? target : total - 1;
       if (nown <= 1)
@@ -730,28 +803,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     __syncwarp(0xffffffffu);  // reconverge the segments of the warp
 
     // ---- 4: scores ----------------------------------------------------------------------
-    const float max_l2e = KM == 1 ? xmax_l2e : row_max * kLog2e;
-    float inv = xinv;
-    if constexpr (kNeedSum || kStore) {
-      float sum0 = 0.0f, sum1 = 0.0f;
-#pragma unroll
-      for (int j = 0; j < NC; ++j) {
-        float x[4], s[4];
-        load_x(stage, j, x);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if constexpr (SF != SF_SIGMOID) s[u] = exp_shifted(x[u], max_l2e);
-          else s[u] = sigmoid_f32(x[u]);
-        }
-        if constexpr (kNeedSum) {
-          const float add = (s[0] + s[1]) + (s[2] + s[3]);
-          if (j & 1) sum1 += add; else sum0 += add;
-        }
-        if constexpr (kStore)
-          sts_f4(stage + 16 * (li + SEG * j), make_float4(s[0], s[1], s[2], s[3]));
-      }
-      if constexpr (kNeedSum) inv = 1.0f / seg_sum<SEG>(sum0 + sum1);
-    }
+    if (!released) score_pass();
     float pf = a.scaling;
     if constexpr (kSigTopk) pf = a.scaling / seg_sum<SEG>(part);
     else if constexpr (SF == SF_SOFTMAX && OP != 1) pf = a.scaling * inv;
@@ -769,7 +821,9 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
           if (k < K) {
             const unsigned long long w = sorted_sel[k];
             const int idx = static_cast<int>(~static_cast<uint32_t>(w));
-            const float x = stage_x1<DT>(stage, idx);
+            // the logit itself: its ordered key (logit keys), else the stage
+            const float x = KM == 0 ? key_to_float(static_cast<uint32_t>(w >> 32))
+                                    : stage_x1<DT>(stage, idx);
             const float wt = (SF != SF_SIGMOID) ? exp_shifted(x, max_l2e) : sigmoid_f32(x);
             a.topk_w[t * a.ld_w + k] = wt * pf;
             a.topk_i[t * a.ld_i + k] = idx;
@@ -807,7 +861,7 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
       __syncwarp(smask);
       write_compact_row<SEG>(a, row, li, cand, cand_p);
       }
-      dense = a.map != nullptr || a.probs != nullptr || a.scores != nullptr;
+      dense = !released && (a.map != nullptr || a.probs != nullptr || a.scores != nullptr);
     }
 
     // ---- 5: outputs -----------------------------------------------------------------------
@@ -855,7 +909,10 @@ router_fwd_staged_kernel(const FwdArgs a, const StagedLayout L, int* status) {
     }
     fence_proxy_async_smem();
     __syncwarp(0xffffffffu);
-    if (steal) {
+    if (one) {
+      if (!released) next_one = refill_one(stage);
+      cur = next_one;
+    } else if (steal) {
       // the row after next: the one the request in flight took, if any
       int nn = -1;
       if (pending) {

@@ -146,6 +146,9 @@ struct StagedPlan {
   int tail_bytes;  // after the slices: the block's expert maps (op 3)
   int steal_blocks;  // resident one-warp blocks of the stealing launch (0: none);
                      // batches of more rows than that launch it
+  StagedLayout layout1;  // compact-only outputs: the one-stage slice
+  int steal_blocks1;     // resident one-stage blocks (0: not used); compact-only
+                         // batches of more rows than that launch them
 };
 
 // compiled (SEG, NC) pairs of the staged forward
@@ -164,6 +167,15 @@ cudaError_t launch_staged_inst(const FwdArgs& a, const StagedPlan& p, int* statu
   if constexpr (SEG == 32 && KM == 0 && OP <= 2) {
     // more rows than resident warps: one one-warp block per row, the warps
     // taking over the rows of blocks not yet started
+    if constexpr (OP == 2) {
+      const bool compact_only = a.map == nullptr && a.probs == nullptr && a.scores == nullptr;
+      if (compact_only && p.steal_blocks1 > 0 && a.T > p.steal_blocks1) {
+        StagedLayout L = p.layout1;
+        L.steal = 1;
+        return launch_kernel(kern, dim3(static_cast<unsigned>(a.T)), dim3(32),
+                             static_cast<size_t>(L.head_bytes) + L.seg_bytes, st, a, L, status);
+      }
+    }
     if (p.steal_blocks > 0 && a.T > p.steal_blocks) {
       StagedLayout L = p.layout;
       L.steal = 1;

@@ -187,8 +187,25 @@ def test_staged_compact_rows_taken_over(R, dt):
     case.logits = x if dt == "f32" else round_to_bf16_values(x)
     prev = R.force_path("staged")
     try:
+        xd = to_dev(case.logits, dt)
         for sf in ("softmax", "sigmoid", "softmax_post"):
             check_compact(R, case, K, sf, c=1.5)
+            # without dense outputs (fp32 rows of this width: one stage per
+            # warp, refilled before the ranking): the same compact rows, for
+            # batches above and below that launch's row threshold
+            for t in (T, 3000, 2000):
+                full = R.router_topk_fwd_compact(xd[:t], K, sf, scaling_factor=1.5, dense=True)
+                only = R.router_topk_fwd_compact(xd[:t], K, sf, scaling_factor=1.5)
+                assert only[3] is None and only[4] is None and only[5] is None
+                for a, b in zip(full[:3], only[:3]):
+                    assert torch.equal(a, b)
+        # rows that do not fill the chunk grid (2000 of 2304 slots)
+        xp = xd[:, :2000].contiguous()
+        for sf in ("softmax", "sigmoid"):
+            full = R.router_topk_fwd_compact(xp, K, sf, scaling_factor=1.5, dense=True)
+            only = R.router_topk_fwd_compact(xp, K, sf, scaling_factor=1.5)
+            for a, b in zip(full[:3], only[:3]):
+                assert torch.equal(a, b)
     finally:
         R.force_path(prev)
     assert R.device_status() == 0
