@@ -82,6 +82,14 @@ def check_compact(R, case, K, sf, c=1.0, ng=0, gk=0, bias=None, strided=False):
                 + torch.arange(T, device=DEV)[:, None]).to(torch.int32)
     assert torch.equal(tei, want_tei)
 
+    return compare_with_oracle(case, K, sf, c, ng, gk, bias, idx, w)
+
+
+def compare_with_oracle(case, K, sf, c, ng, gk, bias, idx, w):
+    """Compact indices and weights against the oracle: the selected sets
+    equal outside near ties, the rank order by key, the weights within the
+    fp32 bound; returns the number of rows whose selected set differs."""
+    T = case.logits.shape[0]
     ref = O.topk_fwd_compact(case.logits, K, sf, ng, gk, c, bias)
     gi = idx.cpu().numpy().astype(np.int64)
     gw = w.cpu().numpy().astype(np.float64)
@@ -208,6 +216,24 @@ def test_staged_compact_rows_taken_over(R, dt):
                 assert torch.equal(a, b)
     finally:
         R.force_path(prev)
+    assert R.device_status() == 0
+
+
+@pytest.mark.parametrize("sf", ["softmax", "sigmoid"])
+def test_unaligned_compact_rows(R, sf):
+    # logits 4 bytes past a 16-byte boundary: no bulk copy can take the rows,
+    # which a batch this size would otherwise send to the one-stage launch
+    E, K, T = 2304, 36, 3000
+    case = make_case(T, E, K, seed=31)
+    buf = torch.zeros(T * E + 1, device=DEV)
+    x = buf[1:].view(T, E)
+    x.copy_(to_dev(case.logits))
+    assert x.data_ptr() % 16 != 0
+    w, idx, tei, *_ = R.router_topk_fwd_compact(x, K, sf, scaling_factor=1.5)
+    assert compare_with_oracle(case, K, sf, 1.5, 0, 0, None, idx, w) == 0
+    want_tei = (torch.arange(K, device=DEV)[None, :] * T
+                + torch.arange(T, device=DEV)[:, None]).to(torch.int32)
+    assert torch.equal(tei, want_tei)
     assert R.device_status() == 0
 
 
