@@ -203,9 +203,14 @@ __device__ __forceinline__ void group_mask(const FwdArgs& a, int lane, float (&s
 
 // Registers per thread: 64 keeps 32 warps per SM; the compact-output kernels
 // at 512 experts get 80 (25 warps), which spills much less, except fp32 rows
-// of exactly 512 experts without bias or groups, which fit 64.
+// of exactly 512 experts without bias or groups, which fit 64.  Rows of at
+// most 256 experts without bias or groups get 48 (42 warps): at 8192 x 256,
+// K = 8, the top-K forward took 6.46 against 6.57 us (fp32 softmax) and 6.53
+// against 7.01 us (bf16 sigmoid), with a few bytes of spills in the aux-score
+// kernels only.
 template <int NC, int OP, int KM, bool FULL, int DT>
 constexpr int reg_max_regs() {
+  if (NC == 2 && KM == 0) return 48;
   return (NC == 4 && OP == 2 && !(KM == 0 && FULL && DT == DT_F32)) ? 80 : 64;
 }
 
